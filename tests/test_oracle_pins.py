@@ -1,0 +1,373 @@
+"""Pins for the CPU oracle: checks against facts that do not come from the oracle.
+
+Each test compares the oracle with one of: a value the pages print (fixtures in
+tests/golden/, each carrying its citation), a closed form, an algebraic identity
+the pages state, or brute force in exact Python integers / rationals with float32
+rounding done by ``struct`` (independent of numpy's float32 arithmetic). They are
+chosen so that a dropped term, a wrong sign or index, or a transposed operand in
+the oracle fails at least one of them.
+"""
+import json
+import math
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from oracle import qmm_oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+# --- independent float helpers (no numpy float32 arithmetic) ---------------
+
+def f32(x: float) -> float:
+    """Round a Python float (double) to the nearest float32, ties to even."""
+    return struct.unpack("<f", struct.pack("<f", x))[0]
+
+
+def f32_from_bits(bits: int) -> float:
+    return struct.unpack("<f", struct.pack("<I", bits))[0]
+
+
+def bf16_round_value(v: float) -> float:
+    """Nearest bf16 value (8 significant bits), ties to even, via frexp + round()."""
+    if v == 0.0:
+        return 0.0
+    m, e = math.frexp(v)          # v = m * 2**e with 0.5 <= |m| < 1
+    r = round(m * 256)            # Python's round() breaks ties to even
+    return math.ldexp(r, e - 8)
+
+
+def bf16_bits_value(bits: int) -> float:
+    return f32_from_bits(int(bits) << 16)
+
+
+# ---------------------------------------------------------------------------
+# number formats
+# ---------------------------------------------------------------------------
+
+def test_wrap_int32_closed_form():
+    vals = np.array([0, 2**31 - 1, 2**31, -2**31, -2**31 - 1, 2**32 + 5, 65025 * 34816], np.int64)
+    got = O.wrap_int32(vals)
+    want = [0, 2**31 - 1, -2**31, -2**31, 2**31 - 1, 5, 65025 * 34816 - 2**32]
+    assert got.tolist() == want
+
+
+def test_bf16_rounding_specials():
+    one = 1.0
+    cases = {
+        one: 0x3F80,
+        one + 2**-8: 0x3F80,               # tie, kept part even -> stays
+        one + 3 * 2**-8: 0x3F82,           # tie, kept part odd -> rounds up
+        one + 2**-8 + 2**-20: 0x3F81,      # just above the tie
+        -(one + 2**-8): 0xBF80,
+        255.0: 0x437F,
+        257.0: 0x4380,                     # 256 + 1: tie at ulp 2 -> even (256)
+        259.0: 0x4382,                     # tie -> even (260)
+    }
+    x = np.array(list(cases.keys()), np.float32)
+    got = O.f32_to_bf16_bits(x)
+    assert [int(g) for g in got] == list(cases.values())
+
+
+def test_bf16_rounding_bruteforce():
+    rng = np.random.default_rng(1)
+    x = (rng.standard_normal(4000) * np.exp(rng.uniform(-20, 20, 4000))).astype(np.float32)
+    got = O.f32_to_bf16_bits(x)
+    for xi, gi in zip(x.tolist(), got.tolist()):
+        assert bf16_bits_value(gi) == bf16_round_value(xi)
+
+
+# ---------------------------------------------------------------------------
+# form (a): factored int8-weight dequant matmul
+# ---------------------------------------------------------------------------
+
+def _w8_case(seed, M, K, N, per_column):
+    rng = np.random.default_rng(seed)
+    A = rng.uniform(-1, 1, (M, K)).astype(np.float32)
+    B = rng.integers(-128, 128, (K, N), dtype=np.int8)
+    if per_column:
+        scale = rng.uniform(0.001, 0.05, N).astype(np.float32)
+        zp = rng.integers(-20, 20, N).astype(np.int32)
+    else:
+        scale = np.array([0.02], np.float32)
+        zp = np.array([3], np.int32)
+    return A, B, scale, zp
+
+
+@pytest.mark.parametrize("per_column", [False, True])
+def test_w8_bruteforce_unfactored_rationals(per_column):
+    """Exact rational sum of a_k * (b_k - zp) * scale, the unfactored dequantisation."""
+    A, B, scale, zp = _w8_case(2, 3, 9, 4, per_column)
+    got = O.w8_dequant(A, B, scale, zp)
+    M, K = A.shape
+    N = B.shape[1]
+    for m in range(M):
+        for n in range(N):
+            s = Fraction(float(scale[n if per_column else 0]))
+            z = int(zp[n if per_column else 0])
+            exact = sum(Fraction(float(A[m, k])) * (int(B[k, n]) - z) * s for k in range(K))
+            assert abs(got[m, n] - float(exact)) <= 1e-12 * (1 + abs(float(exact)))
+
+
+@pytest.mark.parametrize("per_column", [False, True])
+def test_w8_factoring_identity_vs_explicit_dequant(per_column):
+    """The factored form equals dequantise-then-matmul (the identity the kernel rests on)."""
+    A, B, scale, zp = _w8_case(3, 17, 130, 23, per_column)
+    fused = O.w8_dequant(A, B, scale, zp)
+    explicit = O.w8_dequant_explicit(A, B, scale, zp)
+    mag = np.abs(A).astype(np.float64) @ np.abs(B).astype(np.float64) + 1.0
+    assert np.all(np.abs(fused - explicit) <= 1e-12 * mag)
+
+
+def test_w8_zero_point_zero_is_plain_matmul():
+    A, B, _, _ = _w8_case(4, 5, 33, 6, False)
+    got = O.w8_dequant(A, B, [0.5], [0])
+    M, K = A.shape
+    for m in range(M):
+        for n in range(B.shape[1]):
+            exact = sum(Fraction(float(A[m, k])) * int(B[k, n]) for k in range(K)) * Fraction(1, 2)
+            assert abs(got[m, n] - float(exact)) <= 1e-12 * (1 + abs(float(exact)))
+
+
+def test_w8_error_bound_shape_and_value():
+    A = np.array([[1.0, -2.0]], np.float32)
+    B = np.array([[3], [-4]], np.int8)
+    bound = O.w8_dequant_error_bound(A, B, [0.5], [1])
+    # |1|*|0.5*(3-1)| + |-2|*|0.5*(-4-1)| = 1 + 5 = 6
+    assert bound.shape == (1, 1)
+    assert abs(bound[0, 0] - (1e-3 * 6 + 1e-6)) < 1e-15
+
+
+# ---------------------------------------------------------------------------
+# form (b): A8W8
+# ---------------------------------------------------------------------------
+
+def test_a8w8_bruteforce_python_ints_and_struct_f32():
+    rng = np.random.default_rng(5)
+    M, K, N = 4, 37, 5
+    A = rng.integers(-127, 128, (M, K), dtype=np.int8)
+    B = rng.integers(-127, 128, (K, N), dtype=np.int8)
+    a_s = rng.uniform(0.005, 0.02, M).astype(np.float32)
+    w_s = rng.uniform(0.001, 0.01, N).astype(np.float32)
+    got32 = O.a8w8(A, B, a_s, w_s, "f32")
+    got16 = O.a8w8(A, B, a_s, w_s, "bf16")
+    for m in range(M):
+        for n in range(N):
+            acc = sum(int(A[m, k]) * int(B[k, n]) for k in range(K))
+            f = f32(float(acc))
+            f = f32(f * float(a_s[m]))
+            f = f32(f * float(w_s[n]))
+            assert float(got32[m, n]) == f
+            assert bf16_bits_value(got16[m, n]) == bf16_round_value(f)
+
+
+def test_a8w8_scale_orientation_golden():
+    g = golden("a8w8_scale_orientation.json")
+    M, N = g["M"], g["N"]
+    A = np.eye(M, dtype=np.int8)
+    B = np.ones((M, N), np.int8)
+    got = O.a8w8(A, B, np.array(g["act_scale"], np.float32), np.array(g["weight_scale"], np.float32))
+    assert got.tolist() == g["expected_f32"]
+
+
+def test_a8w8_scalar_scales_broadcast():
+    A = np.array([[1, 2], [3, 4]], np.int8)
+    B = np.array([[1, 0], [0, 1]], np.int8)
+    got = O.a8w8(A, B, [0.5], [2.0])
+    assert got.tolist() == [[1.0, 2.0], [3.0, 4.0]]
+
+
+def test_a8w8_acc_wraps():
+    K = 131073                      # 16384 * K > 2^31
+    A = np.full((1, K), -128, np.int8)
+    B = np.full((K, 1), -128, np.int8)
+    assert int(O.a8w8_acc(A, B)[0, 0]) == 16384 * K - 2**32
+
+
+def test_a8w8_error_bound_value():
+    A = np.array([[2, -3]], np.int8)
+    B = np.array([[5], [7]], np.int8)
+    b = O.a8w8_error_bound(A, B, [0.5], [0.25])
+    assert abs(b[0, 0] - (1e-3 * (10 + 21) * 0.125 + 1e-6)) < 1e-15
+
+
+# ---------------------------------------------------------------------------
+# form (c): MatMulInteger
+# ---------------------------------------------------------------------------
+
+def test_matmul_integer_page_value_len259():
+    g = golden("matmul_integer_u8_len259.json")
+    K = g["K"]
+    A = np.full((1, K), g["a_value"], np.uint8)
+    B = np.full((K, 1), g["b_value"], np.uint8)
+    got = O.matmul_integer(A, B, g["a_zero_point"], g["b_zero_point"])
+    assert int(got[0, 0]) == g["expected"]
+
+
+def test_f32_accumulation_threshold_of_the_page():
+    """65025*K fits the 24-bit significand only up to K=258, so float32 cannot hold the 259 sum."""
+    assert 65025 * 258 < 2**24 <= 65025 * 259
+    acc = np.float32(0)
+    for _ in range(259):
+        acc = np.float32(acc + np.float32(65025))
+    assert int(acc) != 16841475
+
+
+def test_matmul_integer_max_magnitude_product():
+    K = 3
+    A = np.full((1, K), 255, np.uint8)
+    B = np.full((K, 1), -128, np.int8)
+    assert int(O.matmul_integer(A, B, 0, 127)[0, 0]) == -65025 * K
+
+
+def test_matmul_integer_wrap_k34816():
+    K = 34816
+    A = np.full((1, K), 255, np.uint8)
+    B = np.full((K, 2), 255, np.uint8)
+    got = O.matmul_integer(A, B)
+    assert got.tolist() == [[65025 * K - 2**32] * 2]
+
+
+@pytest.mark.parametrize("adt,bdt", [(np.uint8, np.int8), (np.int8, np.int8), (np.uint8, np.uint8), (np.int8, np.uint8)])
+def test_matmul_integer_bruteforce(adt, bdt):
+    rng = np.random.default_rng(6)
+    M, K, N = 3, 11, 4
+    info_a, info_b = np.iinfo(adt), np.iinfo(bdt)
+    A = rng.integers(info_a.min, info_a.max + 1, (M, K)).astype(adt)
+    B = rng.integers(info_b.min, info_b.max + 1, (K, N)).astype(bdt)
+    a_zp = rng.integers(info_a.min, info_a.max + 1, M).astype(adt)      # per row
+    b_zp = rng.integers(info_b.min, info_b.max + 1, N).astype(bdt)      # per column
+    got = O.matmul_integer(A, B, a_zp, b_zp)
+    for m in range(M):
+        for n in range(N):
+            s = sum((int(A[m, k]) - int(a_zp[m])) * (int(B[k, n]) - int(b_zp[n])) for k in range(K))
+            assert int(got[m, n]) == s
+
+
+def test_matmul_integer_direct_equals_expanded_mod_2_32():
+    """sum (a-za)(b-zb) == sum ab - za*colsum(B) - zb*rowsum(A) + K*za*zb (mod 2^32)."""
+    rng = np.random.default_rng(7)
+    M, K, N = 6, 300, 9
+    A = rng.integers(0, 256, (M, K)).astype(np.uint8)
+    B = rng.integers(-128, 128, (K, N)).astype(np.int8)
+    za = 131
+    zb = rng.integers(-128, 128, N).astype(np.int8)
+    got = O.matmul_integer(A, B, za, zb)
+    for m in range(M):
+        for n in range(N):
+            ab = sum(int(A[m, k]) * int(B[k, n]) for k in range(K))
+            rs = sum(int(A[m, k]) for k in range(K))
+            cs = sum(int(B[k, n]) for k in range(K))
+            e = ab - za * cs - int(zb[n]) * rs + K * za * int(zb[n])
+            e = (e + 2**31) % 2**32 - 2**31
+            assert int(got[m, n]) == e
+
+
+def test_matmul_integer_shared_b_equals_per_batch_copies():
+    rng = np.random.default_rng(8)
+    A = rng.integers(-128, 128, (2, 3, 4, 40)).astype(np.int8)
+    B = rng.integers(-128, 128, (40, 5)).astype(np.int8)
+    shared = O.matmul_integer(A, B, -5, 7)
+    copied = O.matmul_integer(A, np.broadcast_to(B, (2, 3, 40, 5)).copy(), -5, 7)
+    assert shared.shape == (2, 3, 4, 5)
+    assert np.array_equal(shared, copied)
+    # and each batch equals its own rank-2 product
+    for i in range(2):
+        for j in range(3):
+            assert np.array_equal(shared[i, j], O.matmul_integer(A[i, j], B, -5, 7))
+
+
+def test_matmul_integer_zero_points_zero_is_a8w8_acc():
+    rng = np.random.default_rng(9)
+    A = rng.integers(-127, 128, (5, 70)).astype(np.int8)
+    B = rng.integers(-127, 128, (70, 6)).astype(np.int8)
+    assert np.array_equal(O.matmul_integer(A, B, 0, 0), O.a8w8_acc(A, B))
+    for m in range(5):
+        for n in range(6):
+            assert int(O.a8w8_acc(A, B)[m, n]) == sum(int(A[m, k]) * int(B[k, n]) for k in range(70))
+
+
+# ---------------------------------------------------------------------------
+# form (d): DynamicQuantizeLinear
+# ---------------------------------------------------------------------------
+
+def test_dql_all_zero_golden():
+    g = golden("dql_all_zero.json")
+    y, s, zp = O.dynamic_quantize_linear(np.array(g["x"], np.float32))
+    assert float(s) == g["scale"] and int(zp) == g["zero_point"]
+    assert y.tolist() == g["y"]
+
+
+def test_dql_empty_input():
+    y, s, zp = O.dynamic_quantize_linear(np.zeros(0, np.float32))
+    assert float(s) == 1.0 and int(zp) == 0 and y.size == 0
+
+
+def test_dql_hand_worked_golden():
+    g = golden("dql_hand_worked.json")
+    y, s, zp = O.dynamic_quantize_linear(np.array(g["x"], np.float32))
+    assert int(np.float32(s).view(np.uint32)) == g["scale_f32_bits"]
+    assert int(zp) == g["zero_point"]
+    assert y.tolist() == g["y"]
+
+
+def test_dql_ties_to_even_golden():
+    g = golden("dql_ties.json")
+    y, s, zp = O.dynamic_quantize_linear(np.array(g["x"], np.float32))
+    assert float(s) == g["scale"] and int(zp) == g["zero_point"]
+    assert y.tolist() == g["y"]
+
+
+def test_dql_one_sided_golden():
+    for c in golden("dql_one_sided.json")["cases"]:
+        y, _, zp = O.dynamic_quantize_linear(np.array(c["x"], np.float32))
+        assert int(zp) == c["zero_point"]
+        assert y.tolist() == c["y"]
+
+
+def test_quantize_linear_saturates():
+    y = O.quantize_linear(np.array([1000.0, -1000.0, 3.0, 10.0], np.float32), np.float32(1.0), 0)
+    assert y.tolist() == [255, 0, 3, 10]
+    y = O.quantize_linear(np.array([10.0, -300.0], np.float32), np.float32(1.0), 250)
+    assert y.tolist() == [255, 0]
+
+
+def test_dql_bruteforce_struct_f32():
+    rng = np.random.default_rng(10)
+    for trial in range(20):
+        n = int(rng.integers(1, 300))
+        x = rng.standard_normal(n).astype(np.float32)
+        x[rng.random(n) < 0.05] *= np.float32(20)
+        if trial % 5 == 1:
+            x = np.abs(x)
+        if trial % 5 == 2:
+            x = -np.abs(x)
+        y, s, zp = O.dynamic_quantize_linear(x)
+        xs = [float(v) for v in x]
+        lo = min(0.0, min(xs))
+        hi = max(0.0, max(xs))
+        r = f32(hi - lo)
+        scale = 1.0 if r == 0.0 else f32(r / 255.0)
+        z = min(255, max(0, round(f32(-lo / scale))))
+        assert float(s) == scale and int(zp) == z
+        want = [min(255, max(0, round(f32(v / scale)) + z)) for v in xs]
+        assert y.tolist() == want
+
+
+def test_row_and_col_sums_bruteforce():
+    rng = np.random.default_rng(11)
+    y = rng.integers(0, 256, 4 * 13).astype(np.uint8)
+    rs = O.row_sums(y, 13)
+    assert rs.tolist() == [sum(int(v) for v in y[i * 13:(i + 1) * 13]) for i in range(4)]
+    B = rng.integers(-128, 128, (9, 5)).astype(np.int8)
+    cs = O.col_sums(B)
+    assert cs.tolist() == [sum(int(B[k, n]) for k in range(9)) for n in range(5)]
