@@ -1,0 +1,191 @@
+/*
+ * qmm.h -- C ABI of the GB300 (sm_103a) integer-quantised matmul library.
+ *
+ * Four operations, each an integer matmul whose dequantisation is fused into
+ * the kernel so that no dequantised (float) copy of a quantised operand is
+ * ever written to memory:
+ *   qmm_w8_dequant           float activations x int8 weight, scale/zero point
+ *   qmm_a8w8                 int8 x int8 -> exact int32 -> row/column scales
+ *   matmul_integer           ONNX MatMulInteger with zero points, shared B
+ *   dynamic_quantize_linear  ONNX DynamicQuantizeLinear to uint8
+ *
+ * Conventions for every entry point:
+ *  - Tensors are caller-owned DEVICE pointers, row-major and contiguous in the
+ *    last dimension, on the current CUDA device. The library never allocates
+ *    device or host memory and never takes ownership.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and runs asynchronously; the call returns after the launch.
+ *  - Scales and zero points are device pointers too, so a chain of calls
+ *    (e.g. dynamic_quantize_linear then matmul_integer) needs no host sync.
+ *  - Arguments are validated before anything is launched; an invalid call
+ *    returns QMM_ERR_INVALID_ARG (malformed) or QMM_ERR_UNSUPPORTED (well
+ *    formed but outside what the kernels implement) and enqueues nothing.
+ *  - The CUDA last-error state is cleared before each launch and read after
+ *    it; a launch failure returns QMM_ERR_CUDA (qmm_last_cuda_error() gives
+ *    the cudaError_t value).
+ *  - Kernels never trap or spin without bound. A device-side wait that runs
+ *    out (about one second) records a code in a device error word and the
+ *    kernel returns; qmm_check_device_error() reports it as QMM_ERR_TIMEOUT.
+ *  - Integer results wrap modulo 2^32 (two's complement); nothing saturates
+ *    except the uint8 outputs of dynamic_quantize_linear.
+ *  - Shapes use int64_t; each dimension must fit in int32 (< 2^31).
+ *
+ * The operations follow five public web pages; each declaration names the
+ * page (title) and the section it implements.
+ */
+#ifndef QMM_H
+#define QMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  QMM_OK = 0,
+  QMM_ERR_INVALID_ARG = 1,
+  QMM_ERR_UNSUPPORTED = 2,
+  QMM_ERR_CUDA = 3,
+  QMM_ERR_TIMEOUT = 4
+} qmm_status;
+
+/* Element types (values of the *_dtype arguments). */
+typedef enum {
+  QMM_F32 = 0,
+  QMM_BF16 = 1,
+  QMM_S8 = 2,
+  QMM_U8 = 3,
+  QMM_S32 = 4
+} qmm_dtype;
+
+/*
+ * Form (a): int8-weight matmul with the affine dequantisation factored out.
+ * TrainDeeploy PR #53, "feat(PULPOpen): matmul that dequantises an int8
+ * weight in-kernel", section "The kernel":
+ *     C[m,n] = scale_n * ( sum_k A[m,k]*B[k,n]  -  zp_n * sum_k A[m,k] )
+ * i.e. sum_k A[m,k] * scale_n*(B[k,n] - zp_n) with one correction multiply per
+ * output instead of one per multiply-accumulate.
+ *
+ *  A           [M,K] activations, a_dtype QMM_F32 or QMM_BF16
+ *  B           [K,N] int8 weight
+ *  scale       device float[scale_count], scale_count 1 (per tensor) or N (per column)
+ *  zero_point  device int32[zp_count], zp_count 0 (no zero point), 1 or N; may be
+ *              NULL when zp_count is 0
+ *  C           [M,N] output, c_dtype QMM_F32 or QMM_BF16 (round to nearest even)
+ * Kernels: for bf16 A with 1 <= M <= 16 (the decode shape; K % 4 == 0,
+ * N % 16 == 0, A 8-byte and B 16-byte aligned) a weight-streaming tensor-core
+ * GEMV; otherwise a CUDA-core tiled kernel. Accumulation is fp32.
+ * Accuracy: |C - exact| <= 1e-3 * sum_k |A[m,k]*scale_n*(B[k,n]-zp_n)| + 1e-6,
+ * plus half an ulp of the output type.
+ */
+qmm_status qmm_w8_dequant(const void* A, int a_dtype, const int8_t* B, int64_t M, int64_t K, int64_t N,
+                          const float* scale, int64_t scale_count, const int32_t* zero_point, int64_t zp_count,
+                          void* C, int c_dtype, void* stream);
+
+/*
+ * Form (b): A8W8 matmul-dequant. PyPTO PR #1920, "Feature/a8w8 matmul dequant
+ * fusion", the walkthrough's sequence diagram (INT8 matmul into an INT32
+ * accumulator, cast to FP32, act_scale on rows, weight_scale on columns, cast
+ * to out_dtype) and the review comments on 1-D scales ([M] scales rows,
+ * [N] scales columns, never a last-dimension broadcast):
+ *     acc = sum_k A[m,k]*B[k,n]              (exact, int32, wrapping)
+ *     C   = out( ((float)acc * act_scale[m]) * weight_scale[n] )
+ * each float step a single fp32 multiply rounded to nearest even.
+ *
+ *  A             [M,K] int8;  B [K,N] int8
+ *  act_scale     device float[act_count], act_count 1 (scalar) or M
+ *  weight_scale  device float[w_count], w_count 1 or N
+ *  C             [M,N], c_dtype QMM_F32 or QMM_BF16
+ * Kernel: exact integer GEMM on the tcgen05 tensor cores with the scaling in
+ * the epilogue. sm_103a has no 8-bit integer MMA kind, so the product runs on
+ * fp16 copies of the bytes (exact) in K-chunks short enough for the fp32
+ * accumulator to stay exact, drained into an int32 sum. Results are
+ * bit-identical to the float32 chain above.
+ */
+qmm_status qmm_a8w8(const int8_t* A, const int8_t* B, int64_t M, int64_t K, int64_t N, const float* act_scale,
+                    int64_t act_count, const float* weight_scale, int64_t w_count, void* C, int c_dtype,
+                    void* stream);
+
+/*
+ * Form (c): MatMulInteger with zero points. ROCm hip-ep PR #1248,
+ * "feat(onnx-to-hip): lower quantized integer conv and matmul", section
+ * "What", MatMulInteger paragraph:
+ *     C[b,m,n] = sum_k (A[b,m,k] - a_zp) * (B[b,k,n] - b_zp)     (int32, wrapping)
+ * ranks 2-4 with the batch dimensions flattened into `batch` by the caller;
+ * a rank-2 B (or one whose batch dims are all 1) is one matrix shared by all
+ * batches: pass b_batch_stride = 0. A size-1 batch on A is expanded: pass
+ * a_batch_stride = 0.
+ *
+ *  A               [batch][M][K] 8-bit, a_dtype QMM_S8 or QMM_U8
+ *  B               [batch][K][N] 8-bit, b_dtype QMM_S8 or QMM_U8
+ *  a_batch_stride  elements between A batches (M*K for a dense batch, 0 = broadcast)
+ *  b_batch_stride  elements between B batches (K*N, or 0 = shared rank-2 B)
+ *  a_zero_point    device array of a_dtype: a_zp_count 0 (none), 1 (scalar) or M (per row)
+ *  b_zero_point    device array of b_dtype: b_zp_count 0, 1 or N (per column)
+ *  C               [batch][M][N] int32, contiguous
+ * Computed as sum ab - a_zp*colsum(B) - b_zp*rowsum(A) + K*a_zp*b_zp, exact
+ * modulo 2^32, with the row/column sums taken in the same pass as the product.
+ */
+qmm_status matmul_integer(const void* A, int a_dtype, const void* B, int b_dtype, int64_t batch, int64_t M,
+                          int64_t K, int64_t N, int64_t a_batch_stride, int64_t b_batch_stride,
+                          const void* a_zero_point, int64_t a_zp_count, const void* b_zero_point,
+                          int64_t b_zp_count, int32_t* C, void* stream);
+
+/*
+ * Form (d): DynamicQuantizeLinear, uint8 only. ROCm hip-ep PR #1248, section
+ * "What", DynamicQuantizeLinear paragraph (reduce to a scalar min and max,
+ * scale (max-min)/255 with a zero range selecting scale 1, ties-to-even zero
+ * point, quantize), with the range widened to include 0:
+ *     lo = min(0, min x); hi = max(0, max x)
+ *     scale = (hi - lo) == 0 ? 1 : (hi - lo) / 255
+ *     zp    = sat_u8(rne(-lo / scale))
+ *     y     = sat_u8(rne(x / scale) + zp)
+ * every step one IEEE fp32 operation (true division), ties to even.
+ *
+ *  x             [n] float32 (NaN/Inf inputs are outside the domain: undefined)
+ *  y             [n] uint8 output
+ *  y_scale       device float[1] output
+ *  y_zero_point  device uint8[1] output
+ *  row_sums      optional device int32[n / row_len]: the sum of each run of
+ *                row_len elements of y (the rowsum(A) of a following
+ *                matmul_integer); NULL to skip. Requires n % row_len == 0.
+ *  workspace     device scratch of at least
+ *                dynamic_quantize_linear_workspace_bytes(n) bytes, 16-byte
+ *                aligned, caller-owned; its contents on entry do not matter.
+ * n == 0 writes scale 1 and zero point 0.
+ */
+size_t dynamic_quantize_linear_workspace_bytes(int64_t n);
+qmm_status dynamic_quantize_linear(const float* x, int64_t n, uint8_t* y, float* y_scale, uint8_t* y_zero_point,
+                                   int32_t* row_sums, int64_t row_len, void* workspace, size_t workspace_bytes,
+                                   void* stream);
+
+/* Human-readable name of a status. Never NULL. */
+const char* qmm_status_string(int status);
+
+/* Name of the kernel(s) the last successful call on this host thread launched
+ * (a test hook: it shows which path actually ran). Never NULL. */
+const char* qmm_last_kernel(void);
+
+/* cudaError_t of the last call that returned QMM_ERR_CUDA on this thread. */
+int qmm_last_cuda_error(void);
+
+/* Synchronise `stream`, then read and clear the device error word of the
+ * current device: QMM_OK if no kernel timed out since the last check,
+ * QMM_ERR_TIMEOUT if one did (qmm_last_device_error() gives its site code),
+ * QMM_ERR_CUDA if the synchronisation failed. */
+qmm_status qmm_check_device_error(void* stream);
+unsigned qmm_last_device_error(void);
+
+/* Number of streaming multiprocessors of the current device (0 on error). */
+int qmm_num_sms(void);
+
+/* ABI version of this header: 1. */
+int qmm_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QMM_H */

@@ -1,0 +1,240 @@
+"""Python binding of the GB300 integer-quantised matmul library (libqmm.so).
+
+Argument marshalling only: each function checks dtypes/shapes of torch
+tensors, passes raw device pointers, sizes and the current CUDA stream to the
+C ABI of the same name (include/qmm.h), and raises ``QmmError`` on a non-OK
+status. Every step of the computation runs in the library's CUDA kernels;
+there is no CPU or PyTorch fallback. Output tensors are allocated with torch
+when the caller does not pass one (device memory is PyTorch's job here).
+
+If the shared library is missing it is built from ``csrc/`` with nvcc on
+first import; if that fails the import fails loudly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+QMM_OK, QMM_ERR_INVALID_ARG, QMM_ERR_UNSUPPORTED, QMM_ERR_CUDA, QMM_ERR_TIMEOUT = range(5)
+QMM_F32, QMM_BF16, QMM_S8, QMM_U8, QMM_S32 = range(5)
+
+_TORCH_TO_QMM = {
+    torch.float32: QMM_F32,
+    torch.bfloat16: QMM_BF16,
+    torch.int8: QMM_S8,
+    torch.uint8: QMM_U8,
+    torch.int32: QMM_S32,
+}
+
+
+class QmmError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        detail = ""
+        if status == QMM_ERR_CUDA:
+            detail = f" (cudaError {_lib.qmm_last_cuda_error()})"
+        if status == QMM_ERR_TIMEOUT:
+            detail = f" (device error site 0x{_lib.qmm_last_device_error():x})"
+        super().__init__(f"{fn}: {_lib.qmm_status_string(status).decode()}{detail}")
+
+
+def _load() -> ctypes.CDLL:
+    path = _build.build()
+    lib = ctypes.CDLL(path)
+    i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+    lib.qmm_w8_dequant.argtypes = [vp, ci, vp, i64, i64, i64, vp, i64, vp, i64, vp, ci, vp]
+    lib.qmm_a8w8.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, i64, vp, ci, vp]
+    lib.matmul_integer.argtypes = [vp, ci, vp, ci, i64, i64, i64, i64, i64, i64, vp, i64, vp, i64, vp, vp]
+    lib.dynamic_quantize_linear_workspace_bytes.argtypes = [i64]
+    lib.dynamic_quantize_linear_workspace_bytes.restype = ctypes.c_size_t
+    lib.dynamic_quantize_linear.argtypes = [vp, i64, vp, vp, vp, vp, i64, vp, ctypes.c_size_t, vp]
+    for fn in ("qmm_w8_dequant", "qmm_a8w8", "matmul_integer", "dynamic_quantize_linear"):
+        getattr(lib, fn).restype = ci
+    lib.qmm_status_string.argtypes = [ci]
+    lib.qmm_status_string.restype = ctypes.c_char_p
+    lib.qmm_last_kernel.restype = ctypes.c_char_p
+    lib.qmm_last_cuda_error.restype = ci
+    lib.qmm_last_device_error.restype = ctypes.c_uint
+    lib.qmm_check_device_error.argtypes = [vp]
+    lib.qmm_check_device_error.restype = ci
+    lib.qmm_num_sms.restype = ci
+    lib.qmm_abi_version.restype = ci
+    return lib
+
+
+_lib = _load()
+LIB_PATH = _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn: str, status: int):
+    if status != QMM_OK:
+        raise QmmError(fn, status)
+
+
+def _need(t, dtypes, name):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def last_kernel() -> str:
+    """Name of the kernel(s) the last successful call on this thread launched."""
+    return _lib.qmm_last_kernel().decode()
+
+
+def check_device_error(stream=None) -> None:
+    """Synchronise the stream and raise if a kernel recorded a timed-out wait."""
+    _check("qmm_check_device_error", _lib.qmm_check_device_error(_stream(stream)))
+
+
+def qmm_w8_dequant(A, B, scale, zero_point=None, out=None, out_dtype=torch.float32, stream=None):
+    """Form (a): C = scale_n * (A @ B - zp_n * rowsum(A)); A f32/bf16 [M,K], B int8 [K,N]."""
+    _need(A, (torch.float32, torch.bfloat16), "A")
+    _need(B, (torch.int8,), "B")
+    _need(scale, (torch.float32,), "scale")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ")
+    zp_count = 0
+    if zero_point is not None:
+        _need(zero_point, (torch.int32,), "zero_point")
+        zp_count = zero_point.numel()
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    _need(out, (torch.float32, torch.bfloat16), "out")
+    st = _lib.qmm_w8_dequant(_ptr(A), _TORCH_TO_QMM[A.dtype], _ptr(B), M, K, N, _ptr(scale), scale.numel(),
+                             _ptr(zero_point), zp_count, _ptr(out), _TORCH_TO_QMM[out.dtype], _stream(stream))
+    _check("qmm_w8_dequant", st)
+    return out
+
+
+def qmm_a8w8(A, B, act_scale, weight_scale, out=None, out_dtype=torch.bfloat16, stream=None):
+    """Form (b): C = out(f32(A @ B) * act_scale[m] * weight_scale[n]); A, B int8."""
+    _need(A, (torch.int8,), "A")
+    _need(B, (torch.int8,), "B")
+    _need(act_scale, (torch.float32,), "act_scale")
+    _need(weight_scale, (torch.float32,), "weight_scale")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    _need(out, (torch.float32, torch.bfloat16), "out")
+    st = _lib.qmm_a8w8(_ptr(A), _ptr(B), M, K, N, _ptr(act_scale), act_scale.numel(), _ptr(weight_scale),
+                       weight_scale.numel(), _ptr(out), _TORCH_TO_QMM[out.dtype], _stream(stream))
+    _check("qmm_a8w8", st)
+    return out
+
+
+def matmul_integer(A, B, a_zero_point=None, b_zero_point=None, out=None, stream=None):
+    """Form (c): int32 C = (A - a_zp) @ (B - b_zp), A [...,M,K], B [K,N] (shared) or [...,K,N]."""
+    _need(A, (torch.int8, torch.uint8), "A")
+    _need(B, (torch.int8, torch.uint8), "B")
+    if A.dim() < 2 or A.dim() > 4 or B.dim() < 2 or B.dim() > 4:
+        raise ValueError("MatMulInteger takes ranks 2 to 4")
+    M, K = A.shape[-2:]
+    K2, N = B.shape[-2:]
+    if K2 != K:
+        raise ValueError("inner dimensions differ")
+    a_batch = A.shape[:-2]
+    b_batch = B.shape[:-2]
+    shared_b = all(d == 1 for d in b_batch)
+    batch_shape = torch.broadcast_shapes(a_batch, b_batch)
+    batch = 1
+    for d in batch_shape:
+        batch *= d
+    if shared_b:
+        b_stride = 0
+    elif tuple(b_batch) == tuple(batch_shape):
+        b_stride = K * N
+    else:
+        raise ValueError("B batch dims must be all 1 or equal to the result's batch dims")
+    a_count = 1
+    for d in a_batch:
+        a_count *= d
+    if a_count == 1:
+        a_stride = 0
+    elif tuple(a_batch) == tuple(batch_shape):
+        a_stride = M * K
+    else:
+        raise ValueError("A batch dims must be all 1 or equal to the result's batch dims")
+    az = bz = 0
+    if a_zero_point is not None:
+        _need(a_zero_point, (A.dtype,), "a_zero_point")
+        az = a_zero_point.numel()
+    if b_zero_point is not None:
+        _need(b_zero_point, (B.dtype,), "b_zero_point")
+        bz = b_zero_point.numel()
+    if out is None:
+        out = torch.empty((*batch_shape, M, N), dtype=torch.int32, device=A.device)
+    _need(out, (torch.int32,), "out")
+    st = _lib.matmul_integer(_ptr(A), _TORCH_TO_QMM[A.dtype], _ptr(B), _TORCH_TO_QMM[B.dtype], batch, M, K, N,
+                             a_stride, b_stride, _ptr(a_zero_point), az, _ptr(b_zero_point), bz, _ptr(out),
+                             _stream(stream))
+    _check("matmul_integer", st)
+    return out
+
+
+def dynamic_quantize_linear_workspace_bytes(n: int) -> int:
+    return int(_lib.dynamic_quantize_linear_workspace_bytes(n))
+
+
+def dynamic_quantize_linear(x, row_len=None, workspace=None, y=None, stream=None):
+    """Form (d): (y uint8, y_scale f32[1], y_zero_point u8[1][, row_sums int32]) of float32 x.
+
+    With row_len, also returns the sum of each run of row_len elements of y."""
+    _need(x, (torch.float32,), "x")
+    n = x.numel()
+    dev = x.device
+    if y is None:
+        y = torch.empty(x.shape, dtype=torch.uint8, device=dev)
+    y_scale = torch.empty(1, dtype=torch.float32, device=dev)
+    y_zp = torch.empty(1, dtype=torch.uint8, device=dev)
+    ws_bytes = dynamic_quantize_linear_workspace_bytes(n)
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    row_sums = None
+    rl = 0
+    if row_len is not None:
+        rl = int(row_len)
+        row_sums = torch.empty(n // rl if rl > 0 else 0, dtype=torch.int32, device=dev)
+    st = _lib.dynamic_quantize_linear(_ptr(x), n, _ptr(y), _ptr(y_scale), _ptr(y_zp), _ptr(row_sums), rl,
+                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _stream(stream))
+    _check("dynamic_quantize_linear", st)
+    if row_sums is not None:
+        return y, y_scale, y_zp, row_sums
+    return y, y_scale, y_zp
+
+
+def num_sms() -> int:
+    return int(_lib.qmm_num_sms())
+
+
+__all__ = [
+    "qmm_w8_dequant", "qmm_a8w8", "matmul_integer", "dynamic_quantize_linear",
+    "dynamic_quantize_linear_workspace_bytes", "last_kernel", "check_device_error", "QmmError", "lib",
+    "num_sms", "LIB_PATH",
+]

@@ -1,0 +1,239 @@
+// DynamicQuantizeLinear to uint8, as lowered in ROCm hip-ep PR #1248
+// ("feat(onnx-to-hip): lower quantized integer conv and matmul", section
+// "What", DynamicQuantizeLinear paragraph): reduce the input to a scalar
+// minimum and maximum, take scale = (max - min)/255 (scale 1 when the range is
+// zero) and a ties-to-even zero point, then quantize.
+//
+// The range includes 0: lo = min(0, min x), hi = max(0, max x), which keeps
+// zero exactly representable and the zero point inside [0, 255].
+// Every float step is a single IEEE operation rounded to nearest even:
+//   r = hi - lo; scale = r == 0 ? 1 : r / 255; zp = sat_u8(rne(-lo / scale));
+//   y = sat_u8(rne(x / scale) + zp)
+// with true division (__fdiv_rn), never a reciprocal multiply.
+//
+// Two passes over x (HBM-bound):
+//   pass 1: each CTA reduces a contiguous chunk to a (min, max) partial;
+//   pass 2: every CTA reduces all partials (order-free: min/max are exact),
+//           derives scale and zero point, CTA 0 publishes them, and the grid
+//           quantizes with 16-byte loads and 4-byte stores. Pass 2 walks the
+//           chunks in reverse so its first reads hit what pass 1 left in L2.
+//   Optionally pass 2 also writes the sum of each row of y (row_len elements),
+//   the rowsum(A) a following MatMulInteger needs for its zero-point term.
+#include "common.cuh"
+#include "kernels.h"
+
+#include <algorithm>
+
+namespace qmm {
+namespace dql {
+
+constexpr int THREADS = 256;
+constexpr long long CHUNK_MIN = 32768;   // elements per pass-1 CTA at least
+
+__device__ __forceinline__ void block_minmax(float& lo, float& hi) {
+  __shared__ float slo[THREADS / 32], shi[THREADS / 32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+    hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+  }
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    slo[w] = lo;
+    shi[w] = hi;
+  }
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    lo = threadIdx.x < THREADS / 32 ? slo[threadIdx.x] : 0.f;
+    hi = threadIdx.x < THREADS / 32 ? shi[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+      hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+    }
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ void chunk_range(long long n, int parts, int b, long long& beg, long long& end) {
+  // chunk boundaries on multiples of 4 elements so vector loads stay aligned
+  const long long n4 = (n + 3) / 4;
+  beg = (n4 * b / parts) * 4;
+  end = (n4 * (b + 1) / parts) * 4;
+  if (end > n) end = n;
+  if (beg > n) beg = n;
+}
+
+__global__ void __launch_bounds__(THREADS) dql_minmax_kernel(const float* __restrict__ x, long long n, int vec,
+                                                             float* __restrict__ partials) {
+  long long beg, end;
+  chunk_range(n, gridDim.x, blockIdx.x, beg, end);
+  float lo = 0.f, hi = 0.f;   // the range always includes 0
+  if (vec) {
+    const float4* x4 = reinterpret_cast<const float4*>(x);
+    for (long long i = beg / 4 + threadIdx.x; i < end / 4; i += THREADS) {
+      const float4 v = __ldg(x4 + i);
+      lo = fminf(lo, fminf(fminf(v.x, v.y), fminf(v.z, v.w)));
+      hi = fmaxf(hi, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+    }
+    for (long long i = (end / 4) * 4 + threadIdx.x; i < end; i += THREADS) {
+      const float v = __ldg(x + i);
+      lo = fminf(lo, v);
+      hi = fmaxf(hi, v);
+    }
+  } else {
+    for (long long i = beg + threadIdx.x; i < end; i += THREADS) {
+      const float v = __ldg(x + i);
+      lo = fminf(lo, v);
+      hi = fmaxf(hi, v);
+    }
+  }
+  block_minmax(lo, hi);
+  if (threadIdx.x == 0) {
+    partials[2 * blockIdx.x] = lo;
+    partials[2 * blockIdx.x + 1] = hi;
+  }
+}
+
+struct ScaleZp {
+  float scale;
+  float zp;       // integer-valued, in [0, 255]
+};
+
+__device__ __forceinline__ ScaleZp reduce_partials(const float* __restrict__ partials, int num_partials) {
+  __shared__ ScaleZp s_out;
+  float lo = 0.f, hi = 0.f;
+  for (int i = threadIdx.x; i < num_partials; i += THREADS) {
+    lo = fminf(lo, partials[2 * i]);
+    hi = fmaxf(hi, partials[2 * i + 1]);
+  }
+  block_minmax(lo, hi);
+  if (threadIdx.x == 0) {
+    const float r = __fsub_rn(hi, lo);
+    const float scale = (r == 0.f) ? 1.f : __fdiv_rn(r, 255.f);
+    float zp = rintf(__fdiv_rn(-lo, scale));
+    zp = fminf(fmaxf(zp, 0.f), 255.f);
+    s_out.scale = scale;
+    s_out.zp = zp;
+  }
+  __syncthreads();
+  return s_out;
+}
+
+__device__ __forceinline__ uint32_t quant1(float v, float scale, int zp) {
+  float q = rintf(__fdiv_rn(v, scale));
+  q = fminf(fmaxf(q, -1024.f), 1024.f);   // keeps the int conversion in range; saturation follows
+  int y = __float2int_rn(q) + zp;
+  y = min(max(y, 0), 255);
+  return (uint32_t)y;
+}
+
+__global__ void __launch_bounds__(THREADS) dql_quantize_kernel(const float* __restrict__ x, long long n, int vec,
+                                                               const float* __restrict__ partials,
+                                                               int num_partials, int num_chunks,
+                                                               uint8_t* __restrict__ y, float* y_scale,
+                                                               uint8_t* y_zp) {
+  const ScaleZp sz = reduce_partials(partials, num_partials);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *y_scale = sz.scale;
+    *y_zp = (uint8_t)(int)sz.zp;
+  }
+  const int zp = (int)sz.zp;
+  // reverse chunk order: start where pass 1 finished
+  for (int c = (int)gridDim.x - 1 - (int)blockIdx.x; c >= 0 && c < num_chunks; c -= (int)gridDim.x) {
+    long long beg, end;
+    chunk_range(n, num_chunks, c, beg, end);
+    if (vec) {
+      const float4* x4 = reinterpret_cast<const float4*>(x);
+      uint32_t* y4 = reinterpret_cast<uint32_t*>(y);
+      for (long long i = beg / 4 + threadIdx.x; i < end / 4; i += THREADS) {
+        const float4 v = __ldg(x4 + i);
+        y4[i] = quant1(v.x, sz.scale, zp) | (quant1(v.y, sz.scale, zp) << 8) | (quant1(v.z, sz.scale, zp) << 16) |
+                (quant1(v.w, sz.scale, zp) << 24);
+      }
+      for (long long i = (end / 4) * 4 + threadIdx.x; i < end; i += THREADS)
+        y[i] = (uint8_t)quant1(__ldg(x + i), sz.scale, zp);
+    } else {
+      for (long long i = beg + threadIdx.x; i < end; i += THREADS) y[i] = (uint8_t)quant1(__ldg(x + i), sz.scale, zp);
+    }
+  }
+}
+
+// Quantize whole rows, one warp per row, and write each row's sum of y.
+__global__ void __launch_bounds__(THREADS) dql_quantize_rows_kernel(const float* __restrict__ x, long long rows,
+                                                                    long long row_len, int vec,
+                                                                    const float* __restrict__ partials,
+                                                                    int num_partials, uint8_t* __restrict__ y,
+                                                                    float* y_scale, uint8_t* y_zp,
+                                                                    int32_t* __restrict__ row_sums) {
+  const ScaleZp sz = reduce_partials(partials, num_partials);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *y_scale = sz.scale;
+    *y_zp = (uint8_t)(int)sz.zp;
+  }
+  const int zp = (int)sz.zp;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long total_warps = (long long)gridDim.x * (THREADS / 32);
+  // reverse row order, as in the flat kernel
+  for (long long wr = (long long)(gridDim.x - 1 - blockIdx.x) * (THREADS / 32) + warp; wr < rows;
+       wr += total_warps) {
+    const float* xr = x + wr * row_len;
+    uint8_t* yr = y + wr * row_len;
+    int s = 0;
+    if (vec) {
+      const float4* x4 = reinterpret_cast<const float4*>(xr);
+      uint32_t* y4 = reinterpret_cast<uint32_t*>(yr);
+      for (long long i = lane; i < row_len / 4; i += 32) {
+        const float4 v = __ldg(x4 + i);
+        const uint32_t q0 = quant1(v.x, sz.scale, zp), q1 = quant1(v.y, sz.scale, zp);
+        const uint32_t q2 = quant1(v.z, sz.scale, zp), q3 = quant1(v.w, sz.scale, zp);
+        y4[i] = q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
+        s += (int)(q0 + q1 + q2 + q3);
+      }
+    } else {
+      for (long long i = lane; i < row_len; i += 32) {
+        const uint32_t q = quant1(__ldg(xr + i), sz.scale, zp);
+        yr[i] = (uint8_t)q;
+        s += (int)q;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) row_sums[wr] = s;
+  }
+}
+
+}  // namespace dql
+
+int dql_num_partials(long long n) {
+  long long p = (n + dql::CHUNK_MIN - 1) / dql::CHUNK_MIN;
+  if (p < 1) p = 1;
+  const long long cap = std::min<long long>(kDqlMaxPartials, 4LL * std::max(1, num_sms()));
+  return (int)std::min<long long>(p, cap);
+}
+
+cudaError_t launch_dql(const float* x, long long n, uint8_t* y, float* y_scale, uint8_t* y_zp, int32_t* row_sums,
+                       long long row_len, float* partials, int num_partials, cudaStream_t s,
+                       const char** kernel_name) {
+  using namespace dql;
+  const int vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (reinterpret_cast<uintptr_t>(y) % 4 == 0);
+  dql_minmax_kernel<<<num_partials, THREADS, 0, s>>>(x, n, vec, partials);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (row_sums) {
+    const long long rows = n / row_len;
+    const int rvec = vec && (row_len % 4 == 0);
+    const long long want = (rows + (THREADS / 32) - 1) / (THREADS / 32);
+    const int grid = (int)std::max<long long>(1, std::min<long long>(want, 8LL * num_sms()));
+    *kernel_name = "dql_minmax+dql_quantize_rows";
+    dql_quantize_rows_kernel<<<grid, THREADS, 0, s>>>(x, rows, row_len, rvec, partials, num_partials, y, y_scale,
+                                                       y_zp, row_sums);
+  } else {
+    *kernel_name = "dql_minmax+dql_quantize";
+    dql_quantize_kernel<<<num_partials, THREADS, 0, s>>>(x, n, vec, partials, num_partials, num_partials, y,
+                                                          y_scale, y_zp);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace qmm

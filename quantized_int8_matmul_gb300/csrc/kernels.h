@@ -1,0 +1,76 @@
+// Host-side launch interfaces of the sm_103a kernels (internal to the library).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace qmm {
+
+// ---------------------------------------------------------------------------
+// Exact 8-bit GEMM on tcgen05 (A8W8 and MatMulInteger epilogues).
+// ---------------------------------------------------------------------------
+struct GemmArgs {
+  const uint8_t* A;        // [batch][M][K] 8-bit, row-major
+  const uint8_t* B;        // [batch][K][N] 8-bit, row-major
+  long long a_bstride;     // elements between batches of A (0 = one A for all)
+  long long b_bstride;     // elements between batches of B (0 = shared B)
+  int batch, M, K, N;
+  // epilogue, A8W8: C = bf16/f32( f32(acc) * act_scale[m] * weight_scale[n] )
+  void* C;                 // [batch][M][N]
+  int c_f32;               // A8W8 only: 1 = f32 out, 0 = bf16 out
+  const float* act_scale;  int act_count;   // 1 or M
+  const float* w_scale;    int w_count;     // 1 or N
+  // epilogue, MatMulInteger: C = acc - za*colsum(B) - zb*rowsum(A) + K*za*zb (int32, wrapping)
+  const void* a_zp;        int a_zp_count;  // 0 (none), 1, or per row
+  const void* b_zp;        int b_zp_count;  // 0 (none), 1, or N
+  int zp_row_mod;          // row index modulus for per-row a_zp / act_scale
+  unsigned* err;           // device error word
+};
+
+// mmi = MatMulInteger epilogue (int32 out); otherwise A8W8 (s8 x s8 only).
+// chunk_k: K-chunk length between exact drains (multiple of 64).
+cudaError_t launch_gemm_tc(const GemmArgs& a, bool a_u8, bool b_u8, bool mmi, int chunk_k, cudaStream_t s,
+                           const char** kernel_name);
+
+// Largest exact chunk length for the operand signedness (fp32 sums <= 2^24).
+int gemm_default_chunk_k(bool a_u8, bool b_u8);
+
+// ---------------------------------------------------------------------------
+// Decode GEMV: bf16 A [M<=16][K] x int8 W [K][N], per-column or scalar scale/zp.
+// ---------------------------------------------------------------------------
+struct GemvArgs {
+  const uint16_t* A;       // bf16 bits [M][K]
+  const int8_t* W;         // [K][N]
+  int M, K, N;
+  const float* scale; int scale_count;        // 1 or N
+  const int32_t* zp;  int zp_count;           // 0, 1 or N
+  void* C; int c_f32;                         // [M][N] bf16 (0) or f32 (1)
+};
+bool gemv_supported(long long M, long long K, long long N, const void* A, const void* W);
+cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, const char** kernel_name);
+
+// ---------------------------------------------------------------------------
+// Generic CUDA-core form (a): float A (f32 or bf16) x int8 B, any shape.
+// ---------------------------------------------------------------------------
+struct W8SimtArgs {
+  const void* A; int a_bf16;   // [M][K]
+  const int8_t* B;             // [K][N]
+  int M, K, N;
+  const float* scale; int scale_count;
+  const int32_t* zp;  int zp_count;
+  void* C; int c_f32;
+};
+cudaError_t launch_w8_simt(const W8SimtArgs& a, cudaStream_t s, const char** kernel_name);
+
+// ---------------------------------------------------------------------------
+// DynamicQuantizeLinear: two-pass grid min/max + vectorised quantize.
+// ---------------------------------------------------------------------------
+constexpr int kDqlMaxPartials = 1024;
+int dql_num_partials(long long n);
+cudaError_t launch_dql(const float* x, long long n, uint8_t* y, float* y_scale, uint8_t* y_zp, int32_t* row_sums,
+                       long long row_len, float* partials, int num_partials, cudaStream_t s,
+                       const char** kernel_name);
+
+int num_sms();
+
+}  // namespace qmm

@@ -1,0 +1,305 @@
+// The library's C ABI (include/qmm.h): argument validation, kernel selection,
+// launch-error handling, the device error word, and the per-thread record of
+// which kernel ran.
+//
+// Error handling follows the launch convention of ROCm hip-ep PR #1248
+// ("What", last paragraph): the CUDA last-error state is cleared before a
+// launch and read back after it.
+#include "kernels.h"
+#include "../../include/qmm.h"
+
+#include <climits>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+namespace qmm {
+
+// Device error word: a timed-out wait inside a kernel records its site here.
+__device__ unsigned g_qmm_error_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+thread_local const char* t_last_kernel = "none";
+thread_local int t_last_cuda_error = 0;
+thread_local unsigned t_last_device_error = 0;
+
+std::mutex g_mu;
+unsigned* g_err_ptr[kMaxDevices] = {};
+int g_sms[kMaxDevices] = {};
+
+int current_device() {
+  int d = 0;
+  if (cudaGetDevice(&d) != cudaSuccess) return -1;
+  return d;
+}
+
+unsigned* err_word() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return nullptr;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_err_ptr[d]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_qmm_error_word) != cudaSuccess) return nullptr;
+    g_err_ptr[d] = static_cast<unsigned*>(p);
+  }
+  return g_err_ptr[d];
+}
+
+bool dim_ok(int64_t v) { return v >= 0 && v <= (int64_t)INT_MAX; }
+
+qmm_status finish_launch(cudaError_t e, const char* name) {
+  if (e != cudaSuccess) {
+    t_last_cuda_error = (int)e;
+    return QMM_ERR_CUDA;
+  }
+  t_last_kernel = name;
+  return QMM_OK;
+}
+
+// Chunk length between exact drains of the tensor-core accumulator. The
+// environment variable QMM_CHUNK_K may only shorten it (a multiple of 64):
+// it exists to exercise the drain path with more chunks per tile.
+int chunk_k_for(bool a_u8, bool b_u8) {
+  const int dflt = gemm_default_chunk_k(a_u8, b_u8);
+  const char* env = std::getenv("QMM_CHUNK_K");
+  if (env) {
+    const int v = std::atoi(env);
+    if (v >= 64 && v % 64 == 0 && v < dflt) return v;
+  }
+  return dflt;
+}
+
+}  // namespace
+
+int num_sms() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return 0;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_sms[d]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, d) != cudaSuccess) return 0;
+    g_sms[d] = n;
+  }
+  return g_sms[d];
+}
+
+}  // namespace qmm
+
+using namespace qmm;
+
+extern "C" {
+
+const char* qmm_status_string(int s) {
+  switch (s) {
+    case QMM_OK: return "QMM_OK";
+    case QMM_ERR_INVALID_ARG: return "QMM_ERR_INVALID_ARG";
+    case QMM_ERR_UNSUPPORTED: return "QMM_ERR_UNSUPPORTED";
+    case QMM_ERR_CUDA: return "QMM_ERR_CUDA";
+    case QMM_ERR_TIMEOUT: return "QMM_ERR_TIMEOUT";
+    default: return "QMM_UNKNOWN_STATUS";
+  }
+}
+
+const char* qmm_last_kernel(void) { return t_last_kernel; }
+int qmm_last_cuda_error(void) { return t_last_cuda_error; }
+unsigned qmm_last_device_error(void) { return t_last_device_error; }
+int qmm_num_sms(void) { return num_sms(); }
+int qmm_abi_version(void) { return 1; }
+
+qmm_status qmm_check_device_error(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) {
+    t_last_cuda_error = (int)e;
+    return QMM_ERR_CUDA;
+  }
+  unsigned* w = err_word();
+  if (!w) return QMM_ERR_CUDA;
+  unsigned v = 0;
+  e = cudaMemcpy(&v, w, sizeof(v), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) {
+    t_last_cuda_error = (int)e;
+    return QMM_ERR_CUDA;
+  }
+  t_last_device_error = v;
+  if (v != 0) {
+    cudaMemset(w, 0, sizeof(unsigned));
+    return QMM_ERR_TIMEOUT;
+  }
+  return QMM_OK;
+}
+
+qmm_status qmm_w8_dequant(const void* A, int a_dtype, const int8_t* B, int64_t M, int64_t K, int64_t N,
+                          const float* scale, int64_t scale_count, const int32_t* zero_point, int64_t zp_count,
+                          void* C, int c_dtype, void* stream) {
+  if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return QMM_ERR_INVALID_ARG;
+  if (a_dtype != QMM_F32 && a_dtype != QMM_BF16) return QMM_ERR_INVALID_ARG;
+  if (c_dtype != QMM_F32 && c_dtype != QMM_BF16) return QMM_ERR_INVALID_ARG;
+  if (scale_count != 1 && scale_count != N) return QMM_ERR_INVALID_ARG;
+  if (zp_count != 0 && zp_count != 1 && zp_count != N) return QMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) {
+    t_last_kernel = "none";
+    return QMM_OK;
+  }
+  if (!scale || !C || (K > 0 && (!A || !B)) || (zp_count > 0 && !zero_point)) return QMM_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  const char* name = "none";
+  if (a_dtype == QMM_BF16 && gemv_supported(M, K, N, A, B)) {
+    GemvArgs g{};
+    g.A = static_cast<const uint16_t*>(A);
+    g.W = B;
+    g.M = (int)M;
+    g.K = (int)K;
+    g.N = (int)N;
+    g.scale = scale;
+    g.scale_count = (int)scale_count;
+    g.zp = zero_point;
+    g.zp_count = (int)zp_count;
+    g.C = C;
+    g.c_f32 = c_dtype == QMM_F32;
+    return finish_launch(launch_gemv(g, s, &name), name);
+  }
+  if ((M + 63) / 64 > 65535) return QMM_ERR_UNSUPPORTED;
+  W8SimtArgs w{};
+  w.A = A;
+  w.a_bf16 = a_dtype == QMM_BF16;
+  w.B = B;
+  w.M = (int)M;
+  w.K = (int)K;
+  w.N = (int)N;
+  w.scale = scale;
+  w.scale_count = (int)scale_count;
+  w.zp = zero_point;
+  w.zp_count = (int)zp_count;
+  w.C = C;
+  w.c_f32 = c_dtype == QMM_F32;
+  return finish_launch(launch_w8_simt(w, s, &name), name);
+}
+
+qmm_status qmm_a8w8(const int8_t* A, const int8_t* B, int64_t M, int64_t K, int64_t N, const float* act_scale,
+                    int64_t act_count, const float* weight_scale, int64_t w_count, void* C, int c_dtype,
+                    void* stream) {
+  if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return QMM_ERR_INVALID_ARG;
+  if (c_dtype != QMM_F32 && c_dtype != QMM_BF16) return QMM_ERR_INVALID_ARG;
+  if (act_count != 1 && act_count != M) return QMM_ERR_INVALID_ARG;
+  if (w_count != 1 && w_count != N) return QMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) {
+    t_last_kernel = "none";
+    return QMM_OK;
+  }
+  if (!act_scale || !weight_scale || !C || (K > 0 && (!A || !B))) return QMM_ERR_INVALID_ARG;
+  const long long tiles = ((M + 127) / 128) * ((N + 255) / 256);
+  if (tiles > INT_MAX) return QMM_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  if (K == 0) {   // empty sum: acc = 0, so every output is +0
+    const size_t bytes = (size_t)M * (size_t)N * (c_dtype == QMM_F32 ? 4 : 2);
+    return finish_launch(cudaMemsetAsync(C, 0, bytes, s), "memset_zero");
+  }
+  unsigned* err = err_word();
+  if (!err) return QMM_ERR_CUDA;
+  GemmArgs g{};
+  g.A = reinterpret_cast<const uint8_t*>(A);
+  g.B = reinterpret_cast<const uint8_t*>(B);
+  g.a_bstride = 0;
+  g.b_bstride = 0;
+  g.batch = 1;
+  g.M = (int)M;
+  g.K = (int)K;
+  g.N = (int)N;
+  g.C = C;
+  g.c_f32 = c_dtype == QMM_F32;
+  g.act_scale = act_scale;
+  g.act_count = (int)act_count;
+  g.w_scale = weight_scale;
+  g.w_count = (int)w_count;
+  g.zp_row_mod = (int)M;
+  g.err = err;
+  const char* name = "none";
+  return finish_launch(launch_gemm_tc(g, false, false, false, chunk_k_for(false, false), s, &name), name);
+}
+
+qmm_status matmul_integer(const void* A, int a_dtype, const void* B, int b_dtype, int64_t batch, int64_t M,
+                          int64_t K, int64_t N, int64_t a_batch_stride, int64_t b_batch_stride,
+                          const void* a_zero_point, int64_t a_zp_count, const void* b_zero_point,
+                          int64_t b_zp_count, int32_t* C, void* stream) {
+  if (!dim_ok(batch) || !dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return QMM_ERR_INVALID_ARG;
+  if ((a_dtype != QMM_S8 && a_dtype != QMM_U8) || (b_dtype != QMM_S8 && b_dtype != QMM_U8))
+    return QMM_ERR_INVALID_ARG;
+  if (a_batch_stride < 0 || b_batch_stride < 0) return QMM_ERR_INVALID_ARG;
+  if (a_zp_count != 0 && a_zp_count != 1 && a_zp_count != M) return QMM_ERR_INVALID_ARG;
+  if (b_zp_count != 0 && b_zp_count != 1 && b_zp_count != N) return QMM_ERR_INVALID_ARG;
+  if (batch == 0 || M == 0 || N == 0) {
+    t_last_kernel = "none";
+    return QMM_OK;
+  }
+  if (!C || (K > 0 && (!A || !B)) || (a_zp_count > 0 && !a_zero_point) || (b_zp_count > 0 && !b_zero_point))
+    return QMM_ERR_INVALID_ARG;
+  if (batch * M > (int64_t)INT_MAX) return QMM_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  if (K == 0) {   // empty sums: every output is 0
+    return finish_launch(cudaMemsetAsync(C, 0, (size_t)batch * M * N * sizeof(int32_t), s), "memset_zero");
+  }
+  unsigned* err = err_word();
+  if (!err) return QMM_ERR_CUDA;
+  // A shared B with a densely batched A is one GEMM with the batch folded into M.
+  int64_t gb = batch, gm = M;
+  if (batch > 1 && b_batch_stride == 0 && a_batch_stride == M * K) {
+    gm = batch * M;
+    gb = 1;
+  }
+  const long long tiles = gb * ((gm + 127) / 128) * ((N + 255) / 256);
+  if (tiles > INT_MAX) return QMM_ERR_UNSUPPORTED;
+  GemmArgs g{};
+  g.A = static_cast<const uint8_t*>(A);
+  g.B = static_cast<const uint8_t*>(B);
+  g.a_bstride = gb > 1 ? a_batch_stride : 0;
+  g.b_bstride = gb > 1 ? b_batch_stride : 0;
+  g.batch = (int)gb;
+  g.M = (int)gm;
+  g.K = (int)K;
+  g.N = (int)N;
+  g.C = C;
+  g.a_zp = a_zero_point;
+  g.a_zp_count = (int)a_zp_count;
+  g.b_zp = b_zero_point;
+  g.b_zp_count = (int)b_zp_count;
+  g.zp_row_mod = (int)M;
+  g.err = err;
+  const bool au = a_dtype == QMM_U8, bu = b_dtype == QMM_U8;
+  const char* name = "none";
+  return finish_launch(launch_gemm_tc(g, au, bu, true, chunk_k_for(au, bu), s, &name), name);
+}
+
+size_t dynamic_quantize_linear_workspace_bytes(int64_t n) {
+  long long p = (n + 32767) / 32768;
+  if (p < 1) p = 1;
+  if (p > kDqlMaxPartials) p = kDqlMaxPartials;
+  return (size_t)p * 2 * sizeof(float);
+}
+
+qmm_status dynamic_quantize_linear(const float* x, int64_t n, uint8_t* y, float* y_scale, uint8_t* y_zero_point,
+                                   int32_t* row_sums, int64_t row_len, void* workspace, size_t workspace_bytes,
+                                   void* stream) {
+  if (n < 0) return QMM_ERR_INVALID_ARG;
+  if (!y_scale || !y_zero_point || (n > 0 && (!x || !y))) return QMM_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) % 16) != 0) return QMM_ERR_INVALID_ARG;
+  if (workspace_bytes < dynamic_quantize_linear_workspace_bytes(n)) return QMM_ERR_INVALID_ARG;
+  if (row_sums) {
+    if (row_len <= 0 || n % row_len != 0) return QMM_ERR_INVALID_ARG;
+    if (n / row_len > (int64_t)INT_MAX) return QMM_ERR_UNSUPPORTED;
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  const int parts = dql_num_partials(n);
+  const char* name = "none";
+  return finish_launch(launch_dql(x, n, y, y_scale, y_zero_point, row_sums, row_len,
+                                  static_cast<float*>(workspace), parts, s, &name),
+                       name);
+}
+
+}  // extern "C"
