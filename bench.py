@@ -1,0 +1,409 @@
+#!/usr/bin/env python
+"""Benchmark of the integer-quantised matmul hot path on GB300.
+
+Headline workload: the A8W8 GEMM at M = K = N = 4096 (int8 x int8, exact int32
+accumulation, act_scale[M] / weight_scale[N] epilogue, bf16 output), reported
+as TOPS (2*M*N*K integer operations per second). One step = one call of
+qmm_a8w8 on inputs resident in HBM; a 256 MiB write flushes L2 before every
+timed iteration (the inputs, 32 MiB, would otherwise sit in the 126 MiB L2).
+
+The same JSON line also carries the other benchmark workloads of the path,
+each timed with CUDA events on the launching stream: the decode GEMV (int8
+weight 8192x28672, M in {1,4,16}) in GB/s of algorithmic bytes and as a
+fraction of measured HBM bandwidth; DynamicQuantizeLinear on 8192x4096 fp32;
+MatMulInteger 8192x4096x11008 (u8 x s8, zero points); batched MatMulInteger
+65536x1024x1024 with a shared B; and the small fp32 x int8 matmul.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl qmm|reference]
+With N > 1 (torchrun) every rank runs an independent replica (the path has no
+exchange step); value = all ranks' operations / the slowest rank's time.
+--impl reference times the CPU oracle (test infrastructure) on rank 0 only.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import qmm_workloads as W  # noqa: E402
+
+METRIC = "A8W8 int8 GEMM TOPS at 4096^3 (% int8 peak); int8-weight GEMV GB/s (% HBM)"
+WORKLOAD = "a8w8_4096x4096x4096_bf16"
+M = K = N = 4096
+OPS = 2.0 * M * N * K
+FLUSH_BYTES = 256 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_traffic(kernel_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    source is unchanged since the counters were taken; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)[kernel_key]
+        src = os.path.join(ROOT, d["source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if h != d["source_sha256"]:
+            return None
+        return float(d["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError, TypeError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed regions run."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = None
+        self.windows = []
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(prefix="qmm_clocks_", suffix=".csv")
+        os.close(fd)
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if self.uuid:
+            cmd[1:1] = ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def mark(self, t0, t1):
+        self.windows.append((t0, t1))
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "", 1).isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "", 1).isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "", 1).isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+def time_gpu(fn, steps, warmup, flush=None):
+    """Per-iteration device time (ms) of fn, CUDA events on the current stream."""
+    import torch
+    for _ in range(warmup):
+        if flush is not None:
+            flush()
+        fn()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush()
+        ev[i][0].record()
+        fn()
+        ev[i][1].record()
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def cpu_baseline_a8w8(budget_s=12.0, max_rows=4096):
+    """The oracle as it stands on a bounded sample of rows of the 4096^3 workload."""
+    from oracle import qmm_oracle as O
+    w = W.a8w8_4096()
+    rows, t = 0, 0.0
+    step = 8
+    while t < budget_s and rows < max_rows:
+        sl = slice(rows, rows + step)
+        t0 = time.perf_counter()
+        O.a8w8(w.A[sl], w.B, w.act_scale[sl], w.weight_scale, "bf16")
+        t += time.perf_counter() - t0
+        rows += step
+    ops = 2.0 * rows * K * N
+    return {"value": ops / t / 1e12, "unit": "TOPS", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} of 4096 rows of the 4096^3 A8W8 workload (numpy int64 matmul + float32 "
+                      f"epilogue, single thread), {t:.1f} s"}
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    from oracle import qmm_oracle as O
+    w = W.a8w8_4096()
+    times = []
+    cols = 512                      # one step: one row x 512 columns of the output
+    for i in range(args.warmup + args.steps):
+        r = i % M
+        c0 = (i * cols) % N
+        t0 = time.perf_counter()
+        O.a8w8(w.A[r:r + 1], w.B[:, c0:c0 + cols], w.act_scale[r:r + 1], w.weight_scale[c0:c0 + cols], "bf16")
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    per_step_ops = 2.0 * K * cols
+    mean = statistics.mean(times)
+    value = per_step_ops / mean / 1e12
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int64 (oracle)", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "step": "one row x 512 columns of the output"},
+            "cpu_baseline": {"value": value, "unit": "TOPS", "cores": 1, "kind": "oracle",
+                             "sample": "one row x 512 columns of the 4096^3 A8W8 workload per step"},
+            "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="qmm", choices=["qmm", "reference"])
+    ap.add_argument("--no-secondary", action="store_true", help="time only the headline workload")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(v):
+        if dist is None:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    import quantized_int8_matmul_gb300 as q
+    lib = q.lib()
+    peaks, peaks_src = load_peaks()
+    props = torch.cuda.get_device_properties(local_rank)
+    uuid = None
+    try:
+        u = str(props.uuid)
+        uuid = u if u.startswith("GPU-") else "GPU-" + u
+    except AttributeError:
+        pass
+    clocks = ClockSampler(uuid)
+
+    flush_buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def flush():
+        flush_buf.fill_(1)
+
+    # ---------------- headline: A8W8 4096^3 ----------------
+    w = W.a8w8_4096()
+    A = torch.from_numpy(w.A).cuda()
+    B = torch.from_numpy(w.B).cuda()
+    a_s = torch.from_numpy(w.act_scale).cuda()
+    w_s = torch.from_numpy(w.weight_scale).cuda()
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+
+    def a8w8_call():
+        q.qmm_a8w8(A, B, a_s, w_s, out=C)
+
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.time()
+    times = time_gpu(a8w8_call, args.steps, args.warmup, flush=flush)
+    t1 = time.time()
+    barrier()
+    clocks.mark(t0, t1)
+    kernel_name = q.last_kernel()
+    q.check_device_error()
+    mean_ms = statistics.mean(times)
+    slow_ms = max_over_ranks(mean_ms)
+    value = world * OPS / (slow_ms * 1e-3) / 1e12
+    achieved = OPS / (mean_ms * 1e-3) / 1e12
+
+    # end to end: pinned host inputs -> device, call, result -> pinned host
+    hA = torch.from_numpy(w.A).pin_memory()
+    hB = torch.from_numpy(w.B).pin_memory()
+    ha = torch.from_numpy(w.act_scale).pin_memory()
+    hw = torch.from_numpy(w.weight_scale).pin_memory()
+    hC = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+
+    def e2e_call():
+        A.copy_(hA, non_blocking=True)
+        B.copy_(hB, non_blocking=True)
+        a_s.copy_(ha, non_blocking=True)
+        w_s.copy_(hw, non_blocking=True)
+        q.qmm_a8w8(A, B, a_s, w_s, out=C)
+        hC.copy_(C, non_blocking=True)
+
+    e2e_steps = min(args.steps, 50)
+    e2e_times = time_gpu(e2e_call, e2e_steps, 3)
+    e2e_ms = max_over_ranks(statistics.mean(e2e_times))
+    h2d = hA.numel() + hB.numel() + 4 * (ha.numel() + hw.numel())
+    d2h = 2 * hC.numel()
+
+    rows = {}
+    if not args.no_secondary:
+        rows = secondary(q, torch, flush, clocks, peaks)
+    clk = clocks.stop()
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+
+    cpu = cpu_baseline_a8w8() if world == 1 else None
+    line = {
+        "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": slow_ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "s8", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "out": "bf16",
+                   "l2": "flushed before every timed iteration (256 MiB write)",
+                   "parallelism": f"replicas x{world}", "kernel": kernel_name,
+                   "contraction": "exact int8 products on tcgen05 kind::f16 (fp16 operands), "
+                                  "K-chunked fp32 TMEM accumulator drained to int32"},
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": kernel_traffic("gemm_tc05_exact_a8w8"),
+                     "peak_source": f"{peaks_src} dense bf16 (burst); fp16 kind::f16 runs at the same rate"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * OPS / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+        "rows": rows,
+    }
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def secondary(q, torch, flush, clocks, peaks):
+    out = {}
+    hbm = peaks["hbm_gbs"]
+    iters, warm = 20, 3
+
+    def timed(fn, use_flush=False):
+        t0 = time.time()
+        ts = time_gpu(fn, iters, warm, flush=flush if use_flush else None)
+        clocks.mark(t0, time.time())
+        return statistics.mean(ts)
+
+    # decode GEMV, M in {1, 4, 16}: weight stream 235 MB > L2, no flush needed
+    for Mg in (1, 4, 16):
+        g = W.decode_gemv(Mg)
+        Ad = torch.from_numpy(g.A_bits.view(np.int16)).view(torch.bfloat16).cuda()
+        Wd = torch.from_numpy(g.W).cuda()
+        sd = torch.from_numpy(g.scale).cuda()
+        Cd = torch.empty((Mg, 28672), dtype=torch.bfloat16, device="cuda")
+        ms = timed(lambda: q.qmm_w8_dequant(Ad, Wd, sd, None, out=Cd))
+        nbytes = 8192 * 28672 + Mg * 8192 * 2 + 28672 * 4 + Mg * 28672 * 2
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        out[f"decode_gemv_M{Mg}"] = {"us": ms * 1e3, "value": gbs, "unit": "GB/s", "bound": "hbm",
+                                     "frac": gbs / hbm, "kernel": q.last_kernel(), "algorithmic_bytes": nbytes}
+        del Wd
+    torch.cuda.empty_cache()
+
+    # DynamicQuantizeLinear 8192x4096 then MatMulInteger 8192x4096x11008
+    d = W.dql_matmul_integer_8192x4096x11008()
+    x = torch.from_numpy(d.x).cuda()
+    Bd = torch.from_numpy(d.B).cuda()
+    bz = torch.from_numpy(d.b_zp).cuda()
+    ws = torch.empty(q.dynamic_quantize_linear_workspace_bytes(x.numel()), dtype=torch.uint8, device="cuda")
+    res = {}
+
+    def dql_call():
+        res["r"] = q.dynamic_quantize_linear(x, row_len=4096, workspace=ws)
+
+    ms = timed(dql_call)
+    n = x.numel()
+    gbs9 = 9 * n / (ms * 1e-3) / 1e9
+    out["dql_8192x4096"] = {"us": ms * 1e3, "value": gbs9, "unit": "GB/s", "bound": "hbm", "frac": gbs9 / hbm,
+                            "algorithmic_bytes": 9 * n, "note": "9 B/element (read x twice, write u8); "
+                            f"{5 * n / (ms * 1e-3) / 1e9:.0f} GB/s against the 5 B/element floor",
+                            "kernel": q.last_kernel()}
+    y, _, zp, _ = res["r"]
+    Ci = torch.empty((8192, 11008), dtype=torch.int32, device="cuda")
+    ms = timed(lambda: q.matmul_integer(y, Bd, a_zero_point=zp, b_zero_point=bz, out=Ci), use_flush=False)
+    ops = 2.0 * 8192 * 4096 * 11008
+    tops = ops / (ms * 1e-3) / 1e12
+    out["matmul_integer_8192x4096x11008"] = {"us": ms * 1e3, "value": tops, "unit": "TOPS", "bound": "tensor",
+                                             "frac": tops / peaks["bf16_tflops"], "kernel": q.last_kernel(),
+                                             "note": "inputs + int32 output 440 MB exceed L2"}
+    del x, Bd, Ci, y
+    torch.cuda.empty_cache()
+
+    # batched MatMulInteger, shared rank-2 B
+    bm = W.batched_matmul_integer()
+    Ab = torch.from_numpy(bm.A).cuda()
+    Bb = torch.from_numpy(bm.B).cuda()
+    za = torch.tensor([bm.a_zp], dtype=torch.int8, device="cuda")
+    zb = torch.tensor([bm.b_zp], dtype=torch.int8, device="cuda")
+    Cb = torch.empty((8, 16, 512, 1024), dtype=torch.int32, device="cuda")
+    ms = timed(lambda: q.matmul_integer(Ab, Bb, a_zero_point=za, b_zero_point=zb, out=Cb))
+    ops = 2.0 * 65536 * 1024 * 1024
+    tops = ops / (ms * 1e-3) / 1e12
+    nbytes = 65536 * 1024 + 1024 * 1024 + 65536 * 1024 * 4
+    out["batched_matmul_integer_65536x1024x1024"] = {
+        "us": ms * 1e3, "value": tops, "unit": "TOPS", "frac_tensor": tops / peaks["bf16_tflops"],
+        "gbs": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm, "kernel": q.last_kernel()}
+    del Ab, Cb
+    torch.cuda.empty_cache()
+
+    # small fp32 x int8 (latency-bound)
+    s = W.w8_dequant_f32_64x256x192()
+    As, Bs = torch.from_numpy(s.A).cuda(), torch.from_numpy(s.B).cuda()
+    ss, zs = torch.from_numpy(s.scale).cuda(), torch.from_numpy(s.zero_point).cuda()
+    Cs = torch.empty((64, 192), dtype=torch.float32, device="cuda")
+    ms = timed(lambda: q.qmm_w8_dequant(As, Bs, ss, zs, out=Cs), use_flush=True)
+    out["w8_dequant_f32_64x256x192"] = {"us": ms * 1e3, "unit": "us", "bound": "latency", "kernel": q.last_kernel()}
+    return out
+
+
+if __name__ == "__main__":
+    main()

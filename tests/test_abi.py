@@ -1,0 +1,128 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point include/qmm.h declares, and rejects malformed arguments on the host
+before touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qmm.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"\b([A-Za-z_][A-Za-z0-9_]*)\s*\([^;{]*\)\s*;", text)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def qmm():
+    import quantized_int8_matmul_gb300 as q
+    return q
+
+
+def test_header_declares_the_four_forms():
+    names = declared_functions()
+    for fn in ("qmm_w8_dequant", "qmm_a8w8", "matmul_integer", "dynamic_quantize_linear"):
+        assert fn in names
+
+
+def test_library_exports_every_declared_symbol(qmm):
+    lib = ctypes.CDLL(qmm.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert missing == []
+
+
+def test_library_is_built_for_sm_103a_only(qmm):
+    from quantized_int8_matmul_gb300 import _build
+    assert _build.ARCH_FLAGS == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def test_status_strings_and_version(qmm):
+    lib = qmm.lib()
+    assert lib.qmm_abi_version() == 1
+    assert lib.qmm_status_string(0) == b"QMM_OK"
+    assert lib.qmm_status_string(4) == b"QMM_ERR_TIMEOUT"
+    assert lib.qmm_status_string(99) == b"QMM_UNKNOWN_STATUS"
+
+
+def test_dql_workspace_size_is_a_device_independent_bound(qmm):
+    f = qmm.dynamic_quantize_linear_workspace_bytes
+    assert f(0) == 8 and f(1) == 8
+    assert f(32768 * 3) == 24
+    assert f(8192 * 4096) == 8 * 1024          # capped at 1024 partials
+    assert f(10**12) == 8 * 1024
+
+
+# Malformed calls fail validation on the host and enqueue nothing, so they run without a GPU.
+P = ctypes.c_void_p(16)   # a non-null stand-in pointer; never dereferenced on these paths
+
+
+def test_w8_dequant_rejects_bad_arguments(qmm):
+    lib = qmm.lib()
+    ok_args = dict(A=P, a=0, B=P, M=4, K=8, N=8, s=P, sc=1, z=None, zc=0, C=P, c=0, st=None)
+
+    def call(**kw):
+        a = {**ok_args, **kw}
+        return lib.qmm_w8_dequant(a["A"], a["a"], a["B"], a["M"], a["K"], a["N"], a["s"], a["sc"], a["z"],
+                                  a["zc"], a["C"], a["c"], a["st"])
+
+    assert call(a=2) == qmm.QMM_ERR_INVALID_ARG          # int8 activations are not form (a)
+    assert call(c=4) == qmm.QMM_ERR_INVALID_ARG          # int32 output
+    assert call(M=-1) == qmm.QMM_ERR_INVALID_ARG
+    assert call(K=2**31) == qmm.QMM_ERR_INVALID_ARG
+    assert call(sc=3) == qmm.QMM_ERR_INVALID_ARG          # scale count neither 1 nor N
+    assert call(zc=1, z=None) == qmm.QMM_ERR_INVALID_ARG  # zero point count without pointer
+    assert call(zc=5) == qmm.QMM_ERR_INVALID_ARG
+    assert call(s=None) == qmm.QMM_ERR_INVALID_ARG
+    assert call(M=0) == qmm.QMM_OK                        # empty output: nothing to do
+
+
+def test_a8w8_rejects_bad_arguments(qmm):
+    lib = qmm.lib()
+
+    def call(M=4, K=8, N=8, ac=1, wc=1, c=1, A=P, C=P):
+        return lib.qmm_a8w8(A, P, M, K, N, P, ac, P, wc, C, c, None)
+
+    assert call(ac=3) == qmm.QMM_ERR_INVALID_ARG
+    assert call(wc=2) == qmm.QMM_ERR_INVALID_ARG
+    assert call(c=2) == qmm.QMM_ERR_INVALID_ARG
+    assert call(A=None) == qmm.QMM_ERR_INVALID_ARG
+    assert call(C=None) == qmm.QMM_ERR_INVALID_ARG
+    assert call(N=-5) == qmm.QMM_ERR_INVALID_ARG
+    assert call(N=0) == qmm.QMM_OK
+
+
+def test_matmul_integer_rejects_bad_arguments(qmm):
+    lib = qmm.lib()
+
+    def call(ad=3, bd=2, batch=1, M=4, K=8, N=8, sa=0, sb=0, az=None, azc=0, bz=None, bzc=0, C=P):
+        return lib.matmul_integer(P, ad, P, bd, batch, M, K, N, sa, sb, az, azc, bz, bzc, C, None)
+
+    assert call(ad=0) == qmm.QMM_ERR_INVALID_ARG          # float A
+    assert call(bd=4) == qmm.QMM_ERR_INVALID_ARG
+    assert call(sa=-1) == qmm.QMM_ERR_INVALID_ARG
+    assert call(azc=1) == qmm.QMM_ERR_INVALID_ARG         # count without pointer
+    assert call(az=P, azc=3) == qmm.QMM_ERR_INVALID_ARG   # neither 1 nor M
+    assert call(bz=P, bzc=4) == qmm.QMM_ERR_INVALID_ARG   # neither 1 nor N
+    assert call(batch=2**20, M=2**12) == qmm.QMM_ERR_UNSUPPORTED   # batch*M beyond int32
+    assert call(batch=0) == qmm.QMM_OK
+
+
+def test_dql_rejects_bad_arguments(qmm):
+    lib = qmm.lib()
+    ws = ctypes.c_void_p(4096)
+
+    def call(n=100, x=P, y=P, rs=None, rl=0, w=ws, wb=8):
+        return lib.dynamic_quantize_linear(x, n, y, P, P, rs, rl, w, wb, None)
+
+    assert call(n=-1) == qmm.QMM_ERR_INVALID_ARG
+    assert call(x=None) == qmm.QMM_ERR_INVALID_ARG
+    assert call(w=None) == qmm.QMM_ERR_INVALID_ARG
+    assert call(w=ctypes.c_void_p(4100)) == qmm.QMM_ERR_INVALID_ARG     # workspace not 16-byte aligned
+    assert call(n=10**7, wb=8) == qmm.QMM_ERR_INVALID_ARG                # workspace too small
+    assert call(rs=P, rl=7) == qmm.QMM_ERR_INVALID_ARG                   # 100 % 7 != 0
+    assert call(rs=P, rl=0) == qmm.QMM_ERR_INVALID_ARG

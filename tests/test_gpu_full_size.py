@@ -1,0 +1,81 @@
+"""The five benchmark workloads at full size, through the same entry points and
+launch configuration bench.py times, checked against the oracle: in full where
+the oracle is cheap (DynamicQuantizeLinear, the small fp32 case), otherwise on
+sampled rows or columns the oracle computes one by one."""
+import numpy as np
+import pytest
+import torch
+
+import qmm_workloads as W
+from oracle import qmm_oracle as O
+from _helpers import assert_equal, assert_within, bf16_bits_to_f64, bf16_dev, dev, host
+
+pytestmark = pytest.mark.gpu
+q = pytest.importorskip("quantized_int8_matmul_gb300")
+
+
+def sample(n, k, seed):
+    return np.sort(np.random.default_rng(seed).choice(n, size=k, replace=False))
+
+
+def test_w8_dequant_f32_64x256x192():
+    w = W.w8_dequant_f32_64x256x192()
+    C = q.qmm_w8_dequant(dev(w.A), dev(w.B), dev(w.scale), dev(w.zero_point), out_dtype=torch.float32)
+    assert q.last_kernel() == "w8_dequant_simt"
+    exact = O.w8_dequant(w.A, w.B, w.scale, w.zero_point)
+    bound = O.w8_dequant_error_bound(w.A, w.B, w.scale, w.zero_point)
+    assert_within(host(C).astype(np.float64), exact, bound, 23, "w8 64x256x192")
+
+
+def test_a8w8_4096():
+    w = W.a8w8_4096()
+    C = q.qmm_a8w8(dev(w.A), dev(w.B), dev(w.act_scale), dev(w.weight_scale), out_dtype=torch.bfloat16)
+    q.check_device_error()
+    assert q.last_kernel() == "gemm_tc05_exact_a8w8"
+    got = host(C)
+    rows = sample(4096, 40, 1)
+    want = O.a8w8(w.A[rows], w.B, w.act_scale[rows], w.weight_scale, "bf16")
+    assert_equal(got[rows], want, "a8w8 4096^3 sampled rows")
+
+
+def test_dql_then_matmul_integer_8192x4096x11008():
+    w = W.dql_matmul_integer_8192x4096x11008()
+    y, s, zp, rs = q.dynamic_quantize_linear(dev(w.x), row_len=4096)
+    assert q.last_kernel() == "dql_minmax+dql_quantize_rows"
+    wy, ws, wzp = O.dynamic_quantize_linear(w.x)
+    assert float(s.item()) == float(ws) and int(zp.item()) == int(wzp)
+    assert_equal(host(y), wy, "DQL 8192x4096")
+    assert_equal(host(rs), O.row_sums(wy, 4096), "DQL row sums")
+    # the zero point stays on the device between the two calls
+    C = q.matmul_integer(y, dev(w.B), a_zero_point=zp, b_zero_point=dev(w.b_zp))
+    q.check_device_error()
+    assert q.last_kernel() == "gemm_tc05_exact_matmul_integer"
+    rows = sample(8192, 16, 2)
+    want = O.matmul_integer(wy[rows], w.B, int(wzp), w.b_zp)
+    assert_equal(host(C)[rows], want, "MatMulInteger 8192x4096x11008 sampled rows")
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_decode_gemv_8192x28672(M):
+    w = W.decode_gemv(M)
+    C = q.qmm_w8_dequant(bf16_dev(w.A_bits), dev(w.W), dev(w.scale), None, out_dtype=torch.bfloat16)
+    assert q.last_kernel() == "gemv_w8_bf16_mma"
+    got = bf16_bits_to_f64(host(C))
+    cols = sample(28672, 1024, 3)
+    zp0 = np.zeros(1, np.int32)
+    Wc = np.ascontiguousarray(w.W[:, cols])
+    exact = O.w8_dequant(w.A, Wc, w.scale[cols], zp0)
+    bound = O.w8_dequant_error_bound(w.A, Wc, w.scale[cols], zp0)
+    assert_within(got[:, cols], exact, bound, 7, f"GEMV M={M}")
+
+
+def test_batched_matmul_integer_shared_b():
+    w = W.batched_matmul_integer()
+    C = q.matmul_integer(dev(w.A), dev(w.B), a_zero_point=dev(np.array([w.a_zp], np.int8)),
+                         b_zero_point=dev(np.array([w.b_zp], np.int8)))
+    q.check_device_error()
+    assert C.shape == (8, 16, 512, 1024)
+    got = host(C).reshape(-1, 1024)
+    rows = sample(8 * 16 * 512, 48, 4)
+    want = O.matmul_integer(w.A.reshape(-1, 1024)[rows], w.B, w.a_zp, w.b_zp)
+    assert_equal(got[rows], want, "batched MatMulInteger sampled rows")

@@ -1,0 +1,64 @@
+"""Form (a) through the C ABI: the factored int8-weight matmul against the
+oracle's exact value, within 1e-3 * sum_k |a_k * scale*(b_k - zp)| + 1e-6 plus
+half an ulp of the output type; and the small-M decode dispatch."""
+import numpy as np
+import pytest
+import torch
+
+import qmm_workloads as W
+from oracle import qmm_oracle as O
+from _helpers import assert_within, bf16_bits_to_f64, bf16_dev, dev, host
+
+pytestmark = pytest.mark.gpu
+q = pytest.importorskip("quantized_int8_matmul_gb300")
+
+
+def check(A_dev, A_vals, B, scale, zp, out, kernel):
+    zp_dev = None if zp is None else dev(zp.astype(np.int32))
+    C = q.qmm_w8_dequant(A_dev, dev(B), dev(scale), zp_dev, out_dtype=out)
+    torch.cuda.synchronize()
+    assert q.last_kernel() == kernel
+    got = host(C)
+    gotf = bf16_bits_to_f64(got) if out == torch.bfloat16 else got.astype(np.float64)
+    zpv = np.zeros(1, np.int32) if zp is None else zp
+    exact = O.w8_dequant(A_vals, B, scale, zpv)
+    bound = O.w8_dequant_error_bound(A_vals, B, scale, zpv)
+    assert_within(gotf, exact, bound, 7 if out == torch.bfloat16 else 23, kernel)
+
+
+def test_per_tensor_fp32_workload_shape():
+    w = W.w8_dequant_f32_64x256x192()
+    check(dev(w.A), w.A, w.B, w.scale, w.zero_point, torch.float32, "w8_dequant_simt")
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 1, 1), (7, 33, 5), (65, 257, 130), (200, 96, 64)])
+@pytest.mark.parametrize("zp", [None, "tensor", "column"])
+def test_simt_shapes(M, K, N, zp):
+    rng = np.random.default_rng(M + K + N)
+    A = rng.uniform(-1, 1, (M, K)).astype(np.float32)
+    B = rng.integers(-128, 128, (K, N)).astype(np.int8)
+    scale = rng.uniform(0.001, 0.05, N).astype(np.float32)
+    z = None if zp is None else (np.array([3], np.int32) if zp == "tensor" else rng.integers(-9, 9, N).astype(np.int32))
+    check(dev(A), A, B, scale, z, torch.float32, "w8_dequant_simt")
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 5, 16])
+@pytest.mark.parametrize("zp", [None, "tensor", "column"])
+@pytest.mark.parametrize("out", [torch.bfloat16, torch.float32])
+def test_decode_gemv(M, zp, out):
+    w = W.decode_gemv(M, K=1024, N=640, seed=M)
+    rng = np.random.default_rng(M)
+    z = None if zp is None else (np.array([-4], np.int32) if zp == "tensor" else rng.integers(-9, 9, 640).astype(np.int32))
+    kernel = "gemv_w8_bf16_mma" if zp is None else "gemv_w8_bf16_mma_zp"
+    check(bf16_dev(w.A_bits), w.A, w.W, w.scale, z, out, kernel)
+
+
+@pytest.mark.parametrize("M,K,N", [(4, 1024, 200), (4, 1030, 256), (17, 512, 256)])
+def test_decode_shapes_outside_gemv_fall_back_to_cuda_cores(M, K, N):
+    w = W.decode_gemv(M, K=K, N=N, seed=1)
+    check(bf16_dev(w.A_bits), w.A, w.W, w.scale, None, torch.bfloat16, "w8_dequant_simt")
+
+
+def test_gemv_ragged_k_and_scalar_scale():
+    w = W.decode_gemv(3, K=1000, N=384, seed=9)
+    check(bf16_dev(w.A_bits), w.A, w.W, w.scale[:1].copy(), None, torch.float32, "gemv_w8_bf16_mma")
