@@ -161,6 +161,29 @@ qmm_status dynamic_quantize_linear(const float* x, int64_t n, uint8_t* y, float*
                                    int32_t* row_sums, int64_t row_len, void* workspace, size_t workspace_bytes,
                                    void* stream);
 
+/*
+ * dynamic_quantize_linear_noalloc: the same operation and results as
+ * dynamic_quantize_linear, for callers that cannot allocate device memory and
+ * so cannot supply a workspace -- e.g. a plugin inside a host framework that
+ * owns all device memory, an engine whose memory is fixed at start-up, or a
+ * host thread that must not call cudaMalloc because it can synchronise the
+ * device. The pages have no counterpart; this is a library convenience.
+ *
+ * The scratch for the (min, max) partials is a fixed 8 KiB array inside the
+ * library (room for 1024 partials, which covers every n); every GPU that loads
+ * the library keeps it until the process exits. The call allocates nothing.
+ * The first call on a device looks the array's device address up (once, with
+ * that device current), so make that first call before any stream capture.
+ * All calls share the array: calls whose kernels overlap on the GPU race and
+ * give wrong results -- order them on one stream. Nothing in the array needs
+ * to start at zero. Arguments as for dynamic_quantize_linear (minus the
+ * workspace); QMM_ERR_UNSUPPORTED if the partials would not fit the array.
+ * This entry point does not update qmm_last_kernel()/qmm_last_cuda_error().
+ */
+qmm_status dynamic_quantize_linear_noalloc(const float* x, int64_t n, uint8_t* y, float* y_scale,
+                                           uint8_t* y_zero_point, int32_t* row_sums, int64_t row_len,
+                                           void* stream);
+
 /* Human-readable name of a status. Never NULL. */
 const char* qmm_status_string(int status);
 
