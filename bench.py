@@ -123,8 +123,15 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
 
 
+SPIN_CYCLES = 60000   # ~30 us of GPU spin: the host enqueues the timed call while it runs
+
+
 def time_gpu(fn, steps, warmup, flush=None):
-    """Per-iteration device time (ms) of fn, CUDA events on the current stream."""
+    """Per-iteration device time (ms) of fn, CUDA events on the current stream.
+
+    Before each timed call the stream runs the optional L2 flush and a short
+    spin kernel, so the host has enqueued the call (and its end event) before
+    the start event fires: host-side marshalling never shows up as device time."""
     import torch
     for _ in range(warmup):
         if flush is not None:
@@ -135,6 +142,7 @@ def time_gpu(fn, steps, warmup, flush=None):
     for i in range(steps):
         if flush is not None:
             flush()
+        torch.cuda._sleep(SPIN_CYCLES)
         ev[i][0].record()
         fn()
         ev[i][1].record()
@@ -195,8 +203,12 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="qmm", choices=["qmm", "reference"])
     ap.add_argument("--no-secondary", action="store_true", help="time only the headline workload")
+    ap.add_argument("--case", default=None, help="time one named workload alone and exit")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.case:
+        run_case(args)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -323,86 +335,134 @@ def main():
         dist.destroy_process_group()
 
 
+def case_setups(q, torch, peaks):
+    """Setup functions for each benchmark workload. Each returns (call, use_flush, report),
+    report(ms) -> dict. Inputs are created on the device before timing."""
+    hbm = peaks["hbm_gbs"]
+    tc = peaks["bf16_tflops"]
+
+    def a8w8():
+        w = W.a8w8_4096()
+        A, B = torch.from_numpy(w.A).cuda(), torch.from_numpy(w.B).cuda()
+        a_s, w_s = torch.from_numpy(w.act_scale).cuda(), torch.from_numpy(w.weight_scale).cuda()
+        C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        return (lambda: q.qmm_a8w8(A, B, a_s, w_s, out=C)), True, \
+            (lambda ms: {"us": ms * 1e3, "value": OPS / (ms * 1e-3) / 1e12, "unit": "TOPS"})
+
+    def gemv(Mg):
+        def setup():
+            g = W.decode_gemv(Mg)
+            Ad = torch.from_numpy(g.A_bits.view(np.int16)).view(torch.bfloat16).cuda()
+            Wd = torch.from_numpy(g.W).cuda()
+            sd = torch.from_numpy(g.scale).cuda()
+            Cd = torch.empty((Mg, 28672), dtype=torch.bfloat16, device="cuda")
+            nbytes = 8192 * 28672 + Mg * 8192 * 2 + 28672 * 4 + Mg * 28672 * 2
+
+            def report(ms):
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                return {"us": ms * 1e3, "value": gbs, "unit": "GB/s", "bound": "hbm", "frac": gbs / hbm,
+                        "algorithmic_bytes": nbytes}
+            # the weight stream (235 MB) exceeds L2: no flush needed
+            return (lambda: q.qmm_w8_dequant(Ad, Wd, sd, None, out=Cd)), False, report
+        return setup
+
+    def dql():
+        d = W.dql_matmul_integer_8192x4096x11008()
+        x = torch.from_numpy(d.x).cuda()
+        ws = torch.empty(q.dynamic_quantize_linear_workspace_bytes(x.numel()), dtype=torch.uint8, device="cuda")
+        n = x.numel()
+
+        def report(ms):
+            gbs = 9 * n / (ms * 1e-3) / 1e9
+            return {"us": ms * 1e3, "value": gbs, "unit": "GB/s", "bound": "hbm", "frac": gbs / hbm,
+                    "algorithmic_bytes": 9 * n,
+                    "note": f"9 B/element (x read twice, y written); {5 * n / (ms * 1e-3) / 1e9:.0f} GB/s "
+                            "against the 5 B/element floor"}
+        # x (134 MB) exceeds L2: no flush needed
+        return (lambda: q.dynamic_quantize_linear(x, row_len=4096, workspace=ws)), False, report
+
+    def mmi():
+        d = W.dql_matmul_integer_8192x4096x11008()
+        x = torch.from_numpy(d.x).cuda()
+        y, _, zp, _ = q.dynamic_quantize_linear(x, row_len=4096)
+        del x
+        Bd, bz = torch.from_numpy(d.B).cuda(), torch.from_numpy(d.b_zp).cuda()
+        Ci = torch.empty((8192, 11008), dtype=torch.int32, device="cuda")
+        ops = 2.0 * 8192 * 4096 * 11008
+
+        def report(ms):
+            tops = ops / (ms * 1e-3) / 1e12
+            return {"us": ms * 1e3, "value": tops, "unit": "TOPS", "bound": "tensor", "frac": tops / tc,
+                    "note": "inputs + int32 output (440 MB) exceed L2"}
+        return (lambda: q.matmul_integer(y, Bd, a_zero_point=zp, b_zero_point=bz, out=Ci)), False, report
+
+    def batched():
+        bm = W.batched_matmul_integer()
+        Ab, Bb = torch.from_numpy(bm.A).cuda(), torch.from_numpy(bm.B).cuda()
+        za = torch.tensor([bm.a_zp], dtype=torch.int8, device="cuda")
+        zb = torch.tensor([bm.b_zp], dtype=torch.int8, device="cuda")
+        Cb = torch.empty((8, 16, 512, 1024), dtype=torch.int32, device="cuda")
+        ops = 2.0 * 65536 * 1024 * 1024
+        nbytes = 65536 * 1024 + 1024 * 1024 + 65536 * 1024 * 4
+
+        def report(ms):
+            tops = ops / (ms * 1e-3) / 1e12
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            return {"us": ms * 1e3, "value": tops, "unit": "TOPS", "frac_tensor": tops / tc, "gbs": gbs,
+                    "frac_hbm": gbs / hbm}
+        return (lambda: q.matmul_integer(Ab, Bb, a_zero_point=za, b_zero_point=zb, out=Cb)), False, report
+
+    def w8():
+        sw = W.w8_dequant_f32_64x256x192()
+        As, Bs = torch.from_numpy(sw.A).cuda(), torch.from_numpy(sw.B).cuda()
+        ss, zs = torch.from_numpy(sw.scale).cuda(), torch.from_numpy(sw.zero_point).cuda()
+        Cs = torch.empty((64, 192), dtype=torch.float32, device="cuda")
+        return (lambda: q.qmm_w8_dequant(As, Bs, ss, zs, out=Cs)), True, \
+            (lambda ms: {"us": ms * 1e3, "unit": "us", "bound": "latency"})
+
+    return {"a8w8_4096x4096x4096_bf16": a8w8,
+            "decode_gemv_M1": gemv(1), "decode_gemv_M4": gemv(4), "decode_gemv_M16": gemv(16),
+            "dql_8192x4096": dql, "matmul_integer_8192x4096x11008": mmi,
+            "batched_matmul_integer_65536x1024x1024": batched, "w8_dequant_f32_64x256x192": w8}
+
+
+SECONDARY = ["decode_gemv_M1", "decode_gemv_M4", "decode_gemv_M16", "dql_8192x4096",
+             "matmul_integer_8192x4096x11008", "batched_matmul_integer_65536x1024x1024",
+             "w8_dequant_f32_64x256x192"]
+
+
 def secondary(q, torch, flush, clocks, peaks):
     out = {}
-    hbm = peaks["hbm_gbs"]
-    iters, warm = 20, 3
-
-    def timed(fn, use_flush=False):
+    setups = case_setups(q, torch, peaks)
+    for name in SECONDARY:
+        fn, use_flush, report = setups[name]()
         t0 = time.time()
-        ts = time_gpu(fn, iters, warm, flush=flush if use_flush else None)
+        ts = time_gpu(fn, 20, 3, flush=flush if use_flush else None)
         clocks.mark(t0, time.time())
-        return statistics.mean(ts)
-
-    # decode GEMV, M in {1, 4, 16}: weight stream 235 MB > L2, no flush needed
-    for Mg in (1, 4, 16):
-        g = W.decode_gemv(Mg)
-        Ad = torch.from_numpy(g.A_bits.view(np.int16)).view(torch.bfloat16).cuda()
-        Wd = torch.from_numpy(g.W).cuda()
-        sd = torch.from_numpy(g.scale).cuda()
-        Cd = torch.empty((Mg, 28672), dtype=torch.bfloat16, device="cuda")
-        ms = timed(lambda: q.qmm_w8_dequant(Ad, Wd, sd, None, out=Cd))
-        nbytes = 8192 * 28672 + Mg * 8192 * 2 + 28672 * 4 + Mg * 28672 * 2
-        gbs = nbytes / (ms * 1e-3) / 1e9
-        out[f"decode_gemv_M{Mg}"] = {"us": ms * 1e3, "value": gbs, "unit": "GB/s", "bound": "hbm",
-                                     "frac": gbs / hbm, "kernel": q.last_kernel(), "algorithmic_bytes": nbytes}
-        del Wd
-    torch.cuda.empty_cache()
-
-    # DynamicQuantizeLinear 8192x4096 then MatMulInteger 8192x4096x11008
-    d = W.dql_matmul_integer_8192x4096x11008()
-    x = torch.from_numpy(d.x).cuda()
-    Bd = torch.from_numpy(d.B).cuda()
-    bz = torch.from_numpy(d.b_zp).cuda()
-    ws = torch.empty(q.dynamic_quantize_linear_workspace_bytes(x.numel()), dtype=torch.uint8, device="cuda")
-    res = {}
-
-    def dql_call():
-        res["r"] = q.dynamic_quantize_linear(x, row_len=4096, workspace=ws)
-
-    ms = timed(dql_call)
-    n = x.numel()
-    gbs9 = 9 * n / (ms * 1e-3) / 1e9
-    out["dql_8192x4096"] = {"us": ms * 1e3, "value": gbs9, "unit": "GB/s", "bound": "hbm", "frac": gbs9 / hbm,
-                            "algorithmic_bytes": 9 * n, "note": "9 B/element (read x twice, write u8); "
-                            f"{5 * n / (ms * 1e-3) / 1e9:.0f} GB/s against the 5 B/element floor",
-                            "kernel": q.last_kernel()}
-    y, _, zp, _ = res["r"]
-    Ci = torch.empty((8192, 11008), dtype=torch.int32, device="cuda")
-    ms = timed(lambda: q.matmul_integer(y, Bd, a_zero_point=zp, b_zero_point=bz, out=Ci), use_flush=False)
-    ops = 2.0 * 8192 * 4096 * 11008
-    tops = ops / (ms * 1e-3) / 1e12
-    out["matmul_integer_8192x4096x11008"] = {"us": ms * 1e3, "value": tops, "unit": "TOPS", "bound": "tensor",
-                                             "frac": tops / peaks["bf16_tflops"], "kernel": q.last_kernel(),
-                                             "note": "inputs + int32 output 440 MB exceed L2"}
-    del x, Bd, Ci, y
-    torch.cuda.empty_cache()
-
-    # batched MatMulInteger, shared rank-2 B
-    bm = W.batched_matmul_integer()
-    Ab = torch.from_numpy(bm.A).cuda()
-    Bb = torch.from_numpy(bm.B).cuda()
-    za = torch.tensor([bm.a_zp], dtype=torch.int8, device="cuda")
-    zb = torch.tensor([bm.b_zp], dtype=torch.int8, device="cuda")
-    Cb = torch.empty((8, 16, 512, 1024), dtype=torch.int32, device="cuda")
-    ms = timed(lambda: q.matmul_integer(Ab, Bb, a_zero_point=za, b_zero_point=zb, out=Cb))
-    ops = 2.0 * 65536 * 1024 * 1024
-    tops = ops / (ms * 1e-3) / 1e12
-    nbytes = 65536 * 1024 + 1024 * 1024 + 65536 * 1024 * 4
-    out["batched_matmul_integer_65536x1024x1024"] = {
-        "us": ms * 1e3, "value": tops, "unit": "TOPS", "frac_tensor": tops / peaks["bf16_tflops"],
-        "gbs": nbytes / (ms * 1e-3) / 1e9, "frac_hbm": nbytes / (ms * 1e-3) / 1e9 / hbm, "kernel": q.last_kernel()}
-    del Ab, Cb
-    torch.cuda.empty_cache()
-
-    # small fp32 x int8 (latency-bound)
-    s = W.w8_dequant_f32_64x256x192()
-    As, Bs = torch.from_numpy(s.A).cuda(), torch.from_numpy(s.B).cuda()
-    ss, zs = torch.from_numpy(s.scale).cuda(), torch.from_numpy(s.zero_point).cuda()
-    Cs = torch.empty((64, 192), dtype=torch.float32, device="cuda")
-    ms = timed(lambda: q.qmm_w8_dequant(As, Bs, ss, zs, out=Cs), use_flush=True)
-    out["w8_dequant_f32_64x256x192"] = {"us": ms * 1e3, "unit": "us", "bound": "latency", "kernel": q.last_kernel()}
+        r = report(statistics.mean(ts))
+        r["kernel"] = q.last_kernel()
+        out[name] = r
+        del fn
+        torch.cuda.empty_cache()
     return out
+
+
+def run_case(args):
+    """Time one workload alone (used for profiler captures of a single kernel)."""
+    import torch
+    import quantized_int8_matmul_gb300 as q
+    peaks, _ = load_peaks()
+    setups = case_setups(q, torch, peaks)
+    fn, use_flush, report = setups[args.case]()
+    flush = None
+    if use_flush:
+        buf = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+        flush = lambda: buf.fill_(1)  # noqa: E731
+    ts = time_gpu(fn, args.steps, args.warmup, flush=flush)
+    q.check_device_error()
+    r = report(statistics.mean(ts))
+    r.update({"case": args.case, "kernel": q.last_kernel(), "steps": args.steps})
+    print(json.dumps(r), flush=True)
 
 
 if __name__ == "__main__":

@@ -28,6 +28,7 @@ namespace qmm {
 namespace dql {
 
 constexpr int THREADS = 256;
+constexpr int UNROLL = 8;               // 16-byte loads in flight per thread
 constexpr long long CHUNK_MIN = 32768;   // elements per pass-1 CTA at least
 
 __device__ __forceinline__ void block_minmax(float& lo, float& hi) {
@@ -70,14 +71,27 @@ __global__ void __launch_bounds__(THREADS) dql_minmax_kernel(const float* __rest
   chunk_range(n, gridDim.x, blockIdx.x, beg, end);
   float lo = 0.f, hi = 0.f;   // the range always includes 0
   if (vec) {
+    // UNROLL independent 16-byte loads in flight per thread
     const float4* x4 = reinterpret_cast<const float4*>(x);
-    for (long long i = beg / 4 + threadIdx.x; i < end / 4; i += THREADS) {
+    const long long e4 = end / 4;
+    long long i = beg / 4 + threadIdx.x;
+    for (; i + (UNROLL - 1) * THREADS < e4; i += UNROLL * THREADS) {
+      float4 v[UNROLL];
+#pragma unroll
+      for (int u = 0; u < UNROLL; ++u) v[u] = __ldg(x4 + i + u * THREADS);
+#pragma unroll
+      for (int u = 0; u < UNROLL; ++u) {
+        lo = fminf(lo, fminf(fminf(v[u].x, v[u].y), fminf(v[u].z, v[u].w)));
+        hi = fmaxf(hi, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
+      }
+    }
+    for (; i < e4; i += THREADS) {
       const float4 v = __ldg(x4 + i);
       lo = fminf(lo, fminf(fminf(v.x, v.y), fminf(v.z, v.w)));
       hi = fmaxf(hi, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
     }
-    for (long long i = (end / 4) * 4 + threadIdx.x; i < end; i += THREADS) {
-      const float v = __ldg(x + i);
+    for (long long j = e4 * 4 + threadIdx.x; j < end; j += THREADS) {
+      const float v = __ldg(x + j);
       lo = fminf(lo, v);
       hi = fmaxf(hi, v);
     }
@@ -128,6 +142,11 @@ __device__ __forceinline__ uint32_t quant1(float v, float scale, int zp) {
   return (uint32_t)y;
 }
 
+__device__ __forceinline__ uint32_t quant4(const float4 v, float scale, int zp) {
+  return quant1(v.x, scale, zp) | (quant1(v.y, scale, zp) << 8) | (quant1(v.z, scale, zp) << 16) |
+         (quant1(v.w, scale, zp) << 24);
+}
+
 __global__ void __launch_bounds__(THREADS) dql_quantize_kernel(const float* __restrict__ x, long long n, int vec,
                                                                const float* __restrict__ partials,
                                                                int num_partials, int num_chunks,
@@ -146,11 +165,16 @@ __global__ void __launch_bounds__(THREADS) dql_quantize_kernel(const float* __re
     if (vec) {
       const float4* x4 = reinterpret_cast<const float4*>(x);
       uint32_t* y4 = reinterpret_cast<uint32_t*>(y);
-      for (long long i = beg / 4 + threadIdx.x; i < end / 4; i += THREADS) {
-        const float4 v = __ldg(x4 + i);
-        y4[i] = quant1(v.x, sz.scale, zp) | (quant1(v.y, sz.scale, zp) << 8) | (quant1(v.z, sz.scale, zp) << 16) |
-                (quant1(v.w, sz.scale, zp) << 24);
+      const long long e4 = end / 4;
+      long long i = beg / 4 + threadIdx.x;
+      for (; i + (UNROLL - 1) * THREADS < e4; i += UNROLL * THREADS) {
+        float4 v[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) v[u] = __ldg(x4 + i + u * THREADS);
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) y4[i + u * THREADS] = quant4(v[u], sz.scale, zp);
       }
+      for (; i < e4; i += THREADS) y4[i] = quant4(__ldg(x4 + i), sz.scale, zp);
       for (long long i = (end / 4) * 4 + threadIdx.x; i < end; i += THREADS)
         y[i] = (uint8_t)quant1(__ldg(x + i), sz.scale, zp);
     } else {
@@ -183,12 +207,23 @@ __global__ void __launch_bounds__(THREADS) dql_quantize_rows_kernel(const float*
     if (vec) {
       const float4* x4 = reinterpret_cast<const float4*>(xr);
       uint32_t* y4 = reinterpret_cast<uint32_t*>(yr);
-      for (long long i = lane; i < row_len / 4; i += 32) {
-        const float4 v = __ldg(x4 + i);
-        const uint32_t q0 = quant1(v.x, sz.scale, zp), q1 = quant1(v.y, sz.scale, zp);
-        const uint32_t q2 = quant1(v.z, sz.scale, zp), q3 = quant1(v.w, sz.scale, zp);
-        y4[i] = q0 | (q1 << 8) | (q2 << 16) | (q3 << 24);
-        s += (int)(q0 + q1 + q2 + q3);
+      const long long r4 = row_len / 4;
+      long long i = lane;
+      for (; i + (UNROLL - 1) * 32 < r4; i += UNROLL * 32) {
+        float4 v[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) v[u] = __ldg(x4 + i + u * 32);
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+          const uint32_t w = quant4(v[u], sz.scale, zp);
+          y4[i + u * 32] = w;
+          s += (int)__dp4a(w, 0x01010101u, 0u);
+        }
+      }
+      for (; i < r4; i += 32) {
+        const uint32_t w = quant4(__ldg(x4 + i), sz.scale, zp);
+        y4[i] = w;
+        s += (int)__dp4a(w, 0x01010101u, 0u);
       }
     } else {
       for (long long i = lane; i < row_len; i += 32) {

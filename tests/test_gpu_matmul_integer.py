@@ -133,3 +133,15 @@ def test_k_zero_gives_zeros():
     C = q.matmul_integer(A, B)
     assert q.last_kernel() == "memset_zero"
     assert C.shape == (2, 3, 5) and torch.count_nonzero(C).item() == 0
+
+
+@pytest.mark.parametrize("adt,bdt", [("u8", "s8"), ("s8", "s8"), ("u8", "u8")])
+def test_long_k_row_and_column_sums(adt, bdt):
+    """K = 4160 (65 K-stages): the column sums are folded from 16-bit lanes several times per tile."""
+    rng = np.random.default_rng(12)
+    M, K, N = 130, 4160, 272
+    A, B = rand(rng, adt, (M, K)), rand(rng, bdt, (K, N))
+    if bdt == "s8":
+        B[:, :16] = -128            # extreme column sums
+    a_zp, b_zp = rand(rng, adt, (1,)), rand(rng, bdt, (N,))
+    assert_equal(run(A, B, a_zp, b_zp), oracle(A, B, a_zp, b_zp), f"{adt}x{bdt} K=4160")
