@@ -74,9 +74,9 @@ typedef enum {
  *  zero_point  device int32[zp_count], zp_count 0 (no zero point), 1 or N; may be
  *              NULL when zp_count is 0
  *  C           [M,N] output, c_dtype QMM_F32 or QMM_BF16 (round to nearest even)
- * Kernels: for bf16 A with 1 <= M <= 16 (the decode shape; K % 4 == 0,
- * N % 16 == 0, A 8-byte and B 16-byte aligned) a weight-streaming tensor-core
- * GEMV; otherwise a CUDA-core tiled kernel. Accumulation is fp32.
+ * Kernels: for bf16 A with 1 <= M <= 16 (the decode shape; K % 8 == 0,
+ * N % 16 == 0, A and B 16-byte aligned) a weight-streaming tensor-core GEMV
+ * fed by TMA; otherwise a CUDA-core tiled kernel. Accumulation is fp32.
  * Accuracy: |C - exact| <= 1e-3 * sum_k |A[m,k]*scale_n*(B[k,n]-zp_n)| + 1e-6,
  * plus half an ulp of the output type.
  */

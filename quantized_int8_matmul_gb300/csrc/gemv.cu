@@ -7,35 +7,55 @@
 // section "The kernel"). The small-M dispatch to this kernel follows the
 // decode path of PyPTO PR #1920 (reviews on choosing tile.gemv when M == 1).
 //
-// The weight stream is the whole cost (K*N bytes), so the kernel is built
-// around keeping HBM busy:
-//  * each lane issues 16-byte loads of four consecutive K rows of W
-//    (16 columns each), so a warp moves 2 KB of W per 16-K step and every
-//    byte is loaded exactly once;
-//  * the contraction uses mma.sync m16n8k16 (bf16 in, fp32 accumulate) with
-//    the activation rows as the MMA's M (zero-padded to 16). Inside each
-//    16-K step the K order is permuted -- fragment k index 2t,2t+1,2t+8,2t+9
-//    of lane t maps to actual k 4t..4t+3 -- applied identically to A and W,
-//    so a lane's four loaded rows are exactly the K values its fragments need
-//    and no data moves between lanes;
-//  * K is split over a cluster of 4 CTAs (8 warps each); warps reduce through
-//    shared memory and the cluster reduces through distributed shared memory,
-//    so there is no global workspace and the sum order is fixed.
+// The weight stream (K*N bytes, read once) is the whole cost, so the kernel
+// is built to keep HBM busy:
+//  * one producer warp streams stages of W (256 k-rows x 64 columns, 16 KB,
+//    64-byte swizzle) and of A (16 rows x 256 k, bf16, rows >= M zero-filled
+//    by the copy) into a 5-stage shared-memory ring with TMA
+//    (cp.async.bulk.tensor), so ~120 KB per SM are in flight without costing
+//    registers;
+//  * sixteen consumer warps each take one 16-deep K step of every stage and
+//    run mma.sync m16n8k16 (bf16 in, fp32 accumulate) with the activation rows
+//    as the MMA's M (zero-padded to 16) and 8 n8 tiles covering 64 columns;
+//  * the K order inside a step is permuted, identically for A and W: lane t of
+//    a warp handles rows rb(t) + {0, 2, 8, 10} with rb = {0, 1, 4, 5}, which
+//    gives the four row-groups of a half-warp distinct (row bit 0, row bit 2)
+//    and so makes the 8-byte shared-memory reads of the swizzled stage
+//    conflict-free;
+//  * persistent CTAs walk 64-column blocks of N (fine enough to balance the
+//    SMs) over the full K; the warps' partial sums are reduced through shared
+//    memory in a fixed order.
 #include "common.cuh"
 #include "kernels.h"
+#include "tma.h"
 
-#include <cooperative_groups.h>
-
-namespace cg = cooperative_groups;
+#include <algorithm>
 
 namespace qmm {
 namespace gemv {
 
-constexpr int NWARP = 8;
-constexpr int NTHR = NWARP * 32;
-constexpr int CL = 4;          // CTAs per cluster = K splits
-constexpr int BNW = 128;       // columns per CTA
-constexpr int NTILE = BNW / 8; // n8 tiles per warp
+constexpr int NCW = 16;                   // consumer warps, one 16-deep K step of a stage each
+constexpr int NTHR = (NCW + 1) * 32;      // + one producer warp
+constexpr int BNW = 64;                   // columns per block
+constexpr int BKS = 16 * NCW;             // K rows per stage (256)
+constexpr int NST = 5;                    // ring stages
+constexpr int W_BYTES = BKS * BNW;        // 16 KB
+constexpr int A_BOX = 16 * 64 * 2;        // one A box: 16 rows x 64 k bf16 (2 KB)
+constexpr int A_BOXES = BKS / 64;
+constexpr int STAGE = W_BYTES + A_BOXES * A_BOX;
+constexpr int NTILE = BNW / 8;            // n8 tiles per warp
+constexpr int NACC_MAX = NTILE * 4 + 4;
+
+struct Shared {
+  float red[NCW / 2][NACC_MAX][32];       // staged warp reduction
+  uint64_t full[NST];
+  uint64_t empty[NST];
+  int abort_flag;
+};
+
+constexpr size_t SMEM_BYTES = (size_t)NST * STAGE + sizeof(Shared) + 1024;
+
+enum : unsigned { SITE_FULL = 0x200, SITE_EMPTY = 0x201, SITE_DRAIN = 0x202 };
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
@@ -52,40 +72,86 @@ __device__ __forceinline__ float biased_byte_to_float(uint32_t xb, int b) {
   return __uint_as_float(bits) - 8388736.0f;
 }
 
+// Two floats that are small integers (|x| <= 128, so at most 8 significant
+// bits) have all-zero low 16 bits: their bf16 values are exactly their top
+// halves, so packing them is one byte permute (no rounding step needed).
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
+  return prmt(__float_as_uint(lo), __float_as_uint(hi), 0x7632u);
 }
 
-struct StepRegs {
-  uint4 w[4];    // W rows k0+4t+i, columns 16g .. 16g+15 (int8)
-  uint2 a_lo;    // A row g,   k0+4t .. k0+4t+3 (bf16)
-  uint2 a_hi;    // A row g+8
+__device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint4 lds_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ uint2 lds_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+// A[row][k] of the stage: 64-k boxes, 128-byte swizzle (16-byte chunk c of
+// row r stored at chunk position c ^ (r % 8)).
+__device__ __forceinline__ uint32_t a_addr(uint32_t a_base, int row, int k) {
+  const int box = k >> 6, kk = k & 63;
+  return a_base + (uint32_t)box * A_BOX + (uint32_t)row * 128u + ((uint32_t)((kk >> 3) ^ (row & 7)) << 4) +
+         (uint32_t)(kk & 7) * 2u;
+}
+
+// Shared-memory offsets (within a stage) of one lane's operands for its warp's
+// 16-deep K step: stage rows 16*warp + rb(t) + {0, 2, 8, 10}, rb = {0, 1, 4, 5}.
+// They are the same for every stage, so they are computed once.
+//  W stage: 64-byte rows, 64-byte swizzle (16-byte chunk c of row r stored at
+//  chunk position c ^ ((r >> 1) & 3)); this lane reads 8 bytes (columns 8g..8g+7).
+//  A stage: four 64-k boxes (see a_addr); this lane reads rows g and g + 8.
+struct StepOffsets {
+  uint32_t w[4];
+  uint32_t a[8];   // [h * 4 + i]: row g + 8h, k = kb + {0, 2, 8, 10}[i]
 };
 
-__device__ __forceinline__ void load_step(const GemvArgs& p, int step, int n_col, int g, int t, StepRegs& r) {
-  const int k = step * 16 + 4 * t;
-  const bool k_ok = k < p.K;                 // K % 4 == 0: the 4 rows are all in or all out
-  const bool n_ok = n_col < p.N;
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-    r.w[i] = (k_ok && n_ok) ? ldg_nc_v4(p.W + (size_t)(k + i) * p.N + n_col) : make_uint4(0, 0, 0, 0);
-  r.a_lo = (k_ok && g < p.M) ? __ldg(reinterpret_cast<const uint2*>(p.A + (size_t)g * p.K + k)) : make_uint2(0, 0);
-  r.a_hi = (k_ok && g + 8 < p.M) ? __ldg(reinterpret_cast<const uint2*>(p.A + (size_t)(g + 8) * p.K + k))
-                                 : make_uint2(0, 0);
-}
-
-template <bool HAS_ZP>
-__device__ __forceinline__ void compute_step(const StepRegs& r, float (&acc)[NTILE][4], float (&rs)[4]) {
-  // A fragment with the permuted K order: a0/a2 = row g, a1/a3 = row g+8.
-  const uint32_t a[4] = {r.a_lo.x, r.a_hi.x, r.a_lo.y, r.a_hi.y};
-  uint32_t xb[4][4];
+__device__ __forceinline__ StepOffsets step_offsets(int warp, int g, int t) {
+  StepOffsets o;
+  const int kb = 16 * warp + (t & 1) + 4 * (t >> 1);
+  const int ro[4] = {0, 2, 8, 10};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    xb[i][0] = r.w[i].x ^ 0x80808080u;
-    xb[i][1] = r.w[i].y ^ 0x80808080u;
-    xb[i][2] = r.w[i].z ^ 0x80808080u;
-    xb[i][3] = r.w[i].w ^ 0x80808080u;
+    const int r = kb + ro[i];
+    o.w[i] = (uint32_t)r * 64u + ((uint32_t)((g >> 1) ^ ((r >> 1) & 3)) << 4) + (uint32_t)(g & 1) * 8u;
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) o.a[h * 4 + i] = a_addr((uint32_t)W_BYTES, g + 8 * h, kb + ro[i]);
+  return o;
+}
+
+// One 16-deep K step of this warp on the stage at `sbase`.
+template <bool HAS_ZP>
+__device__ __forceinline__ void compute_step(uint32_t sbase, const StepOffsets& o, float (&acc)[NTILE][4],
+                                             float (&rs)[4]) {
+  uint32_t a[4];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {        // h = 0: row g (a0, a2); h = 1: row g + 8 (a1, a3)
+    const uint32_t k0 = lds_u16(sbase + o.a[h * 4 + 0]);
+    const uint32_t k1 = lds_u16(sbase + o.a[h * 4 + 1]);
+    const uint32_t k2 = lds_u16(sbase + o.a[h * 4 + 2]);
+    const uint32_t k3 = lds_u16(sbase + o.a[h * 4 + 3]);
+    a[h] = prmt(k0, k1, 0x5410u);
+    a[2 + h] = prmt(k2, k3, 0x5410u);
+  }
+  uint32_t xb[4][2];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint2 w = lds_v2(sbase + o.w[i]);
+    xb[i][0] = w.x ^ 0x80808080u;
+    xb[i][1] = w.y ^ 0x80808080u;
   }
 #pragma unroll
   for (int j = 0; j < NTILE; ++j) {
@@ -95,138 +161,180 @@ __device__ __forceinline__ void compute_step(const StepRegs& r, float (&acc)[NTI
     mma_bf16(acc[j], a, b0, b1);
   }
   if (HAS_ZP) {
-    const uint32_t ones = 0x3F803F80u;   // bf16 (1, 1): the tile accumulates sum_k A[m,k]
+    const uint32_t ones = 0x3F803F80u;   // bf16 (1, 1): this tile accumulates sum_k A[m,k]
     mma_bf16(rs, a, ones, ones);
   }
 }
 
+__device__ __forceinline__ void consumer_bar() { asm volatile("bar.sync 1, %0;" ::"n"(NCW * 32) : "memory"); }
+
 template <bool HAS_ZP>
-__global__ void __cluster_dims__(CL, 1, 1) __launch_bounds__(NTHR, 2) gemv_kernel(const GemvArgs p) {
+__global__ void __launch_bounds__(NTHR, 1)
+    gemv_tma_kernel(const GemvArgs p, const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
+                    unsigned* err) {
   constexpr int NACC = NTILE * 4 + (HAS_ZP ? 4 : 0);
-  __shared__ float red[4][NACC][32];        // staged warp reduction (4 writer warps per round)
-  cg::cluster_group cluster = cg::this_cluster();
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  Shared& sm = *reinterpret_cast<Shared*>(smem_raw + (sbase - raw) + NST * STAGE);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int nblocks = (p.N + BNW - 1) / BNW;
+  const int spt = (p.K + BKS - 1) / BKS;   // stages per block
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < NST; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], NCW);
+    }
+    sm.abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+
+  if (warp == NCW) {
+    // ---------------- producer ----------------
+    if (lane == 0) {
+      prefetch_tmap(&tmW);
+      prefetch_tmap(&tmA);
+      int it = 0;
+      bool ok = true;
+      for (int nb = blockIdx.x; nb < nblocks && ok; nb += gridDim.x) {
+        for (int s = 0; s < spt; ++s, ++it) {
+          const int slot = it % NST;
+          if (it >= NST && !mbar_wait(&sm.empty[slot], (uint32_t)(((it / NST) - 1) & 1), &sm.abort_flag, err, SITE_EMPTY)) {
+            ok = false;
+            break;
+          }
+          const uint32_t dst = sbase + (uint32_t)slot * STAGE;
+          mbar_arrive_expect_tx(&sm.full[slot], STAGE);
+          tma_load_2d(dst, &tmW, nb * BNW, s * BKS, &sm.full[slot]);
+#pragma unroll
+          for (int b = 0; b < A_BOXES; ++b)
+            tma_load_2d(dst + W_BYTES + b * A_BOX, &tmA, s * BKS + 64 * b, 0, &sm.full[slot]);
+        }
+      }
+      // Before the CTA exits, wait (bounded) until every copy issued has landed.
+      for (int j = (it > NST ? it - NST : 0); j < it; ++j)
+        mbar_wait(&sm.full[j % NST], (uint32_t)((j / NST) & 1), nullptr, err, SITE_DRAIN);
+    }
+    __syncwarp();
+    return;
+  }
+
+  // ---------------- consumers ----------------
   const int g = lane >> 2;
   const int t = lane & 3;
-  const int rank = (int)cluster.block_rank();
-  const int nb = blockIdx.x / CL;
-  const int n_col = nb * BNW + 16 * g;
+  const StepOffsets so = step_offsets(warp, g, t);
+  int it = 0;
+  bool ok = true;
+  for (int nb = blockIdx.x; nb < nblocks; nb += gridDim.x) {
+    float acc[NTILE][4];
+    float rs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < NTILE; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
 
-  const int steps = (p.K + 15) / 16;
-  const int s_beg = (int)(((long long)steps * rank) / CL);
-  const int s_end = (int)(((long long)steps * (rank + 1)) / CL);
-
-  float acc[NTILE][4];
-  float rs[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-  for (int j = 0; j < NTILE; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-
-  // Two steps of loads in flight per warp.
-  StepRegs r0, r1;
-  int s = s_beg + warp;
-  if (s < s_end) load_step(p, s, n_col, g, t, r0);
-  if (s + NWARP < s_end) load_step(p, s + NWARP, n_col, g, t, r1);
-  for (; s < s_end; s += NWARP) {
-    StepRegs r2;
-    if (s + 2 * NWARP < s_end) load_step(p, s + 2 * NWARP, n_col, g, t, r2);
-    compute_step<HAS_ZP>(r0, acc, rs);
-    r0 = r1;
-    r1 = r2;
-  }
-
-  // Warp reduction inside the CTA, fixed order: 4..7 -> 0..3, then 2,3 -> 0,1, then 1 -> 0.
-  auto put = [&](int slot) {
-#pragma unroll
-    for (int j = 0; j < NTILE; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) red[slot][j * 4 + e][lane] = acc[j][e];
-    if (HAS_ZP)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) red[slot][NTILE * 4 + e][lane] = rs[e];
-  };
-  auto take = [&](int slot) {
-#pragma unroll
-    for (int j = 0; j < NTILE; ++j)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[j][e] += red[slot][j * 4 + e][lane];
-    if (HAS_ZP)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) rs[e] += red[slot][NTILE * 4 + e][lane];
-  };
-#pragma unroll 1
-  for (int half = NWARP / 2; half >= 1; half >>= 1) {
-    if (warp >= half && warp < 2 * half) put(warp - half);
-    __syncthreads();
-    if (warp < half) take(warp);
-    __syncthreads();
-  }
-  if (warp == 0) put(0);
-
-  // Cluster reduction: rank 0 adds ranks 1..CL-1 in order through DSMEM.
-  cluster.sync();
-  if (rank == 0 && warp == 0) {
-#pragma unroll 1
-    for (int rr = 1; rr < CL; ++rr) {
-      float(*peer)[NACC][32] = cluster.map_shared_rank(red, rr);
-#pragma unroll
-      for (int j = 0; j < NTILE; ++j)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[j][e] += peer[0][j * 4 + e][lane];
-      if (HAS_ZP)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) rs[e] += peer[0][NTILE * 4 + e][lane];
+    for (int s = 0; s < spt; ++s, ++it) {
+      const int slot = it % NST;
+      if (ok) ok = mbar_wait(&sm.full[slot], (uint32_t)((it / NST) & 1), &sm.abort_flag, err, SITE_FULL);
+      if (ok) compute_step<HAS_ZP>(sbase + (uint32_t)slot * STAGE, so, acc, rs);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.empty[slot]);
     }
-  }
-  cluster.sync();   // peers keep their shared memory alive until rank 0 has read it
 
-  if (rank == 0 && warp == 0) {
-    // Fragment element e of tile j: row g + 8*(e>>1), fragment column 2t + (e&1),
-    // which is actual column nb*128 + 16*(2t + (e&1)) + j.
+    // Reduce the eight warps' partials in a fixed order: 4..7 -> 0..3, 2,3 -> 0,1, 1 -> 0.
+#pragma unroll 1
+    for (int half = NCW / 2; half >= 1; half >>= 1) {
+      if (warp >= half && warp < 2 * half) {
 #pragma unroll
-    for (int j = 0; j < NTILE; ++j) {
+        for (int j = 0; j < NTILE; ++j)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int m = g + 8 * (e >> 1);
-        const int n = nb * BNW + 16 * (2 * t + (e & 1)) + j;
-        if (m < p.M && n < p.N) {
-          const float sc = __ldg(p.scale + (p.scale_count == 1 ? 0 : n));
-          float v = acc[j][e];
-          if (HAS_ZP) {
-            const float zp = (float)__ldg(p.zp + (p.zp_count == 1 ? 0 : n));
-            v = __fsub_rn(v, __fmul_rn(zp, rs[e & 2]));
+          for (int e = 0; e < 4; ++e) sm.red[warp - half][j * 4 + e][lane] = acc[j][e];
+        if (HAS_ZP)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) sm.red[warp - half][NTILE * 4 + e][lane] = rs[e];
+      }
+      consumer_bar();
+      if (warp < half) {
+#pragma unroll
+        for (int j = 0; j < NTILE; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[j][e] += sm.red[warp][j * 4 + e][lane];
+        if (HAS_ZP)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) rs[e] += sm.red[warp][NTILE * 4 + e][lane];
+      }
+      consumer_bar();
+    }
+    (void)NACC;
+
+    if (warp == 0 && ok) {
+      // Fragment element e of tile j: row g + 8*(e>>1), fragment column 2t + (e&1),
+      // which is actual column nb*64 + 8*(2t + (e&1)) + j.
+#pragma unroll
+      for (int j = 0; j < NTILE; ++j) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int m = g + 8 * (e >> 1);
+          const int n = nb * BNW + 8 * (2 * t + (e & 1)) + j;
+          if (m < p.M && n < p.N) {
+            const float sc = __ldg(p.scale + (p.scale_count == 1 ? 0 : n));
+            float v = acc[j][e];
+            if (HAS_ZP) {
+              const float zp = (float)__ldg(p.zp + (p.zp_count == 1 ? 0 : n));
+              v = __fsub_rn(v, __fmul_rn(zp, rs[e & 2]));
+            }
+            v = __fmul_rn(sc, v);
+            if (p.c_f32)
+              reinterpret_cast<float*>(p.C)[(size_t)m * p.N + n] = v;
+            else
+              reinterpret_cast<__nv_bfloat16*>(p.C)[(size_t)m * p.N + n] = __float2bfloat16_rn(v);
           }
-          v = __fmul_rn(sc, v);
-          if (p.c_f32)
-            reinterpret_cast<float*>(p.C)[(size_t)m * p.N + n] = v;
-          else
-            reinterpret_cast<__nv_bfloat16*>(p.C)[(size_t)m * p.N + n] = __float2bfloat16_rn(v);
         }
       }
     }
   }
 }
 
+template <bool HAS_ZP>
+cudaError_t launch_impl(const GemvArgs& a, const CUtensorMap& tw, const CUtensorMap& ta, cudaStream_t s) {
+  auto kern = gemv_tma_kernel<HAS_ZP>;
+  static unsigned attr_mask = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 32 || !(attr_mask & (1u << dev))) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    if (dev < 32) attr_mask |= 1u << dev;
+  }
+  const int nblocks = (a.N + BNW - 1) / BNW;
+  const int grid = std::min(nblocks, num_sms());
+  kern<<<grid, NTHR, SMEM_BYTES, s>>>(a, tw, ta, a.err);
+  return cudaGetLastError();
+}
+
 }  // namespace gemv
 
 bool gemv_supported(long long M, long long K, long long N, const void* A, const void* W) {
-  return M >= 1 && M <= 16 && K >= 4 && K % 4 == 0 && N % 16 == 0 && (reinterpret_cast<uintptr_t>(A) % 8) == 0 &&
-         (reinterpret_cast<uintptr_t>(W) % 16) == 0;
+  return M >= 1 && M <= 16 && K >= 8 && K % 8 == 0 && N >= 16 && N % 16 == 0 &&
+         (reinterpret_cast<uintptr_t>(A) % 16) == 0 && (reinterpret_cast<uintptr_t>(W) % 16) == 0;
 }
 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, const char** kernel_name) {
   using namespace gemv;
-  const int nblocks = (a.N + BNW - 1) / BNW;
-  const dim3 grid(nblocks * CL);
+  CUtensorMap tw, ta;
+  cudaError_t e = make_tmap_2d(&tw, a.W, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)a.N, (uint64_t)a.K,
+                               (uint64_t)a.N, BNW, BKS, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_2d(&ta, a.A, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (uint64_t)a.K, (uint64_t)a.M, (uint64_t)a.K * 2, 64,
+                   16, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
   if (a.zp_count > 0) {
-    *kernel_name = "gemv_w8_bf16_mma_zp";
-    gemv_kernel<true><<<grid, NTHR, 0, s>>>(a);
-  } else {
-    *kernel_name = "gemv_w8_bf16_mma";
-    gemv_kernel<false><<<grid, NTHR, 0, s>>>(a);
+    *kernel_name = "gemv_w8_bf16_tma_zp";
+    return launch_impl<true>(a, tw, ta, s);
   }
-  return cudaGetLastError();
+  *kernel_name = "gemv_w8_bf16_tma";
+  return launch_impl<false>(a, tw, ta, s);
 }
 
 }  // namespace qmm

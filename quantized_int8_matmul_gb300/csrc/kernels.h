@@ -45,6 +45,7 @@ struct GemvArgs {
   const float* scale; int scale_count;        // 1 or N
   const int32_t* zp;  int zp_count;           // 0, 1 or N
   void* C; int c_f32;                         // [M][N] bf16 (0) or f32 (1)
+  unsigned* err;                              // device error word
 };
 bool gemv_supported(long long M, long long K, long long N, const void* A, const void* W);
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, const char** kernel_name);

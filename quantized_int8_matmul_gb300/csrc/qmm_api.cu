@@ -160,6 +160,8 @@ qmm_status qmm_w8_dequant(const void* A, int a_dtype, const int8_t* B, int64_t M
     g.zp_count = (int)zp_count;
     g.C = C;
     g.c_f32 = c_dtype == QMM_F32;
+    g.err = err_word();
+    if (!g.err) return QMM_ERR_CUDA;
     return finish_launch(launch_gemv(g, s, &name), name);
   }
   if ((M + 63) / 64 > 65535) return QMM_ERR_UNSUPPORTED;

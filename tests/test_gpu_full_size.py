@@ -59,7 +59,7 @@ def test_dql_then_matmul_integer_8192x4096x11008():
 def test_decode_gemv_8192x28672(M):
     w = W.decode_gemv(M)
     C = q.qmm_w8_dequant(bf16_dev(w.A_bits), dev(w.W), dev(w.scale), None, out_dtype=torch.bfloat16)
-    assert q.last_kernel() == "gemv_w8_bf16_mma"
+    assert q.last_kernel() == "gemv_w8_bf16_tma"
     got = bf16_bits_to_f64(host(C))
     cols = sample(28672, 1024, 3)
     zp0 = np.zeros(1, np.int32)

@@ -49,7 +49,7 @@ def test_decode_gemv(M, zp, out):
     w = W.decode_gemv(M, K=1024, N=640, seed=M)
     rng = np.random.default_rng(M)
     z = None if zp is None else (np.array([-4], np.int32) if zp == "tensor" else rng.integers(-9, 9, 640).astype(np.int32))
-    kernel = "gemv_w8_bf16_mma" if zp is None else "gemv_w8_bf16_mma_zp"
+    kernel = "gemv_w8_bf16_tma" if zp is None else "gemv_w8_bf16_tma_zp"
     check(bf16_dev(w.A_bits), w.A, w.W, w.scale, z, out, kernel)
 
 
@@ -61,4 +61,4 @@ def test_decode_shapes_outside_gemv_fall_back_to_cuda_cores(M, K, N):
 
 def test_gemv_ragged_k_and_scalar_scale():
     w = W.decode_gemv(3, K=1000, N=384, seed=9)
-    check(bf16_dev(w.A_bits), w.A, w.W, w.scale[:1].copy(), None, torch.float32, "gemv_w8_bf16_mma")
+    check(bf16_dev(w.A_bits), w.A, w.W, w.scale[:1].copy(), None, torch.float32, "gemv_w8_bf16_tma")
