@@ -18,4 +18,10 @@ cudaError_t make_tmap_2d(CUtensorMap* map, const void* base, CUtensorMapDataType
                          uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer,
                          CUtensorMapSwizzle swizzle);
 
+// 3-D variant: dims {inner, mid, outer} with strides {mid_bytes, outer_bytes}
+// between consecutive mid and outer indices, box {box_inner, box_mid, 1}.
+cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, uint64_t inner,
+                         uint64_t mid, uint64_t outer, uint64_t mid_bytes, uint64_t outer_bytes,
+                         uint32_t box_inner, uint32_t box_mid, CUtensorMapSwizzle swizzle);
+
 }  // namespace qmm
