@@ -134,6 +134,19 @@ __device__ __forceinline__ ScaleZp reduce_partials(const float* __restrict__ par
   return s_out;
 }
 
+// x / scale, correctly rounded to nearest even, by Markstein's correction
+// (P. Markstein, "Computation of elementary functions on the IBM RISC
+// System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with r = RN(1/scale),
+// q = RN(x*r) is within an ulp of x/scale, e = x - q*scale is exact as one
+// FMA, and RN(q + e*r) is the correctly rounded quotient (a quotient of two
+// floats is never exactly halfway between two floats). Valid while 1/scale is
+// finite and normal; the callers fall back to IEEE division otherwise.
+__device__ __forceinline__ float div_markstein(float x, float scale, float r) {
+  const float q = __fmul_rn(x, r);
+  const float e = __fmaf_rn(-q, scale, x);
+  return __fmaf_rn(e, r, q);
+}
+
 __device__ __forceinline__ uint32_t quant1(float v, float scale, int zp) {
   float q = rintf(__fdiv_rn(v, scale));
   q = fminf(fmaxf(q, -1024.f), 1024.f);   // keeps the int conversion in range; saturation follows
@@ -142,9 +155,27 @@ __device__ __forceinline__ uint32_t quant1(float v, float scale, int zp) {
   return (uint32_t)y;
 }
 
-__device__ __forceinline__ uint32_t quant4(const float4 v, float scale, int zp) {
+// Same as quant1, with the division done by div_markstein (r = RN(1/scale)).
+__device__ __forceinline__ uint32_t quant1r(float v, float scale, float r, int zp) {
+  float q = rintf(div_markstein(v, scale, r));
+  q = fminf(fmaxf(q, -1024.f), 1024.f);
+  int y = __float2int_rn(q) + zp;
+  y = min(max(y, 0), 255);
+  return (uint32_t)y;
+}
+
+__device__ __forceinline__ uint32_t quant4(const float4 v, float scale, float r, int zp) {
+  if (r != 0.f)
+    return quant1r(v.x, scale, r, zp) | (quant1r(v.y, scale, r, zp) << 8) | (quant1r(v.z, scale, r, zp) << 16) |
+           (quant1r(v.w, scale, r, zp) << 24);
   return quant1(v.x, scale, zp) | (quant1(v.y, scale, zp) << 8) | (quant1(v.z, scale, zp) << 16) |
          (quant1(v.w, scale, zp) << 24);
+}
+
+// RN(1/scale) when it is finite and normal (and 1/r is finite), else 0 (= use IEEE division).
+__device__ __forceinline__ float safe_recip(float scale) {
+  const float r = __frcp_rn(scale);
+  return (isfinite(r) && fabsf(r) >= 1.17549435e-38f && fabsf(r) <= 1.0e37f) ? r : 0.f;
 }
 
 __global__ void __launch_bounds__(THREADS) dql_quantize_kernel(const float* __restrict__ x, long long n, int vec,
@@ -158,6 +189,7 @@ __global__ void __launch_bounds__(THREADS) dql_quantize_kernel(const float* __re
     *y_zp = (uint8_t)(int)sz.zp;
   }
   const int zp = (int)sz.zp;
+  const float rcp = safe_recip(sz.scale);
   // reverse chunk order: start where pass 1 finished
   for (int c = (int)gridDim.x - 1 - (int)blockIdx.x; c >= 0 && c < num_chunks; c -= (int)gridDim.x) {
     long long beg, end;
@@ -172,9 +204,9 @@ __global__ void __launch_bounds__(THREADS) dql_quantize_kernel(const float* __re
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) v[u] = __ldg(x4 + i + u * THREADS);
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) y4[i + u * THREADS] = quant4(v[u], sz.scale, zp);
+        for (int u = 0; u < UNROLL; ++u) y4[i + u * THREADS] = quant4(v[u], sz.scale, rcp, zp);
       }
-      for (; i < e4; i += THREADS) y4[i] = quant4(__ldg(x4 + i), sz.scale, zp);
+      for (; i < e4; i += THREADS) y4[i] = quant4(__ldg(x4 + i), sz.scale, rcp, zp);
       for (long long i = (end / 4) * 4 + threadIdx.x; i < end; i += THREADS)
         y[i] = (uint8_t)quant1(__ldg(x + i), sz.scale, zp);
     } else {
@@ -196,6 +228,7 @@ __global__ void __launch_bounds__(THREADS) dql_quantize_rows_kernel(const float*
     *y_zp = (uint8_t)(int)sz.zp;
   }
   const int zp = (int)sz.zp;
+  const float rcp = safe_recip(sz.scale);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long total_warps = (long long)gridDim.x * (THREADS / 32);
   // reverse row order, as in the flat kernel
@@ -215,13 +248,13 @@ __global__ void __launch_bounds__(THREADS) dql_quantize_rows_kernel(const float*
         for (int u = 0; u < UNROLL; ++u) v[u] = __ldg(x4 + i + u * 32);
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-          const uint32_t w = quant4(v[u], sz.scale, zp);
+          const uint32_t w = quant4(v[u], sz.scale, rcp, zp);
           y4[i + u * 32] = w;
           s += (int)__dp4a(w, 0x01010101u, 0u);
         }
       }
       for (; i < r4; i += 32) {
-        const uint32_t w = quant4(__ldg(x4 + i), sz.scale, zp);
+        const uint32_t w = quant4(__ldg(x4 + i), sz.scale, rcp, zp);
         y4[i] = w;
         s += (int)__dp4a(w, 0x01010101u, 0u);
       }

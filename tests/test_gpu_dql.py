@@ -87,3 +87,18 @@ def test_empty_input():
     x = torch.empty(0, dtype=torch.float32, device="cuda")
     y, s, zp = q.dynamic_quantize_linear(x)
     assert float(s.item()) == 1.0 and int(zp.item()) == 0 and y.numel() == 0
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2, 3])
+def test_quotients_near_halfway(seed):
+    """x/scale lands within a few ulps of k + 1/2: the rounded quotient decides the byte."""
+    rng = np.random.default_rng(100 + seed)
+    lo, hi = -np.float32(rng.uniform(0.1, 50)), np.float32(rng.uniform(0.1, 50))
+    scale = np.float32(np.float32(hi - lo) / np.float32(255))
+    k = rng.integers(-200, 200, 200000).astype(np.float32)
+    base = ((k + np.float32(0.5)) * scale).astype(np.float32)
+    ulps = rng.integers(-3, 4, base.size).astype(np.int32)
+    x = (base.view(np.int32) + ulps).view(np.float32)
+    x = np.clip(x, lo, hi).astype(np.float32)
+    x[:2] = [lo, hi]
+    check(x, f"near-halfway seed={seed}")
