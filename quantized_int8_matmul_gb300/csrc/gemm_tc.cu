@@ -22,15 +22,20 @@
 //    + K*za*zb, exact modulo 2^32. rowsum(A) and colsum(B) are computed by the
 //    converter warps from the same bytes they convert, in the same pass.
 //
-// CTA organisation (one persistent CTA per SM, 288 threads):
-//  * warps 0-7 ("workers"): load 8-bit tiles from global memory into
-//    registers (two stages of prefetch), convert them to fp16 and write them to
-//    shared memory in the canonical 128-byte-swizzled layouts the MMA reads
-//    (A K-major, B MN-major); keep the row/column sums; drain the TMEM
-//    accumulator after each K-chunk; run the epilogue and store C.
+// CTA organisation (one persistent CTA per SM, 320 threads):
+//  * warp 9 (producer): one lane copies 8-bit tiles of A (128 rows x 64 k) and
+//    B (64 k x 256 columns) from global memory into a 4-stage shared-memory
+//    staging ring with TMA (cp.async.bulk.tensor, completion counted on the
+//    stage's mbarrier); out-of-range rows and columns arrive as zeros.
+//  * warps 0-7 ("workers"): read a staged stage with 16-byte shared loads,
+//    convert the bytes to fp16 (byte in the mantissa of 1024, bias subtracted)
+//    and write them into a 2-stage ring in the canonical 128-byte-swizzled
+//    layouts the MMA reads (A K-major, B MN-major, so B is never transposed);
+//    keep the row/column sums; drain the TMEM accumulator after each K-chunk;
+//    run the epilogue and store C.
 //  * warp 8: allocates TMEM and, from one lane, issues the MMAs
 //    (M=128, N=256, K=16 per instruction) and the commits.
-// Tile: 128 x 256 outputs, K stage 64, 4 shared-memory stages (48 KB each).
+// Tile: 128 x 256 outputs, K stage 64; fp16 stage 48 KB, int8 stage 24 KB.
 // TMEM: columns [0,256) the fp32 chunk accumulator, [256,512) the int32 sums.
 #include "common.cuh"
 #include "kernels.h"
