@@ -321,7 +321,7 @@ def main():
                    "contraction": "exact int8 products on tcgen05 kind::f16 (fp16 operands), "
                                   "K-chunked fp32 TMEM accumulator drained to int32"},
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"], "traffic": kernel_traffic("gemm_tc05_exact_a8w8"),
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": kernel_traffic(kernel_name),
                      "peak_source": f"{peaks_src} dense bf16 (burst); fp16 kind::f16 runs at the same rate"},
         "cpu_baseline": cpu,
         "e2e": {"value": world * OPS / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS", "h2d_bytes_per_step": h2d,

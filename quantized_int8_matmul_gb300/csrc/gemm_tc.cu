@@ -749,6 +749,8 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, bool a_u8, bool b_u8, bool mmi, in
                    (a.a_bstride % 16 == 0) && (a.b_bstride % 16 == 0);
   const int celem = (mmi || a.c_f32) ? 4 : 2;
   const int c_vec = ((reinterpret_cast<uintptr_t>(a.C) % 16) == 0) && (((long long)a.N * celem) % 16 == 0);
+  // Large aligned problems run on SM pairs (half of B per SM in shared memory).
+  if (vec && a.M >= 256) return launch_gemm_tc_pair(a, a_u8, b_u8, mmi, chunk_k, c_vec, s, kernel_name);
   CUtensorMap ta{}, tb{};
   if (vec) {
     const cudaError_t e = make_operand_maps(a, &ta, &tb);

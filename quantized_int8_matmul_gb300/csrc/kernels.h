@@ -32,6 +32,11 @@ struct GemmArgs {
 cudaError_t launch_gemm_tc(const GemmArgs& a, bool a_u8, bool b_u8, bool mmi, int chunk_k, cudaStream_t s,
                            const char** kernel_name);
 
+// The same GEMM on a CTA pair (tcgen05 cta_group::2, 256 x 256 pair tiles).
+// Requires 16-byte-aligned operand rows (the TMA path) and M >= 256.
+cudaError_t launch_gemm_tc_pair(const GemmArgs& a, bool a_u8, bool b_u8, bool mmi, int chunk_k, int c_vec,
+                                cudaStream_t s, const char** kernel_name);
+
 // Largest exact chunk length for the operand signedness (fp32 sums <= 2^24).
 int gemm_default_chunk_k(bool a_u8, bool b_u8);
 

@@ -51,3 +51,13 @@ def assert_equal(got: np.ndarray, want: np.ndarray, what: str):
         i = np.argwhere(bad)[0]
         raise AssertionError(f"{what}: {int(bad.sum())} of {got.size} elements differ; first at {tuple(i)}: "
                              f"got {got[tuple(i)]!r}, want {want[tuple(i)]!r}")
+
+
+def gemm_kernel(form: str, M: int, K: int, N: int) -> str:
+    """Name of the exact-GEMM kernel the library is expected to launch: the SM-pair
+    kernel for 16-byte-aligned rows and M >= 256 (M after folding a batch), the
+    single-SM TMA kernel for other aligned shapes, the byte-wise one otherwise."""
+    vec = K % 16 == 0 and N % 16 == 0
+    if vec and M >= 256:
+        return f"gemm_tc05_pair_exact_{form}"
+    return f"gemm_tc05_exact_{form}" + ("" if vec else "_bytewise")

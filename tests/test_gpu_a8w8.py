@@ -8,7 +8,7 @@ import torch
 
 import qmm_workloads as W
 from oracle import qmm_oracle as O
-from _helpers import assert_equal, assert_within, bf16_bits_to_f64, dev, host
+from _helpers import assert_equal, assert_within, bf16_bits_to_f64, dev, gemm_kernel, host
 
 pytestmark = pytest.mark.gpu
 q = pytest.importorskip("quantized_int8_matmul_gb300")
@@ -29,8 +29,7 @@ def run(A, B, a_s, w_s, out):
 def test_a8w8_matches_oracle(M, K, N, out):
     w = W.a8w8(M, K, N, seed=M * 7 + K * 3 + N)
     got = run(w.A, w.B, w.act_scale, w.weight_scale, out)
-    vec = K % 16 == 0 and N % 16 == 0
-    assert q.last_kernel() == ("gemm_tc05_exact_a8w8" if vec else "gemm_tc05_exact_a8w8_bytewise")
+    assert q.last_kernel() == gemm_kernel("a8w8", M, K, N)
     want = O.a8w8(w.A, w.B, w.act_scale, w.weight_scale, out)
     assert_equal(got, want, f"a8w8 {out} {M}x{K}x{N}")
     exact = O.a8w8_exact(w.A, w.B, w.act_scale, w.weight_scale)

@@ -31,7 +31,7 @@ def test_a8w8_4096():
     w = W.a8w8_4096()
     C = q.qmm_a8w8(dev(w.A), dev(w.B), dev(w.act_scale), dev(w.weight_scale), out_dtype=torch.bfloat16)
     q.check_device_error()
-    assert q.last_kernel() == "gemm_tc05_exact_a8w8"
+    assert q.last_kernel() == "gemm_tc05_pair_exact_a8w8"
     got = host(C)
     rows = sample(4096, 40, 1)
     want = O.a8w8(w.A[rows], w.B, w.act_scale[rows], w.weight_scale, "bf16")
@@ -49,7 +49,7 @@ def test_dql_then_matmul_integer_8192x4096x11008():
     # the zero point stays on the device between the two calls
     C = q.matmul_integer(y, dev(w.B), a_zero_point=zp, b_zero_point=dev(w.b_zp))
     q.check_device_error()
-    assert q.last_kernel() == "gemm_tc05_exact_matmul_integer"
+    assert q.last_kernel() == "gemm_tc05_pair_exact_matmul_integer"
     rows = sample(8192, 16, 2)
     want = O.matmul_integer(wy[rows], w.B, int(wzp), w.b_zp)
     assert_equal(host(C)[rows], want, "MatMulInteger 8192x4096x11008 sampled rows")

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from oracle import qmm_oracle as O
-from _helpers import assert_equal, dev, host
+from _helpers import assert_equal, dev, gemm_kernel, host
 
 pytestmark = pytest.mark.gpu
 q = pytest.importorskip("quantized_int8_matmul_gb300")
@@ -48,8 +48,7 @@ def test_matmul_integer_matches_oracle(adt, bdt, zp, M, K, N):
     elif zp == "b_only":
         b_zp = rand(rng, bdt, (N,))
     got = run(A, B, a_zp, b_zp)
-    vec = K % 16 == 0 and N % 16 == 0
-    assert q.last_kernel() == ("gemm_tc05_exact_matmul_integer" if vec else "gemm_tc05_exact_matmul_integer_bytewise")
+    assert q.last_kernel() == gemm_kernel("matmul_integer", M, K, N)
     assert_equal(got, oracle(A, B, a_zp, b_zp), f"{adt}x{bdt} zp={zp} {M}x{K}x{N}")
 
 
