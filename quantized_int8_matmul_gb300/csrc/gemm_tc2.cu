@@ -16,14 +16,14 @@
 // holds its own 128 rows x 256 columns. Per 64-deep K stage an SM therefore
 // moves 96 KB through shared memory instead of 144 KB for the same MACs.
 //
-// CTA organisation (cluster of 2 CTAs, 320 threads each, one CTA per SM):
-//  * warp 9 (producer): TMA copies of this CTA's int8 A rows (128 x 64) and
+// CTA organisation (cluster of 2 CTAs, 576 threads each, one CTA per SM):
+//  * warp 17 (producer): TMA copies of this CTA's int8 A rows (128 x 64) and
 //    B columns (64 x 128) into a 4-stage staging ring.
-//  * warps 0-7 (workers): convert staged bytes to fp16 in the canonical
+//  * warps 0-15 (workers): convert staged bytes to fp16 in the canonical
 //    128-byte-swizzled layouts (A K-major, B MN-major), 4-stage ring; the row
 //    sums of their A rows and the column sums of their B columns; drain the
 //    TMEM accumulator after each K-chunk; run the epilogue and store C.
-//  * warp 8: allocates TMEM for the pair (with the peer's warp 8); in the even
+//  * warp 16: allocates TMEM for the pair (with the peer's warp 16); in the even
 //    CTA, one lane issues the pair MMAs (M=256, N=256, K=16) and the commits,
 //    which arrive on the barriers of both CTAs.
 // A stage is published to the MMA by one arrival per worker warp of either
@@ -53,9 +53,11 @@ constexpr int BK = 64;
 constexpr int NS = 4;                  // fp16 stages read by the MMA
 constexpr int NI = 4;                  // int8 staging stages filled by TMA
 constexpr int LOOKAHEAD = NS - 1;      // stages produced past a chunk before it is drained
-constexpr int NWW = 8;                 // worker warps
+constexpr int NWW = 16;                // worker warps
 constexpr int NW = NWW * 32;
 constexpr int NT = NW + 64;            // + MMA warp + TMA producer warp
+constexpr int PPT = 512 / NW;          // 16-byte pieces of A, and of B, per worker thread per stage
+constexpr int CPW = 1024 / NWW;        // accumulator columns per worker warp in drains and epilogues
 constexpr int A_BYTES = BM * BK * 2;   // fp16 A: 16 KB
 constexpr int B_BYTES = BK * BNH * 2;  // fp16 B half: 16 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -67,6 +69,7 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t SUM_COL = 256;      // TMEM columns [256, 512): running int32 sums
 constexpr int PAIR_ARRIVALS = 2 * NWW; // one arrival per worker warp of both CTAs
 static_assert((NS & (NS - 1)) == 0 && (NI & (NI - 1)) == 0, "ring sizes are powers of two");
+static_assert(NWW == 8 || NWW == 16, "worker warps: 8 or 16");
 
 struct Shared {
   int part[NWW][BNH];               // column-sum partials of this CTA's B half, per warp
@@ -115,23 +118,27 @@ __device__ __forceinline__ TileCoord tile_coord(const GemmArgs& p, int tile_loca
   return c;
 }
 
-// Piece assignment of worker thread t (0..255) in one 64-deep K stage.
-//  A: 2 pieces of 16 bytes: rows t/4 and 64 + t/4, k bytes (t%4)*16. A
-//     quarter-warp reads rows 2p, 2p+1 (64-byte staging rows: 8 distinct bank
-//     groups) and writes 8 distinct swizzle slots.
-//  B: 2 pieces of 16 bytes of the 64 x 128 half: k rows 2*(t/16) + (t/4)%2 and
-//     that + 32, columns 16*nq with nq = (t%8) ^ 4*((t/8)%2). A quarter-warp
-//     reads 8 different 16-byte columns of two 128-byte staging rows (8 bank
-//     groups) and writes, for two consecutive k rows, 4 chunk pairs each, which
-//     the swizzle puts in 8 distinct slots: both shared-memory sides are free of
-//     bank conflicts.
-__device__ __forceinline__ int a_row(int t, int j) { return (t >> 2) + 64 * j; }
+// Piece assignment of worker thread t (0..NW-1) in one 64-deep K stage: the
+// stage holds 512 pieces of 16 bytes of A and 512 of B; each thread takes PPT
+// of each.
+//  A: rows t/4 + j*NW/4, k bytes (t%4)*16. A quarter-warp reads rows 2p, 2p+1
+//     (64-byte staging rows: 8 distinct bank groups) and writes 8 distinct
+//     swizzle slots.
+//  B (the 64 x 128 half): k rows 2*(t/16) + (t/4)%2 + j*NW/8, columns 16*nq
+//     with nq = (t%8) ^ 4*((t/8)%2). A quarter-warp reads 8 different 16-byte
+//     columns of two 128-byte staging rows (8 bank groups) and writes, for two
+//     consecutive k rows, 4 chunk pairs each, which the swizzle puts in 8
+//     distinct slots: both shared-memory sides are free of bank conflicts.
+__device__ __forceinline__ int a_row(int t, int j) { return (t >> 2) + (NW / 4) * j; }
 __device__ __forceinline__ int a_kq(int t) { return t & 3; }
 __device__ __forceinline__ int b_nq(int t) { return (t & 7) ^ (((t >> 3) & 1) << 2); }
-__device__ __forceinline__ int b_krow(int t, int j) { return 2 * (t >> 4) + ((t >> 2) & 1) + 32 * j; }
+__device__ __forceinline__ int b_krow(int t, int j) { return 2 * (t >> 4) + ((t >> 2) & 1) + (NW / 8) * j; }
+// byte steps between a thread's pieces: int8 staging (A, B) and fp16 stage (A, B)
+constexpr uint32_t I8_A_STEP = (NW / 4) * 64u, I8_B_STEP = (NW / 8) * 128u;
+constexpr uint32_t F16_A_STEP = (NW / 4) * 128u, F16_B_STEP = (NW / 8) * 256u;
 
 // Shared-memory byte offsets (within a stage) of this thread's first A and B
-// pieces, chunks 0 and 1; the second piece of each is 8192 bytes further.
+// pieces, chunks 0 and 1; piece j of each is j * F16_A_STEP / F16_B_STEP further.
 //  A: K-major, 128-byte swizzle: row r is 128 bytes (64 fp16 along K), 8-row
 //     groups form 1024-byte atoms, 16-byte chunk c of row r sits at c ^ (r % 8).
 //  B: MN-major, 128-byte swizzle: atom (k/8, n/64) at (k/8)*2048 + (n/64)*1024,
@@ -156,11 +163,11 @@ __device__ __forceinline__ StoreOffsets store_offsets(int t) {
 }
 
 template <bool AU, bool BU>
-__device__ __forceinline__ void store_stage(uint32_t base, const StoreOffsets& o, const uint4 (&v)[4]) {
+__device__ __forceinline__ void store_stage(uint32_t base, const StoreOffsets& o, const uint4 (&v)[2 * PPT]) {
 #pragma unroll
-  for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < 2 * PPT; ++j) {
     uint32_t hv[8];
-    const bool isa = j < 2;
+    const bool isa = j < PPT;
     if (isa) {
       bytes_to_half4<AU>(v[j].x, hv[0], hv[1]);
       bytes_to_half4<AU>(v[j].y, hv[2], hv[3]);
@@ -172,7 +179,7 @@ __device__ __forceinline__ void store_stage(uint32_t base, const StoreOffsets& o
       bytes_to_half4<BU>(v[j].z, hv[4], hv[5]);
       bytes_to_half4<BU>(v[j].w, hv[6], hv[7]);
     }
-    const uint32_t off = (uint32_t)(j & 1) * 8192u;
+    const uint32_t off = isa ? (uint32_t)j * F16_A_STEP : (uint32_t)(j - PPT) * F16_B_STEP;
     st_shared_v4(base + (isa ? o.a0 : o.b0) + off, hv[0], hv[1], hv[2], hv[3]);
     st_shared_v4(base + (isa ? o.a1 : o.b1) + off, hv[4], hv[5], hv[6], hv[7]);
   }
@@ -192,8 +199,8 @@ __device__ __forceinline__ bool worker_sync(Shared& sm, int& phase, unsigned* er
 }
 
 // Epilogue of one tile (this CTA's 128 rows x 256 columns): read the final
-// int32 sums from TMEM (this warp's 32 rows, its 128-column half, 16 columns at
-// a time), apply the fused dequantisation / zero-point correction, store C.
+// int32 sums from TMEM (this warp's 32 rows, its CPW-column slice, 16 columns
+// at a time), apply the fused dequantisation / zero-point correction, store C.
 template <bool AU, bool BU, bool MMI>
 __device__ __noinline__ void epilogue(const GemmArgs& p, Shared& sm, uint32_t tbase, const TileCoord tc, int tile_local,
                                       int q, int h, int lane, int c_vec, bool need_cs, uint32_t peer) {
@@ -215,11 +222,11 @@ __device__ __noinline__ void epilogue(const GemmArgs& p, Shared& sm, uint32_t tb
   const uint32_t rs = (MMI && p.b_zp_count > 0) ? (uint32_t)sm.rowsum[slot][rloc] : 0u;
 
 #pragma unroll 1
-  for (int g = 0; g < 8; ++g) {
+  for (int g = 0; g < CPW / 16; ++g) {
     uint32_t tot[16];
     if ((g & 1) == 0) {
       uint32_t t32[32];
-      tmem_ld32(tbase + lane_off + SUM_COL + (uint32_t)(h * 128 + g * 16), t32);   // warp-collective
+      tmem_ld32(tbase + lane_off + SUM_COL + (uint32_t)(h * CPW + g * 16), t32);   // warp-collective
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         tot[i] = t32[i];
@@ -229,14 +236,14 @@ __device__ __noinline__ void epilogue(const GemmArgs& p, Shared& sm, uint32_t tb
 #pragma unroll
       for (int i = 0; i < 16; ++i) tot[i] = hold[i];
     }
-    const int nb = tc.n0 + h * 128 + g * 16;
+    const int nb = tc.n0 + h * CPW + g * 16;
     if (!row_ok || nb >= p.N || !cs_ok) continue;
     const bool full = (nb + 16 <= p.N) && c_vec;
     uint32_t o[16];
     if (!MMI) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float ws = __uint_as_float(sm.col_op[slot][h * 128 + g * 16 + i]);
+        const float ws = __uint_as_float(sm.col_op[slot][h * CPW + g * 16 + i]);
         float v = __int2float_rn((int)tot[i]);
         v = __fmul_rn(v, as);
         o[i] = __float_as_uint(__fmul_rn(v, ws));
@@ -269,8 +276,8 @@ __device__ __noinline__ void epilogue(const GemmArgs& p, Shared& sm, uint32_t tb
     } else {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const uint32_t zb = sm.col_op[slot][h * 128 + g * 16 + i];
-        const uint32_t cs = (p.a_zp_count > 0) ? (uint32_t)sm.colsum[slot][h * 128 + g * 16 + i] : 0u;
+        const uint32_t zb = sm.col_op[slot][h * CPW + g * 16 + i];
+        const uint32_t cs = (p.a_zp_count > 0) ? (uint32_t)sm.colsum[slot][h * CPW + g * 16 + i] : 0u;
         o[i] = tot[i] - za * cs - zb * rs + (uint32_t)p.K * za * zb;
       }
       int32_t* out = reinterpret_cast<int32_t*>(p.C) + crow + nb;
@@ -416,7 +423,7 @@ __global__ void __launch_bounds__(NT, 1)
   } else {
     // ---------------- workers ----------------
     const int q = warp & 3;
-    const int h = warp >> 2;
+    const int h = warp >> 2;     // column slice [h*CPW, (h+1)*CPW) of the tile
     const bool need_rs = MMI && p.b_zp_count > 0;
     const bool need_cs = MMI && p.a_zp_count > 0;
     const uint32_t full_leader0 = mapa_shared(smem_u32(&sm.full[0]), 0);
@@ -427,7 +434,9 @@ __global__ void __launch_bounds__(NT, 1)
     int dr_d = 0, dr_tl = 0, dr_c = 0;
     int dr_last = min(cs, spt) - 1;
 
-    int rs_acc[2] = {0, 0};
+    int rs_acc[PPT];
+#pragma unroll
+    for (int j = 0; j < PPT; ++j) rs_acc[j] = 0;
     uint32_t ce[4] = {0u, 0u, 0u, 0u}, co[4] = {0u, 0u, 0u, 0u};
     // Column sums of this CTA's B half accumulate in sm.part[warp][column]:
     // lanes 0-7 own the 16 columns b_nq(lane)*16.. of their warp's row.
@@ -447,10 +456,10 @@ __global__ void __launch_bounds__(NT, 1)
         return false;
       tc_fence_after();
       const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-      const uint32_t t_acc = tbase + lane_off + (uint32_t)(h * 128);
+      const uint32_t t_acc = tbase + lane_off + (uint32_t)(h * CPW);
       const uint32_t t_sum = t_acc + SUM_COL;
 #pragma unroll 1
-      for (int g = 0; g < 8; ++g) {
+      for (int g = 0; g < CPW / 16; ++g) {
         uint32_t acc[16];
         uint32_t sum[16];
         if (dr_c > 0) {
@@ -481,14 +490,15 @@ __global__ void __launch_bounds__(NT, 1)
     };
 
     auto step = [&](int g) -> bool {
-      uint4 cur[4];
+      uint4 cur[2 * PPT];
       const int is = g & (NI - 1);
       if (!mbar_wait(&sm.i8_full[is], (uint32_t)((g / NI) & 1), &sm.abort_flag, p.err, SITE_I8_FULL)) return false;
       const uint32_t src = i8base + (uint32_t)is * I8_STAGE;
-      cur[0] = ld_shared_v4(src + ia0);
-      cur[1] = ld_shared_v4(src + ia0 + 64u * 64u);
-      cur[2] = ld_shared_v4(src + ib0);
-      cur[3] = ld_shared_v4(src + ib0 + 32u * 128u);
+#pragma unroll
+      for (int j = 0; j < PPT; ++j) {
+        cur[j] = ld_shared_v4(src + ia0 + (uint32_t)j * I8_A_STEP);
+        cur[PPT + j] = ld_shared_v4(src + ib0 + (uint32_t)j * I8_B_STEP);
+      }
       const int slot = g & (NS - 1);
       if (g >= NS) {
         if (!mbar_wait_cluster(&sm.empty[slot], (uint32_t)(((g / NS) - 1) & 1), &sm.abort_flag, p.err, SITE_EMPTY))
@@ -506,17 +516,18 @@ __global__ void __launch_bounds__(NT, 1)
         const int n = tc.n0 + t;
         const int m = tc.m0 + (t & (BM - 1));
         if (!MMI) {
-          sm.col_op[ring][t] = __float_as_uint(n < p.N ? __ldg(p.w_scale + (p.w_count == 1 ? 0 : n)) : 0.f);
+          if (t < BN)
+            sm.col_op[ring][t] = __float_as_uint(n < p.N ? __ldg(p.w_scale + (p.w_count == 1 ? 0 : n)) : 0.f);
           if (t < BM)
             sm.row_op[ring][t] =
                 __float_as_uint(m < p.M ? __ldg(p.act_scale + (p.act_count == 1 ? 0 : m % p.zp_row_mod)) : 0.f);
         } else {
           uint32_t zb = 0u, za = 0u;
-          if (p.b_zp_count > 0 && n < p.N) {
+          if (p.b_zp_count > 0 && n < p.N && t < BN) {
             const int zi = p.b_zp_count == 1 ? 0 : n;
             zb = BU ? (uint32_t)__ldg((const uint8_t*)p.b_zp + zi) : (uint32_t)(int)__ldg((const int8_t*)p.b_zp + zi);
           }
-          sm.col_op[ring][t] = zb;
+          if (t < BN) sm.col_op[ring][t] = zb;
           if (t < BM) {
             if (p.a_zp_count > 0 && m < p.M) {
               const int zi = p.a_zp_count == 1 ? 0 : m % p.zp_row_mod;
@@ -528,7 +539,7 @@ __global__ void __launch_bounds__(NT, 1)
       }
       if (need_rs) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < PPT; ++j) {
           rs_acc[j] = dp4a_ones<AU>(cur[j].x, rs_acc[j]);
           rs_acc[j] = dp4a_ones<AU>(cur[j].y, rs_acc[j]);
           rs_acc[j] = dp4a_ones<AU>(cur[j].z, rs_acc[j]);
@@ -537,8 +548,8 @@ __global__ void __launch_bounds__(NT, 1)
       }
       if (need_cs) {
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-          const uint32_t w[4] = {cur[2 + j].x, cur[2 + j].y, cur[2 + j].z, cur[2 + j].w};
+        for (int j = 0; j < PPT; ++j) {
+          const uint32_t w[4] = {cur[PPT + j].x, cur[PPT + j].y, cur[PPT + j].z, cur[PPT + j].w};
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq) {
             const uint32_t u = BU ? w[qq] : (w[qq] ^ 0x80808080u);
@@ -548,8 +559,8 @@ __global__ void __launch_bounds__(NT, 1)
         }
         // A 16-bit lane holds at most 257 additions of 255. The four lanes of a
         // warp that share columns (lane ^ 12, ^ 16, ^ 28) are combined before the
-        // fold, so fold every 32 stages (4 lanes x 2 pieces x 32 stages = 256
-        // additions) and at the tile end.
+        // fold, so fold every 32 stages (4 lanes x PPT <= 2 pieces x 32 stages
+        // <= 256 additions) and at the tile end.
         if ((st_s & 31) == 31 || st_s == spt - 1) {
 #pragma unroll
           for (int qq = 0; qq < 4; ++qq) {
@@ -573,7 +584,7 @@ __global__ void __launch_bounds__(NT, 1)
         const int ring = st_tl % SUM_RING;
         if (need_rs) {
 #pragma unroll
-          for (int j = 0; j < 2; ++j) {
+          for (int j = 0; j < PPT; ++j) {
             int v = rs_acc[j];
             v += __shfl_xor_sync(0xffffffffu, v, 1);
             v += __shfl_xor_sync(0xffffffffu, v, 2);
