@@ -109,6 +109,27 @@ qmm_status qmm_a8w8(const int8_t* A, const int8_t* B, int64_t M, int64_t K, int6
                     void* stream);
 
 /*
+ * qmm_a8w8_ws: the same operation and bit-identical results as qmm_a8w8, with
+ * a caller-provided workspace that lets large problems run in two passes: a
+ * bandwidth-bound pre-pass writes exact fp16 copies of A and B into the
+ * workspace once, and the GEMM then stages fp16 tiles with TMA straight into
+ * the tensor-core layout on SM pairs, instead of converting every operand
+ * tile once for each output tile that uses it.
+ *
+ *  workspace        device scratch of at least qmm_a8w8_workspace_bytes(M, K, N)
+ *                   bytes, 16-byte aligned, caller-owned; contents on entry do
+ *                   not matter, contents on return are unspecified.
+ * qmm_a8w8_workspace_bytes returns 0 when the two-pass path does not apply to
+ * the shape (M < 256, or K or N not a multiple of 16); the call then runs
+ * qmm_a8w8 and ignores the workspace (which may be NULL). The same happens
+ * when A or B is not 16-byte aligned.
+ */
+size_t qmm_a8w8_workspace_bytes(int64_t M, int64_t K, int64_t N);
+qmm_status qmm_a8w8_ws(const int8_t* A, const int8_t* B, int64_t M, int64_t K, int64_t N, const float* act_scale,
+                       int64_t act_count, const float* weight_scale, int64_t w_count, void* C, int c_dtype,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Form (c): MatMulInteger with zero points. ROCm hip-ep PR #1248,
  * "feat(onnx-to-hip): lower quantized integer conv and matmul", section
  * "What", MatMulInteger paragraph:
@@ -132,6 +153,28 @@ qmm_status matmul_integer(const void* A, int a_dtype, const void* B, int b_dtype
                           int64_t K, int64_t N, int64_t a_batch_stride, int64_t b_batch_stride,
                           const void* a_zero_point, int64_t a_zp_count, const void* b_zero_point,
                           int64_t b_zp_count, int32_t* C, void* stream);
+
+/*
+ * matmul_integer_ws: the same operation and results as matmul_integer, run in
+ * two passes when a workspace is supplied: the pre-pass writes exact fp16
+ * copies of A and B together with rowsum(A) (when b_zp is given) and
+ * colsum(B) (when a_zp is given), then the SM-pair GEMM reads fp16 tiles with
+ * TMA and applies the zero-point expansion with the precomputed sums.
+ *
+ *  workspace   at least matmul_integer_workspace_bytes(batch, M, K, N,
+ *              a_batch_stride, b_batch_stride) bytes, 16-byte aligned.
+ * The size function returns 0 when the two-pass path does not apply: M < 256
+ * after folding a dense batch over a shared B into M, K or N not a multiple
+ * of 16, or batch strides other than 0 or dense. The call then runs
+ * matmul_integer and ignores the workspace; likewise for unaligned A or B.
+ */
+size_t matmul_integer_workspace_bytes(int64_t batch, int64_t M, int64_t K, int64_t N, int64_t a_batch_stride,
+                                      int64_t b_batch_stride);
+qmm_status matmul_integer_ws(const void* A, int a_dtype, const void* B, int b_dtype, int64_t batch, int64_t M,
+                             int64_t K, int64_t N, int64_t a_batch_stride, int64_t b_batch_stride,
+                             const void* a_zero_point, int64_t a_zp_count, const void* b_zero_point,
+                             int64_t b_zp_count, int32_t* C, void* workspace, size_t workspace_bytes,
+                             void* stream);
 
 /*
  * Form (d): DynamicQuantizeLinear, uint8 only. ROCm hip-ep PR #1248, section

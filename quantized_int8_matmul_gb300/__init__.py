@@ -49,10 +49,18 @@ def _load() -> ctypes.CDLL:
     lib.qmm_w8_dequant.argtypes = [vp, ci, vp, i64, i64, i64, vp, i64, vp, i64, vp, ci, vp]
     lib.qmm_a8w8.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, i64, vp, ci, vp]
     lib.matmul_integer.argtypes = [vp, ci, vp, ci, i64, i64, i64, i64, i64, i64, vp, i64, vp, i64, vp, vp]
+    sz = ctypes.c_size_t
+    lib.qmm_a8w8_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.qmm_a8w8_workspace_bytes.restype = sz
+    lib.qmm_a8w8_ws.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, i64, vp, ci, vp, sz, vp]
+    lib.matmul_integer_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64]
+    lib.matmul_integer_workspace_bytes.restype = sz
+    lib.matmul_integer_ws.argtypes = [vp, ci, vp, ci, i64, i64, i64, i64, i64, i64, vp, i64, vp, i64, vp, vp, sz, vp]
     lib.dynamic_quantize_linear_workspace_bytes.argtypes = [i64]
     lib.dynamic_quantize_linear_workspace_bytes.restype = ctypes.c_size_t
     lib.dynamic_quantize_linear.argtypes = [vp, i64, vp, vp, vp, vp, i64, vp, ctypes.c_size_t, vp]
-    for fn in ("qmm_w8_dequant", "qmm_a8w8", "matmul_integer", "dynamic_quantize_linear"):
+    for fn in ("qmm_w8_dequant", "qmm_a8w8", "qmm_a8w8_ws", "matmul_integer", "matmul_integer_ws",
+               "dynamic_quantize_linear"):
         getattr(lib, fn).restype = ci
     lib.qmm_status_string.argtypes = [ci]
     lib.qmm_status_string.restype = ctypes.c_char_p
@@ -129,8 +137,32 @@ def qmm_w8_dequant(A, B, scale, zero_point=None, out=None, out_dtype=torch.float
     return out
 
 
-def qmm_a8w8(A, B, act_scale, weight_scale, out=None, out_dtype=torch.bfloat16, stream=None):
-    """Form (b): C = out(f32(A @ B) * act_scale[m] * weight_scale[n]); A, B int8."""
+def _workspace(ws, nbytes, device):
+    """None -> no workspace; "auto" -> a fresh uint8 buffer of nbytes (torch's
+    caching allocator); a tensor -> used as is. Returns (tensor or None, bytes)."""
+    if ws is None or nbytes == 0:
+        return None, 0
+    if isinstance(ws, str):
+        if ws != "auto":
+            raise ValueError("workspace must be None, 'auto' or a device tensor")
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return ws, ws.numel() * ws.element_size()
+
+
+def qmm_a8w8_workspace_bytes(M: int, K: int, N: int) -> int:
+    return int(_lib.qmm_a8w8_workspace_bytes(M, K, N))
+
+
+def matmul_integer_workspace_bytes(batch, M, K, N, a_batch_stride, b_batch_stride) -> int:
+    return int(_lib.matmul_integer_workspace_bytes(batch, M, K, N, a_batch_stride, b_batch_stride))
+
+
+def qmm_a8w8(A, B, act_scale, weight_scale, out=None, out_dtype=torch.bfloat16, stream=None, workspace=None):
+    """Form (b): C = out(f32(A @ B) * act_scale[m] * weight_scale[n]); A, B int8.
+
+    workspace: None runs the single-pass kernel; "auto" or a device tensor of at
+    least qmm_a8w8_workspace_bytes(M, K, N) bytes runs the two-pass path (fp16
+    operand copies, then the SM-pair GEMM) where it applies."""
     _need(A, (torch.int8,), "A")
     _need(B, (torch.int8,), "B")
     _need(act_scale, (torch.float32,), "act_scale")
@@ -142,14 +174,24 @@ def qmm_a8w8(A, B, act_scale, weight_scale, out=None, out_dtype=torch.bfloat16, 
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=A.device)
     _need(out, (torch.float32, torch.bfloat16), "out")
-    st = _lib.qmm_a8w8(_ptr(A), _ptr(B), M, K, N, _ptr(act_scale), act_scale.numel(), _ptr(weight_scale),
-                       weight_scale.numel(), _ptr(out), _TORCH_TO_QMM[out.dtype], _stream(stream))
-    _check("qmm_a8w8", st)
+    ws, wsb = _workspace(workspace, qmm_a8w8_workspace_bytes(M, K, N), A.device)
+    if ws is None:
+        st = _lib.qmm_a8w8(_ptr(A), _ptr(B), M, K, N, _ptr(act_scale), act_scale.numel(), _ptr(weight_scale),
+                           weight_scale.numel(), _ptr(out), _TORCH_TO_QMM[out.dtype], _stream(stream))
+        _check("qmm_a8w8", st)
+    else:
+        st = _lib.qmm_a8w8_ws(_ptr(A), _ptr(B), M, K, N, _ptr(act_scale), act_scale.numel(), _ptr(weight_scale),
+                              weight_scale.numel(), _ptr(out), _TORCH_TO_QMM[out.dtype], _ptr(ws), wsb,
+                              _stream(stream))
+        _check("qmm_a8w8_ws", st)
     return out
 
 
-def matmul_integer(A, B, a_zero_point=None, b_zero_point=None, out=None, stream=None):
-    """Form (c): int32 C = (A - a_zp) @ (B - b_zp), A [...,M,K], B [K,N] (shared) or [...,K,N]."""
+def matmul_integer(A, B, a_zero_point=None, b_zero_point=None, out=None, stream=None, workspace=None):
+    """Form (c): int32 C = (A - a_zp) @ (B - b_zp), A [...,M,K], B [K,N] (shared) or [...,K,N].
+
+    workspace: as for qmm_a8w8 (None: single pass; "auto" or a tensor: two-pass
+    path with precomputed row/column sums where it applies)."""
     _need(A, (torch.int8, torch.uint8), "A")
     _need(B, (torch.int8, torch.uint8), "B")
     if A.dim() < 2 or A.dim() > 4 or B.dim() < 2 or B.dim() > 4:
@@ -190,10 +232,17 @@ def matmul_integer(A, B, a_zero_point=None, b_zero_point=None, out=None, stream=
     if out is None:
         out = torch.empty((*batch_shape, M, N), dtype=torch.int32, device=A.device)
     _need(out, (torch.int32,), "out")
-    st = _lib.matmul_integer(_ptr(A), _TORCH_TO_QMM[A.dtype], _ptr(B), _TORCH_TO_QMM[B.dtype], batch, M, K, N,
-                             a_stride, b_stride, _ptr(a_zero_point), az, _ptr(b_zero_point), bz, _ptr(out),
-                             _stream(stream))
-    _check("matmul_integer", st)
+    ws, wsb = _workspace(workspace, matmul_integer_workspace_bytes(batch, M, K, N, a_stride, b_stride), A.device)
+    if ws is None:
+        st = _lib.matmul_integer(_ptr(A), _TORCH_TO_QMM[A.dtype], _ptr(B), _TORCH_TO_QMM[B.dtype], batch, M, K, N,
+                                 a_stride, b_stride, _ptr(a_zero_point), az, _ptr(b_zero_point), bz, _ptr(out),
+                                 _stream(stream))
+        _check("matmul_integer", st)
+    else:
+        st = _lib.matmul_integer_ws(_ptr(A), _TORCH_TO_QMM[A.dtype], _ptr(B), _TORCH_TO_QMM[B.dtype], batch, M, K,
+                                    N, a_stride, b_stride, _ptr(a_zero_point), az, _ptr(b_zero_point), bz,
+                                    _ptr(out), _ptr(ws), wsb, _stream(stream))
+        _check("matmul_integer_ws", st)
     return out
 
 

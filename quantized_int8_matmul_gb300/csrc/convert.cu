@@ -1,0 +1,151 @@
+// Operand pre-pass for the fp16-operand GEMM: 8-bit integer matrices become
+// exact fp16 copies (every int8 and uint8 value is an fp16 value), with the
+// row sums of A and the column sums of B that the MatMulInteger zero-point
+// expansion needs (sum_k (a-za)(b-zb) = sum ab - za*colsum(B) - zb*rowsum(A)
+// + K*za*zb; ROCm hip-ep PR #1248, "What"). The pass reads each byte once and
+// writes two; the GEMM that follows then stages fp16 tiles with TMA straight
+// into the tensor core's layout, instead of converting every operand tile once
+// per output tile that uses it.
+#include "common.cuh"
+#include "kernels.h"
+
+#include <algorithm>
+
+namespace qmm {
+namespace conv {
+
+// 16 bytes -> 16 exact fp16 values (8 words), byte order preserved.
+template <bool U>
+__device__ __forceinline__ void convert16(const uint4 v, uint32_t (&h)[8]) {
+  bytes_to_half4<U>(v.x, h[0], h[1]);
+  bytes_to_half4<U>(v.y, h[2], h[3]);
+  bytes_to_half4<U>(v.z, h[4], h[5]);
+  bytes_to_half4<U>(v.w, h[6], h[7]);
+}
+
+__device__ __forceinline__ void st_global_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+template <bool U>
+__device__ __forceinline__ int dp4a_sum(uint32_t w, int acc) {
+  if (U) return (int)__dp4a(w, 0x01010101u, (unsigned)acc);
+  return __dp4a((int)w, 0x01010101, acc);
+}
+
+// One warp per row (grid-stride over rows): row r of `rows` rows of
+// `row_bytes` bytes (a multiple of 16, rows 16-byte aligned) becomes fp16 in
+// dst; with ROWSUM, rowsum[r] = sum of the row's values (int32, wrapping).
+template <bool U, bool ROWSUM>
+__global__ void __launch_bounds__(256) convert_rows_kernel(const uint8_t* __restrict__ src, __half* __restrict__ dst,
+                                                           long long rows, int row_bytes, int* __restrict__ rowsum) {
+  const int lane = threadIdx.x & 31;
+  const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  const int chunks = row_bytes >> 4;
+  for (long long r = warp0; r < rows; r += nwarps) {
+    const uint8_t* s = src + r * row_bytes;
+    __half* d = dst + r * row_bytes;
+    int acc = 0;
+    for (int c = lane; c < chunks; c += 32) {
+      const uint4 v = ldg_nc_v4(s + 16 * c);
+      uint32_t h[8];
+      convert16<U>(v, h);
+      st_global_v4(d + 16 * c, h[0], h[1], h[2], h[3]);
+      st_global_v4(d + 16 * c + 8, h[4], h[5], h[6], h[7]);
+      if (ROWSUM) {
+        acc = dp4a_sum<U>(v.x, acc);
+        acc = dp4a_sum<U>(v.y, acc);
+        acc = dp4a_sum<U>(v.z, acc);
+        acc = dp4a_sum<U>(v.w, acc);
+      }
+    }
+    if (ROWSUM) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) rowsum[r] = acc;
+    }
+  }
+}
+
+// Column sums with the conversion: thread (column chunk cc, row block rb)
+// converts rows [rb*R, rb*R + R) of 16 columns and adds its 16 partial column
+// sums into colsum (zeroed beforehand) with atomics. `mats` matrices of
+// `rows` x `cols` bytes each (batch of B), colsum is [mats][cols].
+constexpr int kColRows = 32;
+
+template <bool U>
+__global__ void __launch_bounds__(256) convert_cols_kernel(const uint8_t* __restrict__ src, __half* __restrict__ dst,
+                                                           int mats, int rows, int cols, int* __restrict__ colsum) {
+  const int cchunks = cols >> 4;
+  const int rblocks = (rows + kColRows - 1) / kColRows;
+  const long long tasks = (long long)mats * rblocks * cchunks;
+  for (long long task = (long long)blockIdx.x * blockDim.x + threadIdx.x; task < tasks;
+       task += (long long)gridDim.x * blockDim.x) {
+    const int cc = (int)(task % cchunks);
+    const long long rest = task / cchunks;
+    const int rb = (int)(rest % rblocks);
+    const int m = (int)(rest / rblocks);
+    const size_t base = (size_t)m * rows * cols;
+    int sum[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) sum[i] = 0;
+    const int r_end = min(rows, (rb + 1) * kColRows);
+    for (int r = rb * kColRows; r < r_end; ++r) {
+      const size_t off = base + (size_t)r * cols + 16 * (size_t)cc;
+      const uint4 v = ldg_nc_v4(src + off);
+      uint32_t h[8];
+      convert16<U>(v, h);
+      st_global_v4(dst + off, h[0], h[1], h[2], h[3]);
+      st_global_v4(dst + off + 8, h[4], h[5], h[6], h[7]);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const uint32_t b = (w[i >> 2] >> (8 * (i & 3))) & 0xFFu;
+        sum[i] += U ? (int)b : (int)(int8_t)b;
+      }
+    }
+    int* cs = colsum + (size_t)m * cols + 16 * (size_t)cc;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) atomicAdd(cs + i, sum[i]);
+  }
+}
+
+int grid_for(long long work_items, int per_block) {
+  const long long blocks = (work_items + per_block - 1) / per_block;
+  return (int)std::max<long long>(1, std::min<long long>(blocks, (long long)num_sms() * 8));
+}
+
+}  // namespace conv
+
+cudaError_t launch_convert_rows(const void* src, bool u8, __half* dst, long long rows, int row_bytes, int* rowsum,
+                                cudaStream_t s) {
+  using namespace conv;
+  if (rows <= 0 || row_bytes <= 0) return cudaSuccess;
+  const int grid = grid_for(rows * 32, 256);
+  const uint8_t* p = static_cast<const uint8_t*>(src);
+  if (rowsum) {
+    if (u8) convert_rows_kernel<true, true><<<grid, 256, 0, s>>>(p, dst, rows, row_bytes, rowsum);
+    else convert_rows_kernel<false, true><<<grid, 256, 0, s>>>(p, dst, rows, row_bytes, rowsum);
+  } else {
+    if (u8) convert_rows_kernel<true, false><<<grid, 256, 0, s>>>(p, dst, rows, row_bytes, nullptr);
+    else convert_rows_kernel<false, false><<<grid, 256, 0, s>>>(p, dst, rows, row_bytes, nullptr);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert_cols(const void* src, bool u8, __half* dst, int mats, int rows, int cols, int* colsum,
+                                cudaStream_t s) {
+  using namespace conv;
+  if (mats <= 0 || rows <= 0 || cols <= 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(colsum, 0, sizeof(int) * (size_t)mats * cols, s);
+  if (e != cudaSuccess) return e;
+  const long long tasks = (long long)mats * ((rows + kColRows - 1) / kColRows) * (cols / 16);
+  const int grid = grid_for(tasks, 256);
+  const uint8_t* p = static_cast<const uint8_t*>(src);
+  if (u8) convert_cols_kernel<true><<<grid, 256, 0, s>>>(p, dst, mats, rows, cols, colsum);
+  else convert_cols_kernel<false><<<grid, 256, 0, s>>>(p, dst, mats, rows, cols, colsum);
+  return cudaGetLastError();
+}
+
+}  // namespace qmm

@@ -1,0 +1,464 @@
+// Exact 8-bit GEMM on SM pairs from fp16 copies of the operands (made once by
+// the pre-pass in convert.cu). The arithmetic is that of gemm_tc.cu: operands
+// are 8-bit integers held exactly in fp16, tcgen05.mma kind::f16 sums their
+// products exactly in fp32 over K-chunks no longer than 2^24 / max|product|,
+// and each chunk is folded into wrapping int32 sums in TMEM (the INT32
+// accumulator of PyPTO PR #1920's sequence diagram; the wrapping int32 of
+// MatMulInteger in ROCm hip-ep PR #1248, "What"). Epilogues: A8W8 row-then-
+// column scaling (PyPTO PR #1920), or the MatMulInteger zero-point expansion
+//   acc - za*colsum(B)[n] - zb*rowsum(A)[m] + K*za*zb
+// with the sums taken from the pre-pass.
+//
+// Because nothing is converted here, the main loop is TMA -> shared memory ->
+// tensor core: per 64-deep K stage each SM receives 32 KB by TMA and its MMA
+// reads 32 KB, and no thread touches operand bytes.
+//
+// Cluster of 2 CTAs (256 x 256 pair tile; each CTA: 128 rows of A, 128
+// columns of B, its 128 x 256 accumulator in its own TMEM), 320 threads:
+//  * warp 9 (producer): TMA copies of this CTA's fp16 A rows (box 64 x 128,
+//    128-byte swizzle: the K-major MMA layout) and B columns (two boxes of
+//    64 k x 64 n: the MN-major layout) into a 6-stage ring. Both CTAs' copies
+//    complete on the even CTA's `full` barrier (cta_group::2 form).
+//  * warp 8: TMEM allocation for the pair; in the even CTA one lane issues
+//    the pair MMAs (M=256, N=256, K=16) and commits to both CTAs' barriers.
+//  * warps 0-7: drain the accumulator after each K-chunk, run the epilogue.
+// Every wait is bounded (see common.cuh).
+#include "common.cuh"
+#include "kernels.h"
+#include "tma.h"
+
+#include <algorithm>
+#include <mutex>
+
+namespace qmm {
+namespace gemmf {
+
+constexpr int BM = 128;
+constexpr int BMP = 2 * BM;
+constexpr int BN = 256;
+constexpr int BNH = BN / 2;
+constexpr int BK = 64;
+constexpr int NS = 6;                   // stages in the ring
+constexpr int NEW = 8;                  // drain / epilogue warps
+constexpr int NT = NEW * 32 + 64;       // + MMA warp + producer warp
+constexpr int CPW = 1024 / NEW;         // accumulator columns per drain warp (128)
+constexpr int A_BYTES = BM * BK * 2;    // 16 KB
+constexpr int B_BYTES = BK * BNH * 2;   // 16 KB
+constexpr int B_BOX = 64 * BK * 2;      // one 64-column B box: 8 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t SUM_COL = 256;
+constexpr int PAIR_ARRIVALS = 2 * NEW;
+
+struct Shared {
+  uint64_t full[NS];      // even CTA: one arrival (expect_tx) + both CTAs' copy bytes
+  uint64_t empty[NS];     // the pair's commit
+  uint64_t acc_full;      // the pair's commit
+  uint64_t acc_empty;     // even CTA: one arrival per drain warp of both CTAs
+  uint64_t teardown;
+  uint32_t tmem_base;
+  int abort_flag;
+};
+
+constexpr size_t SMEM_BYTES = (size_t)NS * STAGE_BYTES + sizeof(Shared) + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+
+enum : unsigned {
+  SITE_EMPTY = 0x400, SITE_FULL = 0x401, SITE_ACC_FULL = 0x402, SITE_ACC_EMPTY = 0x403, SITE_TEARDOWN = 0x404,
+  SITE_FINAL = 0x405
+};
+
+struct TileCoord {
+  int b, m0, n0;   // m0: this CTA's first row; n0: the pair tile's first column
+};
+
+__device__ __forceinline__ TileCoord tile_coord(const GemmF16Args& p, int tile_local, int cid, int ncl, int rank) {
+  const int m_tiles = (p.M + BMP - 1) / BMP;
+  const int n_tiles = (p.N + BN - 1) / BN;
+  const int tile_id = cid + tile_local * ncl;
+  const int per_batch = m_tiles * n_tiles;
+  TileCoord c;
+  c.b = tile_id / per_batch;
+  const int r = tile_id - c.b * per_batch;
+  const int mt = r / n_tiles;
+  c.m0 = mt * BMP + rank * BM;
+  c.n0 = (r - mt * n_tiles) * BN;
+  return c;
+}
+
+// TMA copy completing on an mbarrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap, int x, int y, int z, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
+      "%4}], [%5];" ::"r"(dst),
+      "l"(tmap), "r"(x), "r"(y), "r"(z), "r"(bar_cluster)
+      : "memory");
+}
+
+// Epilogue of one tile: this warp's 32 rows x CPW columns of the final int32
+// sums, dequantised (A8W8) or zero-point corrected (MatMulInteger), to C.
+template <bool AU, bool BU, bool MMI>
+__device__ __noinline__ void epilogue(const GemmF16Args& p, uint32_t tbase, const TileCoord tc, int q, int h, int lane,
+                                      int c_vec) {
+  const int rloc = q * 32 + lane;
+  const int row = tc.m0 + rloc;
+  const bool row_ok = row < p.M;
+  const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+  const size_t crow = ((size_t)tc.b * p.M + (size_t)(row_ok ? row : 0)) * (size_t)p.N;
+  const uint64_t pol = l2_policy_evict_first();
+  float as = 0.f;
+  uint32_t za = 0u, rs = 0u;
+  if (row_ok) {
+    const int mz = row % p.zp_row_mod;
+    if (!MMI) {
+      as = __ldg(p.act_scale + (p.act_count == 1 ? 0 : mz));
+    } else {
+      if (p.a_zp_count > 0) {
+        const int zi = p.a_zp_count == 1 ? 0 : mz;
+        za = AU ? (uint32_t)__ldg((const uint8_t*)p.a_zp + zi) : (uint32_t)(int)__ldg((const int8_t*)p.a_zp + zi);
+      }
+      if (p.b_zp_count > 0) rs = (uint32_t)__ldg(p.rowsum + (size_t)(p.a_bstride ? tc.b : 0) * p.M + row);
+    }
+  }
+  const int* colsum = (MMI && p.a_zp_count > 0) ? p.colsum + (p.b_bstride ? (size_t)tc.b * p.N : 0) : nullptr;
+
+  uint32_t hold[16];
+#pragma unroll 1
+  for (int g = 0; g < CPW / 16; ++g) {
+    uint32_t tot[16];
+    if ((g & 1) == 0) {
+      uint32_t t32[32];
+      tmem_ld32(tbase + lane_off + SUM_COL + (uint32_t)(h * CPW + g * 16), t32);   // warp-collective
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        tot[i] = t32[i];
+        hold[i] = t32[16 + i];
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) tot[i] = hold[i];
+    }
+    const int nb = tc.n0 + h * CPW + g * 16;
+    if (!row_ok || nb >= p.N) continue;
+    const bool full = (nb + 16 <= p.N) && c_vec;
+    uint32_t o[16];
+    if (!MMI) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int n = min(nb + i, p.N - 1);
+        const float ws = __ldg(p.w_scale + (p.w_count == 1 ? 0 : n));
+        float v = __int2float_rn((int)tot[i]);
+        v = __fmul_rn(v, as);
+        o[i] = __float_as_uint(__fmul_rn(v, ws));
+      }
+      if (p.c_f32) {
+        float* out = reinterpret_cast<float*>(p.C) + crow + nb;
+        if (full) {
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) st_global_v4_hint(out + i, o[i], o[i + 1], o[i + 2], o[i + 3], pol);
+        } else {
+          for (int i = 0; i < 16; ++i)
+            if (nb + i < p.N) out[i] = __uint_as_float(o[i]);
+        }
+      } else {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C) + crow + nb;
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+          pk[i] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+        if (full) {
+          st_global_v4_hint(out, pk[0], pk[1], pk[2], pk[3], pol);
+          st_global_v4_hint(out + 8, pk[4], pk[5], pk[6], pk[7], pol);
+        } else {
+          for (int i = 0; i < 16; ++i)
+            if (nb + i < p.N) out[i] = __float2bfloat16_rn(__uint_as_float(o[i]));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int n = min(nb + i, p.N - 1);
+        uint32_t zb = 0u;
+        if (p.b_zp_count > 0) {
+          const int zi = p.b_zp_count == 1 ? 0 : n;
+          zb = BU ? (uint32_t)__ldg((const uint8_t*)p.b_zp + zi) : (uint32_t)(int)__ldg((const int8_t*)p.b_zp + zi);
+        }
+        const uint32_t cs = colsum ? (uint32_t)__ldg(colsum + n) : 0u;
+        o[i] = tot[i] - za * cs - zb * rs + (uint32_t)p.K * za * zb;
+      }
+      int32_t* out = reinterpret_cast<int32_t*>(p.C) + crow + nb;
+      if (full) {
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) st_global_v4_hint(out + i, o[i], o[i + 1], o[i + 2], o[i + 3], pol);
+      } else {
+        for (int i = 0; i < 16; ++i)
+          if (nb + i < p.N) out[i] = (int)o[i];
+      }
+    }
+  }
+}
+
+template <bool AU, bool BU, bool MMI>
+__global__ void __launch_bounds__(NT, 1)
+    gemm_f16pair_kernel(const GemmF16Args p, const int cs, const int c_vec, const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t sbase = (raw + 1023u) & ~1023u;
+  uint8_t* sbase_ptr = smem_raw + (sbase - raw);
+  Shared& sm = *reinterpret_cast<Shared*>(sbase_ptr + NS * STAGE_BYTES);
+
+  const int t = threadIdx.x;
+  const int warp = t >> 5;
+  const int lane = t & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int cid = (int)cluster_id_x();
+  const int ncl = (int)nclusters_x();
+
+  const int m_tiles = (p.M + BMP - 1) / BMP;
+  const int n_tiles = (p.N + BN - 1) / BN;
+  const int num_tiles = p.batch * m_tiles * n_tiles;
+  const int my_tiles = (cid < num_tiles) ? (num_tiles - cid + ncl - 1) / ncl : 0;
+  const int spt = (p.K + BK - 1) / BK;
+  const int cpt = (spt + cs - 1) / cs;
+  const int total_stages = my_tiles * spt;
+  const int total_chunks = my_tiles * cpt;
+
+  if (t == 0) {
+    for (int i = 0; i < NS; ++i) {
+      mbar_init(&sm.full[i], 1);
+      mbar_init(&sm.empty[i], 1);
+    }
+    mbar_init(&sm.acc_full, 1);
+    mbar_init(&sm.acc_empty, PAIR_ARRIVALS);
+    mbar_init(&sm.teardown, 1);
+    sm.abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  if (warp == NEW) {
+    tmem_alloc_pair(&sm.tmem_base, TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync_all();
+  tc_fence_after();
+  const uint32_t tbase = sm.tmem_base;
+
+  if (warp == NEW) {
+    // ---------------- pair MMA issuer (even CTA) ----------------
+    if (rank == 0 && lane == 0) {
+      const uint32_t idesc = idesc_f16_f32(BMP, BN, false, true);
+      int g = 0, d = 0;
+      bool ok = true;
+      for (int tl = 0; tl < my_tiles && ok; ++tl) {
+        for (int c = 0; c < cpt && ok; ++c) {
+          if (d > 0) {
+            ok = mbar_wait_cluster(&sm.acc_empty, (uint32_t)((d - 1) & 1), &sm.abort_flag, p.err, SITE_ACC_EMPTY);
+            if (!ok) break;
+          }
+          tc_fence_after();
+          const int s_beg = c * cs;
+          const int s_end = min(spt, s_beg + cs);
+          for (int s = s_beg; s < s_end; ++s, ++g) {
+            const int slot = g % NS;
+            ok = mbar_wait_cluster(&sm.full[slot], (uint32_t)((g / NS) & 1), &sm.abort_flag, p.err, SITE_FULL);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t a_addr = sbase + (uint32_t)slot * STAGE_BYTES;
+            const uint32_t b_addr = a_addr + A_BYTES;
+#pragma unroll
+            for (int j = 0; j < BK / 16; ++j) {
+              const uint64_t ad = sdesc_sw128(a_addr + (uint32_t)j * 32u, 16u, 1024u);
+              // B: 64-column boxes 8 KB apart (LBO), 8-row k groups 1 KB apart (SBO)
+              const uint64_t bd = sdesc_sw128(b_addr + (uint32_t)j * 2048u, (uint32_t)B_BOX, 1024u);
+              tc_mma_f16_pair(tbase, ad, bd, idesc, (s > s_beg || j > 0) ? 1u : 0u);
+            }
+            tc_commit_pair_mc(&sm.empty[slot], 0x3);
+          }
+          if (!ok) break;
+          tc_commit_pair_mc(&sm.acc_full, 0x3);
+          ++d;
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == NEW + 1) {
+    // ---------------- TMA producer (both CTAs) ----------------
+    if (lane == 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      const uint32_t full_leader0 = mapa_shared(smem_u32(&sm.full[0]), 0);
+      int tl = 0, s = 0;
+      TileCoord tc = tile_coord(p, 0, cid, ncl, (int)rank);
+      int g = 0;
+      for (; g < total_stages; ++g) {
+        const int slot = g % NS;
+        if (g >= NS &&
+            !mbar_wait(&sm.empty[slot], (uint32_t)(((g / NS) - 1) & 1), &sm.abort_flag, p.err, SITE_EMPTY))
+          break;
+        const uint32_t bar = full_leader0 + (uint32_t)slot * 8u;
+        if (rank == 0) mbar_arrive_expect_tx(&sm.full[slot], 2u * STAGE_BYTES);
+        const uint32_t dst = sbase + (uint32_t)slot * STAGE_BYTES;
+        const int ab = p.a_bstride ? tc.b : 0, bb = p.b_bstride ? tc.b : 0;
+        const int nc = tc.n0 + (int)rank * BNH;
+        tma_load_3d_pair(dst, &tmA, s * BK, tc.m0, ab, bar);
+        tma_load_3d_pair(dst + A_BYTES, &tmB, nc, s * BK, bb, bar);
+        tma_load_3d_pair(dst + A_BYTES + B_BOX, &tmB, nc + 64, s * BK, bb, bar);
+        if (++s == spt) {
+          s = 0;
+          tc = tile_coord(p, ++tl, cid, ncl, (int)rank);
+        }
+      }
+      // The even CTA's `full` barriers count both CTAs' bytes: once the phases
+      // of the last stages complete, no copy of either CTA is in flight.
+      if (rank == 0)
+        for (int j = (g > NS ? g - NS : 0); j < g; ++j)
+          mbar_wait_cluster(&sm.full[j % NS], (uint32_t)((j / NS) & 1), nullptr, p.err, SITE_FINAL);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- drain / epilogue warps ----------------
+    const int q = warp & 3;
+    const int h = warp >> 2;
+    const uint32_t acc_empty_leader = mapa_shared(smem_u32(&sm.acc_empty), 0);
+    int tl = 0, c = 0;
+    for (int d = 0; d < total_chunks; ++d) {
+      if (!mbar_wait_cluster(&sm.acc_full, (uint32_t)(d & 1), &sm.abort_flag, p.err, SITE_ACC_FULL)) break;
+      tc_fence_after();
+      const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+      const uint32_t t_acc = tbase + lane_off + (uint32_t)(h * CPW);
+      const uint32_t t_sum = t_acc + SUM_COL;
+#pragma unroll 1
+      for (int g = 0; g < CPW / 16; ++g) {
+        uint32_t acc[16];
+        uint32_t sum[16];
+        if (c > 0) {
+          tmem_ld16x2(t_acc + g * 16, acc, t_sum + g * 16, sum);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sum[i] += (uint32_t)__float2int_rn(__uint_as_float(acc[i]));
+        } else {
+          tmem_ld16(t_acc + g * 16, acc);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) sum[i] = (uint32_t)__float2int_rn(__uint_as_float(acc[i]));
+        }
+        tmem_st16_async(t_sum + g * 16, sum);
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote_cta(acc_empty_leader);
+      if (c == cpt - 1) epilogue<AU, BU, MMI>(p, tbase, tile_coord(p, tl, cid, ncl, (int)rank), q, h, lane, c_vec);
+      if (++c == cpt) {
+        c = 0;
+        ++tl;
+      }
+    }
+    tc_fence_before();
+  }
+
+  __syncthreads();
+  if (t == 0 && sm.abort_flag)
+    st_shared_cluster_u32(mapa_shared(smem_u32(&sm.abort_flag), rank ^ 1u), 1u);
+  if (warp == NEW && rank == 0) {
+    tc_fence_after();
+    if (lane == 0) {
+      tc_commit_pair_mc(&sm.teardown, 0x1);
+      mbar_wait(&sm.teardown, 0u, nullptr, p.err, SITE_TEARDOWN);
+    }
+    __syncwarp();
+  }
+  tc_fence_before();
+  cluster_sync_all();
+  if (warp == NEW) {
+    tc_fence_after();
+    tmem_dealloc_pair(tbase, TMEM_COLS);
+  }
+}
+
+struct DeviceLaunchInfo {
+  bool attr_set = false;
+  int max_clusters = 0;
+};
+
+template <bool AU, bool BU, bool MMI>
+cudaError_t launch_one(const GemmF16Args& a, int cs, int c_vec, const CUtensorMap& ta, const CUtensorMap& tb,
+                       cudaStream_t s) {
+  auto kern = gemm_f16pair_kernel<AU, BU, MMI>;
+  static std::mutex mu;
+  static DeviceLaunchInfo info[64];
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(NT, 1, 1);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int max_clusters = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!info[dev].attr_set) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)SMEM_BYTES);
+      if (e != cudaSuccess) return e;
+      cfg.gridDim = dim3(2 * 64, 1, 1);
+      e = cudaOccupancyMaxActiveClusters(&info[dev].max_clusters, kern, &cfg);
+      if (e != cudaSuccess) return e;
+      if (info[dev].max_clusters < 1) return cudaErrorInvalidConfiguration;
+      info[dev].attr_set = true;
+    }
+    max_clusters = info[dev].max_clusters;
+  }
+  const int m_tiles = (a.M + BMP - 1) / BMP;
+  const int n_tiles = (a.N + BN - 1) / BN;
+  const long long tiles = (long long)a.batch * m_tiles * n_tiles;
+  const int ncl = (int)std::min<long long>(tiles, (long long)max_clusters);
+  cfg.gridDim = dim3(2 * ncl, 1, 1);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, cs, c_vec, ta, tb);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// fp16 operand maps: A as {K, M, batch} (box 64 x 128), B as {N, K, batch}
+// (box 64 x 64), both with 128-byte swizzle.
+cudaError_t make_maps(const GemmF16Args& a, CUtensorMap* ta, CUtensorMap* tb) {
+  const uint64_t ab = a.a_bstride ? (uint64_t)a.batch : 1, bb = a.b_bstride ? (uint64_t)a.batch : 1;
+  const uint64_t as = 2ull * (a.a_bstride ? (uint64_t)a.a_bstride : (uint64_t)a.M * a.K);
+  const uint64_t bs = 2ull * (a.b_bstride ? (uint64_t)a.b_bstride : (uint64_t)a.K * a.N);
+  cudaError_t e = make_tmap_3d(ta, a.A16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)a.K, (uint64_t)a.M, ab,
+                               2ull * a.K, as, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  return make_tmap_3d(tb, a.B16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)a.N, (uint64_t)a.K, bb, 2ull * a.N, bs,
+                      64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+}  // namespace gemmf
+
+cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool mmi, int chunk_k, cudaStream_t s,
+                                const char** kernel_name) {
+  using namespace gemmf;
+  const int cs = chunk_k / BK;
+  const int celem = (mmi || a.c_f32) ? 4 : 2;
+  const int c_vec = ((reinterpret_cast<uintptr_t>(a.C) % 16) == 0) && (((long long)a.N * celem) % 16 == 0);
+  CUtensorMap ta{}, tb{};
+  cudaError_t e = make_maps(a, &ta, &tb);
+  if (e != cudaSuccess) return e;
+  if (!mmi) {
+    *kernel_name = "gemm_tc05_pair_f16ops_a8w8";
+    return launch_one<false, false, false>(a, cs, c_vec, ta, tb, s);
+  }
+  *kernel_name = "gemm_tc05_pair_f16ops_matmul_integer";
+  if (!a_u8 && !b_u8) return launch_one<false, false, true>(a, cs, c_vec, ta, tb, s);
+  if (a_u8 && !b_u8) return launch_one<true, false, true>(a, cs, c_vec, ta, tb, s);
+  if (!a_u8 && b_u8) return launch_one<false, true, true>(a, cs, c_vec, ta, tb, s);
+  return launch_one<true, true, true>(a, cs, c_vec, ta, tb, s);
+}
+
+}  // namespace qmm

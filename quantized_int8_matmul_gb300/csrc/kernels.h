@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <cuda_runtime.h>
+#include <cuda_fp16.h>
 
 namespace qmm {
 
@@ -36,6 +37,35 @@ cudaError_t launch_gemm_tc(const GemmArgs& a, bool a_u8, bool b_u8, bool mmi, in
 // Requires 16-byte-aligned operand rows (the TMA path) and M >= 256.
 cudaError_t launch_gemm_tc_pair(const GemmArgs& a, bool a_u8, bool b_u8, bool mmi, int chunk_k, int c_vec,
                                 cudaStream_t s, const char** kernel_name);
+
+// The same GEMM on SM pairs from exact fp16 copies of the operands (made by
+// the pre-pass below), with the MatMulInteger row/column sums precomputed.
+struct GemmF16Args {
+  const void* A16;         // fp16 [batch][M][K] (or one [M][K] when a_bstride == 0)
+  const void* B16;         // fp16 [batch][K][N] (or one [K][N] when b_bstride == 0)
+  long long a_bstride;     // elements between batches (0 = shared)
+  long long b_bstride;
+  int batch, M, K, N;
+  void* C;                 // [batch][M][N]
+  int c_f32;
+  const float* act_scale;  int act_count;
+  const float* w_scale;    int w_count;
+  const void* a_zp;        int a_zp_count;
+  const void* b_zp;        int b_zp_count;
+  const int* rowsum;       // MatMulInteger with b_zp: rowsum(A), [batch or 1][M]
+  const int* colsum;       // MatMulInteger with a_zp: colsum(B), [batch or 1][N]
+  int zp_row_mod;
+  unsigned* err;
+};
+cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool mmi, int chunk_k, cudaStream_t s,
+                                const char** kernel_name);
+
+// Pre-pass: 8-bit rows -> exact fp16 (one warp per row; optional row sums), and
+// 8-bit [mats][rows][cols] -> fp16 with column sums (colsum zeroed here).
+cudaError_t launch_convert_rows(const void* src, bool u8, __half* dst, long long rows, int row_bytes, int* rowsum,
+                                cudaStream_t s);
+cudaError_t launch_convert_cols(const void* src, bool u8, __half* dst, int mats, int rows, int cols, int* colsum,
+                                cudaStream_t s);
 
 // Largest exact chunk length for the operand signedness (fp32 sums <= 2^24).
 int gemm_default_chunk_k(bool a_u8, bool b_u8);

@@ -72,6 +72,72 @@ int chunk_k_for(bool a_u8, bool b_u8) {
   return dflt;
 }
 
+
+// ---------------------------------------------------------------------------
+// Pre-pass path: operands converted once to exact fp16 copies in a caller
+// workspace (with the MatMulInteger row/column sums), then the SM-pair GEMM
+// stages fp16 tiles with TMA. Used for 16-byte-aligned rows, M >= 256 (after
+// folding a batch) and batches that are dense or shared.
+// Workspace: [A16: rowsA*K fp16][B16: matsB*K*N fp16][rowsum: rowsA int32]
+// [colsum: matsB*N int32], each region 256-byte aligned.
+struct PrepassPlan {
+  bool use = false;
+  int64_t rowsA = 0, matsB = 0;
+  size_t off_b = 0, off_rs = 0, off_cs = 0, bytes = 0;
+};
+
+size_t round256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+PrepassPlan prepass_plan(int64_t gb, int64_t gm, int64_t K, int64_t N, int64_t a_bstride, int64_t b_bstride,
+                         int64_t M) {
+  PrepassPlan pl;
+  if (K <= 0 || K % 16 != 0 || N % 16 != 0 || gm < 256) return pl;
+  if (gb > 1 && ((a_bstride != 0 && a_bstride != M * K) || (b_bstride != 0 && b_bstride != K * N))) return pl;
+  pl.rowsA = (gb > 1 && a_bstride != 0) ? gb * gm : gm;
+  pl.matsB = (gb > 1 && b_bstride != 0) ? gb : 1;
+  pl.off_b = round256((size_t)pl.rowsA * K * 2);
+  pl.off_rs = pl.off_b + round256((size_t)pl.matsB * K * N * 2);
+  pl.off_cs = pl.off_rs + round256((size_t)pl.rowsA * 4);
+  pl.bytes = pl.off_cs + round256((size_t)pl.matsB * N * 4);
+  pl.use = true;
+  return pl;
+}
+
+// Fold a shared B with a densely batched A into one GEMM of batch*M rows.
+void fold_batch(int64_t batch, int64_t M, int64_t K, int64_t a_bstride, int64_t b_bstride, int64_t* gb,
+                int64_t* gm) {
+  *gb = batch;
+  *gm = M;
+  if (batch > 1 && b_bstride == 0 && a_bstride == M * K) {
+    *gm = batch * M;
+    *gb = 1;
+  }
+}
+
+cudaError_t run_prepass_gemm(const PrepassPlan& pl, const void* A, bool au, const void* B, bool bu, bool need_rs,
+                             bool need_cs, void* ws, GemmF16Args& f, bool mmi, int chunk, cudaStream_t s,
+                             const char** name) {
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  __half* a16 = reinterpret_cast<__half*>(base);
+  __half* b16 = reinterpret_cast<__half*>(base + pl.off_b);
+  int* rs = reinterpret_cast<int*>(base + pl.off_rs);
+  int* cs = reinterpret_cast<int*>(base + pl.off_cs);
+  cudaError_t e = launch_convert_rows(A, au, a16, pl.rowsA, f.K, need_rs ? rs : nullptr, s);
+  if (e != cudaSuccess) return e;
+  if (need_cs) e = launch_convert_cols(B, bu, b16, (int)pl.matsB, f.K, f.N, cs, s);
+  else e = launch_convert_rows(B, bu, b16, pl.matsB * f.K, f.N, nullptr, s);
+  if (e != cudaSuccess) return e;
+  f.A16 = a16;
+  f.B16 = b16;
+  f.rowsum = rs;
+  f.colsum = cs;
+  const char* gname = "none";
+  e = launch_gemm_f16pair(f, au, bu, mmi, chunk, s, &gname);
+  *name = mmi ? "f16_prepass+gemm_tc05_pair_f16ops_matmul_integer" : "f16_prepass+gemm_tc05_pair_f16ops_a8w8";
+  return e;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) % 16) == 0; }
 }  // namespace
 
 int num_sms() {
@@ -275,6 +341,102 @@ qmm_status matmul_integer(const void* A, int a_dtype, const void* B, int b_dtype
   const bool au = a_dtype == QMM_U8, bu = b_dtype == QMM_U8;
   const char* name = "none";
   return finish_launch(launch_gemm_tc(g, au, bu, true, chunk_k_for(au, bu), s, &name), name);
+}
+
+size_t qmm_a8w8_workspace_bytes(int64_t M, int64_t K, int64_t N) {
+  if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return 0;
+  const PrepassPlan pl = prepass_plan(1, M, K, N, 0, 0, M);
+  return pl.use ? pl.bytes : 0;
+}
+
+qmm_status qmm_a8w8_ws(const int8_t* A, const int8_t* B, int64_t M, int64_t K, int64_t N, const float* act_scale,
+                       int64_t act_count, const float* weight_scale, int64_t w_count, void* C, int c_dtype,
+                       void* workspace, size_t workspace_bytes, void* stream) {
+  const PrepassPlan pl = (dim_ok(M) && dim_ok(K) && dim_ok(N)) ? prepass_plan(1, M, K, N, 0, 0, M) : PrepassPlan{};
+  if (!pl.use || M == 0 || N == 0 || !aligned16(A) || !aligned16(B))
+    return qmm_a8w8(A, B, M, K, N, act_scale, act_count, weight_scale, w_count, C, c_dtype, stream);
+  if (c_dtype != QMM_F32 && c_dtype != QMM_BF16) return QMM_ERR_INVALID_ARG;
+  if (act_count != 1 && act_count != M) return QMM_ERR_INVALID_ARG;
+  if (w_count != 1 && w_count != N) return QMM_ERR_INVALID_ARG;
+  if (!act_scale || !weight_scale || !C || !A || !B) return QMM_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < pl.bytes) return QMM_ERR_INVALID_ARG;
+  unsigned* err = err_word();
+  if (!err) return QMM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  GemmF16Args f{};
+  f.batch = 1;
+  f.M = (int)M;
+  f.K = (int)K;
+  f.N = (int)N;
+  f.C = C;
+  f.c_f32 = c_dtype == QMM_F32;
+  f.act_scale = act_scale;
+  f.act_count = (int)act_count;
+  f.w_scale = weight_scale;
+  f.w_count = (int)w_count;
+  f.zp_row_mod = (int)M;
+  f.err = err;
+  const char* name = "none";
+  return finish_launch(run_prepass_gemm(pl, A, false, B, false, false, false, workspace, f, false,
+                                        chunk_k_for(false, false), s, &name),
+                       name);
+}
+
+size_t matmul_integer_workspace_bytes(int64_t batch, int64_t M, int64_t K, int64_t N, int64_t a_batch_stride,
+                                      int64_t b_batch_stride) {
+  if (!dim_ok(batch) || !dim_ok(M) || !dim_ok(K) || !dim_ok(N) || batch * M > (int64_t)INT_MAX) return 0;
+  int64_t gb, gm;
+  fold_batch(batch, M, K, a_batch_stride, b_batch_stride, &gb, &gm);
+  const PrepassPlan pl = prepass_plan(gb, gm, K, N, a_batch_stride, b_batch_stride, M);
+  return pl.use ? pl.bytes : 0;
+}
+
+qmm_status matmul_integer_ws(const void* A, int a_dtype, const void* B, int b_dtype, int64_t batch, int64_t M,
+                             int64_t K, int64_t N, int64_t a_batch_stride, int64_t b_batch_stride,
+                             const void* a_zero_point, int64_t a_zp_count, const void* b_zero_point,
+                             int64_t b_zp_count, int32_t* C, void* workspace, size_t workspace_bytes, void* stream) {
+  PrepassPlan pl;
+  int64_t gb = batch, gm = M;
+  if (dim_ok(batch) && dim_ok(M) && dim_ok(K) && dim_ok(N) && batch * M <= (int64_t)INT_MAX &&
+      a_batch_stride >= 0 && b_batch_stride >= 0) {
+    fold_batch(batch, M, K, a_batch_stride, b_batch_stride, &gb, &gm);
+    pl = prepass_plan(gb, gm, K, N, a_batch_stride, b_batch_stride, M);
+  }
+  if (!pl.use || batch == 0 || M == 0 || N == 0 || !aligned16(A) || !aligned16(B))
+    return matmul_integer(A, a_dtype, B, b_dtype, batch, M, K, N, a_batch_stride, b_batch_stride, a_zero_point,
+                          a_zp_count, b_zero_point, b_zp_count, C, stream);
+  if ((a_dtype != QMM_S8 && a_dtype != QMM_U8) || (b_dtype != QMM_S8 && b_dtype != QMM_U8))
+    return QMM_ERR_INVALID_ARG;
+  if (a_zp_count != 0 && a_zp_count != 1 && a_zp_count != M) return QMM_ERR_INVALID_ARG;
+  if (b_zp_count != 0 && b_zp_count != 1 && b_zp_count != N) return QMM_ERR_INVALID_ARG;
+  if (!C || !A || !B || (a_zp_count > 0 && !a_zero_point) || (b_zp_count > 0 && !b_zero_point))
+    return QMM_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < pl.bytes) return QMM_ERR_INVALID_ARG;
+  if (gb * ((gm + 255) / 256) * ((N + 255) / 256) > INT_MAX) return QMM_ERR_UNSUPPORTED;
+  unsigned* err = err_word();
+  if (!err) return QMM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  GemmF16Args f{};
+  f.a_bstride = (gb > 1 && a_batch_stride != 0) ? gm * K : 0;
+  f.b_bstride = (gb > 1 && b_batch_stride != 0) ? K * N : 0;
+  f.batch = (int)gb;
+  f.M = (int)gm;
+  f.K = (int)K;
+  f.N = (int)N;
+  f.C = C;
+  f.a_zp = a_zero_point;
+  f.a_zp_count = (int)a_zp_count;
+  f.b_zp = b_zero_point;
+  f.b_zp_count = (int)b_zp_count;
+  f.zp_row_mod = (int)M;
+  f.err = err;
+  const bool au = a_dtype == QMM_U8, bu = b_dtype == QMM_U8;
+  const char* name = "none";
+  return finish_launch(run_prepass_gemm(pl, A, au, B, bu, b_zp_count > 0, a_zp_count > 0, workspace, f, true,
+                                        chunk_k_for(au, bu), s, &name),
+                       name);
 }
 
 size_t dynamic_quantize_linear_workspace_bytes(int64_t n) {
