@@ -21,7 +21,12 @@
 //    complete on the even CTA's `full` barrier (cta_group::2 form).
 //  * warp 8: TMEM allocation for the pair; in the even CTA one lane issues
 //    the pair MMAs (M=256, N=256, K=16) and commits to both CTAs' barriers.
-//  * warps 0-7: drain the accumulator after each K-chunk, run the epilogue.
+//  * warps 0-7: drain each K-chunk's fp32 accumulator into int32 running sums
+//    held in registers (each thread: one row, 128 columns), then run the
+//    epilogue from those registers.
+// TMEM holds two fp32 accumulators (columns [0,256) and [256,512)); K-chunks
+// alternate between them, so the tensor core fills one while the other is
+// drained and never waits for a drain or an epilogue.
 // Every wait is bounded (see common.cuh).
 #include "common.cuh"
 #include "kernels.h"
@@ -47,17 +52,21 @@ constexpr int B_BYTES = BK * BNH * 2;   // 16 KB
 constexpr int B_BOX = 64 * BK * 2;      // one 64-column B box: 8 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t SUM_COL = 256;
+constexpr uint32_t ACC_COLS = 256;     // one accumulator buffer
 constexpr int PAIR_ARRIVALS = 2 * NEW;
 
 struct Shared {
   uint64_t full[NS];      // even CTA: one arrival (expect_tx) + both CTAs' copy bytes
   uint64_t empty[NS];     // the pair's commit
-  uint64_t acc_full;      // the pair's commit
-  uint64_t acc_empty;     // even CTA: one arrival per drain warp of both CTAs
+  uint64_t acc_full[2];   // per accumulator buffer: the pair's commit
+  uint64_t acc_empty[2];  // even CTA: one arrival per drain warp of both CTAs
   uint64_t teardown;
   uint32_t tmem_base;
   int abort_flag;
+  // per drain warp, the current tile's operands of its CPW columns:
+  // A8W8 weight_scale (float bits) / MatMulInteger b_zp, and colsum(B)
+  uint32_t col_op[NEW][CPW];
+  int col_sum[NEW][CPW];
 };
 
 constexpr size_t SMEM_BYTES = (size_t)NS * STAGE_BYTES + sizeof(Shared) + 1024;
@@ -95,61 +104,70 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
       : "memory");
 }
 
-// Epilogue of one tile: this warp's 32 rows x CPW columns of the final int32
-// sums, dequantised (A8W8) or zero-point corrected (MatMulInteger), to C.
+// Per-tile operands of this warp's CPW columns, staged in shared memory by
+// the warp itself (4 columns per lane).
+template <bool BU, bool MMI>
+__device__ __forceinline__ void stage_columns(const GemmF16Args& p, Shared& sm, const TileCoord tc, int warp, int h,
+                                              int lane) {
+  const int* colsum = (MMI && p.a_zp_count > 0) ? p.colsum + (p.b_bstride ? (size_t)tc.b * p.N : 0) : nullptr;
+#pragma unroll
+  for (int j = 0; j < CPW / 32; ++j) {
+    const int col = lane * (CPW / 32) + j;
+    const int n = tc.n0 + h * CPW + col;
+    uint32_t op = 0u;
+    int cs = 0;
+    if (n < p.N) {
+      if (!MMI) {
+        op = __float_as_uint(__ldg(p.w_scale + (p.w_count == 1 ? 0 : n)));
+      } else {
+        if (p.b_zp_count > 0) {
+          const int zi = p.b_zp_count == 1 ? 0 : n;
+          op = BU ? (uint32_t)__ldg((const uint8_t*)p.b_zp + zi) : (uint32_t)(int)__ldg((const int8_t*)p.b_zp + zi);
+        }
+        if (colsum) cs = __ldg(colsum + n);
+      }
+    }
+    sm.col_op[warp][col] = op;
+    sm.col_sum[warp][col] = cs;
+  }
+  __syncwarp();
+}
+
+// Epilogue of one tile from the int32 sums in registers (this thread: one row,
+// this warp's CPW columns): dequantise (A8W8) or apply the zero-point
+// expansion (MatMulInteger), store C.
 template <bool AU, bool BU, bool MMI>
-__device__ __noinline__ void epilogue(const GemmF16Args& p, uint32_t tbase, const TileCoord tc, int q, int h, int lane,
-                                      int c_vec) {
-  const int rloc = q * 32 + lane;
-  const int row = tc.m0 + rloc;
-  const bool row_ok = row < p.M;
-  const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-  const size_t crow = ((size_t)tc.b * p.M + (size_t)(row_ok ? row : 0)) * (size_t)p.N;
+__device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm, uint32_t (&sums)[CPW],
+                                         const TileCoord tc, int warp, int q, int h, int lane, int c_vec) {
+  const int row = tc.m0 + q * 32 + lane;
+  if (row >= p.M) return;
+  const size_t crow = ((size_t)tc.b * p.M + (size_t)row) * (size_t)p.N;
   const uint64_t pol = l2_policy_evict_first();
+  const int mz = row % p.zp_row_mod;
   float as = 0.f;
   uint32_t za = 0u, rs = 0u;
-  if (row_ok) {
-    const int mz = row % p.zp_row_mod;
-    if (!MMI) {
-      as = __ldg(p.act_scale + (p.act_count == 1 ? 0 : mz));
-    } else {
-      if (p.a_zp_count > 0) {
-        const int zi = p.a_zp_count == 1 ? 0 : mz;
-        za = AU ? (uint32_t)__ldg((const uint8_t*)p.a_zp + zi) : (uint32_t)(int)__ldg((const int8_t*)p.a_zp + zi);
-      }
-      if (p.b_zp_count > 0) rs = (uint32_t)__ldg(p.rowsum + (size_t)(p.a_bstride ? tc.b : 0) * p.M + row);
+  if (!MMI) {
+    as = __ldg(p.act_scale + (p.act_count == 1 ? 0 : mz));
+  } else {
+    if (p.a_zp_count > 0) {
+      const int zi = p.a_zp_count == 1 ? 0 : mz;
+      za = AU ? (uint32_t)__ldg((const uint8_t*)p.a_zp + zi) : (uint32_t)(int)__ldg((const int8_t*)p.a_zp + zi);
     }
+    if (p.b_zp_count > 0) rs = (uint32_t)__ldg(p.rowsum + (size_t)(p.a_bstride ? tc.b : 0) * p.M + row);
   }
-  const int* colsum = (MMI && p.a_zp_count > 0) ? p.colsum + (p.b_bstride ? (size_t)tc.b * p.N : 0) : nullptr;
-
-  uint32_t hold[16];
-#pragma unroll 1
+  const uint32_t kzz = (uint32_t)p.K * za;
+#pragma unroll
   for (int g = 0; g < CPW / 16; ++g) {
-    uint32_t tot[16];
-    if ((g & 1) == 0) {
-      uint32_t t32[32];
-      tmem_ld32(tbase + lane_off + SUM_COL + (uint32_t)(h * CPW + g * 16), t32);   // warp-collective
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        tot[i] = t32[i];
-        hold[i] = t32[16 + i];
-      }
-    } else {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) tot[i] = hold[i];
-    }
     const int nb = tc.n0 + h * CPW + g * 16;
-    if (!row_ok || nb >= p.N) continue;
+    if (nb >= p.N) break;
     const bool full = (nb + 16 <= p.N) && c_vec;
-    uint32_t o[16];
+    uint32_t* o = &sums[g * 16];
     if (!MMI) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const int n = min(nb + i, p.N - 1);
-        const float ws = __ldg(p.w_scale + (p.w_count == 1 ? 0 : n));
-        float v = __int2float_rn((int)tot[i]);
+        float v = __int2float_rn((int)o[i]);
         v = __fmul_rn(v, as);
-        o[i] = __float_as_uint(__fmul_rn(v, ws));
+        o[i] = __float_as_uint(__fmul_rn(v, __uint_as_float(sm.col_op[warp][g * 16 + i])));
       }
       if (p.c_f32) {
         float* out = reinterpret_cast<float*>(p.C) + crow + nb;
@@ -179,14 +197,9 @@ __device__ __noinline__ void epilogue(const GemmF16Args& p, uint32_t tbase, cons
     } else {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const int n = min(nb + i, p.N - 1);
-        uint32_t zb = 0u;
-        if (p.b_zp_count > 0) {
-          const int zi = p.b_zp_count == 1 ? 0 : n;
-          zb = BU ? (uint32_t)__ldg((const uint8_t*)p.b_zp + zi) : (uint32_t)(int)__ldg((const int8_t*)p.b_zp + zi);
-        }
-        const uint32_t cs = colsum ? (uint32_t)__ldg(colsum + n) : 0u;
-        o[i] = tot[i] - za * cs - zb * rs + (uint32_t)p.K * za * zb;
+        const uint32_t zb = sm.col_op[warp][g * 16 + i];
+        const uint32_t cs = (uint32_t)sm.col_sum[warp][g * 16 + i];
+        o[i] = o[i] - za * cs - zb * rs + kzz * zb;
       }
       int32_t* out = reinterpret_cast<int32_t*>(p.C) + crow + nb;
       if (full) {
@@ -231,8 +244,10 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(&sm.full[i], 1);
       mbar_init(&sm.empty[i], 1);
     }
-    mbar_init(&sm.acc_full, 1);
-    mbar_init(&sm.acc_empty, PAIR_ARRIVALS);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.acc_full[i], 1);
+      mbar_init(&sm.acc_empty[i], PAIR_ARRIVALS);
+    }
     mbar_init(&sm.teardown, 1);
     sm.abort_flag = 0;
     fence_mbarrier_init();
@@ -254,11 +269,14 @@ __global__ void __launch_bounds__(NT, 1)
       bool ok = true;
       for (int tl = 0; tl < my_tiles && ok; ++tl) {
         for (int c = 0; c < cpt && ok; ++c) {
-          if (d > 0) {
-            ok = mbar_wait_cluster(&sm.acc_empty, (uint32_t)((d - 1) & 1), &sm.abort_flag, p.err, SITE_ACC_EMPTY);
+          const int ab = d & 1;   // accumulator buffer of this chunk
+          if (d >= 2) {
+            ok = mbar_wait_cluster(&sm.acc_empty[ab], (uint32_t)(((d >> 1) - 1) & 1), &sm.abort_flag, p.err,
+                                   SITE_ACC_EMPTY);
             if (!ok) break;
           }
           tc_fence_after();
+          const uint32_t tacc = tbase + (uint32_t)ab * ACC_COLS;
           const int s_beg = c * cs;
           const int s_end = min(spt, s_beg + cs);
           for (int s = s_beg; s < s_end; ++s, ++g) {
@@ -273,12 +291,12 @@ __global__ void __launch_bounds__(NT, 1)
               const uint64_t ad = sdesc_sw128(a_addr + (uint32_t)j * 32u, 16u, 1024u);
               // B: 64-column boxes 8 KB apart (LBO), 8-row k groups 1 KB apart (SBO)
               const uint64_t bd = sdesc_sw128(b_addr + (uint32_t)j * 2048u, (uint32_t)B_BOX, 1024u);
-              tc_mma_f16_pair(tbase, ad, bd, idesc, (s > s_beg || j > 0) ? 1u : 0u);
+              tc_mma_f16_pair(tacc, ad, bd, idesc, (s > s_beg || j > 0) ? 1u : 0u);
             }
             tc_commit_pair_mc(&sm.empty[slot], 0x3);
           }
           if (!ok) break;
-          tc_commit_pair_mc(&sm.acc_full, 0x3);
+          tc_commit_pair_mc(&sm.acc_full[ab], 0x3);
           ++d;
         }
       }
@@ -322,37 +340,41 @@ __global__ void __launch_bounds__(NT, 1)
     // ---------------- drain / epilogue warps ----------------
     const int q = warp & 3;
     const int h = warp >> 2;
-    const uint32_t acc_empty_leader = mapa_shared(smem_u32(&sm.acc_empty), 0);
+    const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&sm.acc_empty[0]), 0);
+    const uint32_t lane_off = (uint32_t)(q * 32) << 16;
+    uint32_t sums[CPW];
     int tl = 0, c = 0;
+    TileCoord tc = tile_coord(p, 0, cid, ncl, (int)rank);
+    if (my_tiles > 0) stage_columns<BU, MMI>(p, sm, tc, warp, h, lane);
     for (int d = 0; d < total_chunks; ++d) {
-      if (!mbar_wait_cluster(&sm.acc_full, (uint32_t)(d & 1), &sm.abort_flag, p.err, SITE_ACC_FULL)) break;
+      const int ab = d & 1;
+      if (!mbar_wait_cluster(&sm.acc_full[ab], (uint32_t)((d >> 1) & 1), &sm.abort_flag, p.err, SITE_ACC_FULL))
+        break;
       tc_fence_after();
-      const uint32_t lane_off = (uint32_t)(q * 32) << 16;
-      const uint32_t t_acc = tbase + lane_off + (uint32_t)(h * CPW);
-      const uint32_t t_sum = t_acc + SUM_COL;
-#pragma unroll 1
+      const uint32_t t_acc = tbase + lane_off + (uint32_t)ab * ACC_COLS + (uint32_t)(h * CPW);
+      // exact fp32 chunk sums -> int32, into the running sums (wrapping)
+#pragma unroll
       for (int g = 0; g < CPW / 16; ++g) {
         uint32_t acc[16];
-        uint32_t sum[16];
-        if (c > 0) {
-          tmem_ld16x2(t_acc + g * 16, acc, t_sum + g * 16, sum);
+        tmem_ld16(t_acc + g * 16, acc);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) sum[i] += (uint32_t)__float2int_rn(__uint_as_float(acc[i]));
-        } else {
-          tmem_ld16(t_acc + g * 16, acc);
-#pragma unroll
-          for (int i = 0; i < 16; ++i) sum[i] = (uint32_t)__float2int_rn(__uint_as_float(acc[i]));
+        for (int i = 0; i < 16; ++i) {
+          const uint32_t v = (uint32_t)__float2int_rn(__uint_as_float(acc[i]));
+          sums[g * 16 + i] = (c == 0) ? v : sums[g * 16 + i] + v;
         }
-        tmem_st16_async(t_sum + g * 16, sum);
       }
-      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote_cta(acc_empty_leader);
-      if (c == cpt - 1) epilogue<AU, BU, MMI>(p, tbase, tile_coord(p, tl, cid, ncl, (int)rank), q, h, lane, c_vec);
+      if (lane == 0) mbar_arrive_remote_cta(acc_empty_leader0 + (uint32_t)ab * 8u);
+      if (c == cpt - 1) {
+        epilogue<AU, BU, MMI>(p, sm, sums, tc, warp, q, h, lane, c_vec);
+        __syncwarp();   // the warp's staged operands are read: restage for the next tile
+        if (tl + 1 < my_tiles) stage_columns<BU, MMI>(p, sm, tile_coord(p, tl + 1, cid, ncl, (int)rank), warp, h, lane);
+      }
       if (++c == cpt) {
         c = 0;
         ++tl;
+        tc = tile_coord(p, tl, cid, ncl, (int)rank);
       }
     }
     tc_fence_before();
