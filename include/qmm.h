@@ -130,6 +130,23 @@ qmm_status qmm_a8w8_ws(const int8_t* A, const int8_t* B, int64_t M, int64_t K, i
                        void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The two passes of qmm_a8w8_ws as separate calls, for callers that time or
+ * schedule them apart, or that run several products on the same packed
+ * operands (e.g. the same A and B with different scales):
+ *   qmm_a8w8_pack    writes the fp16 copies of A and B into the workspace;
+ *   qmm_a8w8_packed  runs the SM-pair GEMM and the fused scaling on them.
+ * qmm_a8w8_pack(...) followed by qmm_a8w8_packed(...) on one stream gives the
+ * same result as qmm_a8w8_ws. Both return QMM_ERR_UNSUPPORTED when
+ * qmm_a8w8_workspace_bytes(M, K, N) is 0; pack requires 16-byte-aligned A and
+ * B. The workspace must not be modified between the two calls.
+ */
+qmm_status qmm_a8w8_pack(const int8_t* A, const int8_t* B, int64_t M, int64_t K, int64_t N, void* workspace,
+                         size_t workspace_bytes, void* stream);
+qmm_status qmm_a8w8_packed(int64_t M, int64_t K, int64_t N, const float* act_scale, int64_t act_count,
+                           const float* weight_scale, int64_t w_count, void* C, int c_dtype, const void* workspace,
+                           size_t workspace_bytes, void* stream);
+
+/*
  * Form (c): MatMulInteger with zero points. ROCm hip-ep PR #1248,
  * "feat(onnx-to-hip): lower quantized integer conv and matmul", section
  * "What", MatMulInteger paragraph:

@@ -53,14 +53,16 @@ def _load() -> ctypes.CDLL:
     lib.qmm_a8w8_workspace_bytes.argtypes = [i64, i64, i64]
     lib.qmm_a8w8_workspace_bytes.restype = sz
     lib.qmm_a8w8_ws.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, i64, vp, ci, vp, sz, vp]
+    lib.qmm_a8w8_pack.argtypes = [vp, vp, i64, i64, i64, vp, sz, vp]
+    lib.qmm_a8w8_packed.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, ci, vp, sz, vp]
     lib.matmul_integer_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64]
     lib.matmul_integer_workspace_bytes.restype = sz
     lib.matmul_integer_ws.argtypes = [vp, ci, vp, ci, i64, i64, i64, i64, i64, i64, vp, i64, vp, i64, vp, vp, sz, vp]
     lib.dynamic_quantize_linear_workspace_bytes.argtypes = [i64]
     lib.dynamic_quantize_linear_workspace_bytes.restype = ctypes.c_size_t
     lib.dynamic_quantize_linear.argtypes = [vp, i64, vp, vp, vp, vp, i64, vp, ctypes.c_size_t, vp]
-    for fn in ("qmm_w8_dequant", "qmm_a8w8", "qmm_a8w8_ws", "matmul_integer", "matmul_integer_ws",
-               "dynamic_quantize_linear"):
+    for fn in ("qmm_w8_dequant", "qmm_a8w8", "qmm_a8w8_ws", "qmm_a8w8_pack", "qmm_a8w8_packed", "matmul_integer",
+               "matmul_integer_ws", "dynamic_quantize_linear"):
         getattr(lib, fn).restype = ci
     lib.qmm_status_string.argtypes = [ci]
     lib.qmm_status_string.restype = ctypes.c_char_p
@@ -157,12 +159,13 @@ def matmul_integer_workspace_bytes(batch, M, K, N, a_batch_stride, b_batch_strid
     return int(_lib.matmul_integer_workspace_bytes(batch, M, K, N, a_batch_stride, b_batch_stride))
 
 
-def qmm_a8w8(A, B, act_scale, weight_scale, out=None, out_dtype=torch.bfloat16, stream=None, workspace=None):
+def qmm_a8w8(A, B, act_scale, weight_scale, out=None, out_dtype=torch.bfloat16, stream=None, workspace="auto"):
     """Form (b): C = out(f32(A @ B) * act_scale[m] * weight_scale[n]); A, B int8.
 
-    workspace: None runs the single-pass kernel; "auto" or a device tensor of at
-    least qmm_a8w8_workspace_bytes(M, K, N) bytes runs the two-pass path (fp16
-    operand copies, then the SM-pair GEMM) where it applies."""
+    workspace: "auto" (default) or a device tensor of at least
+    qmm_a8w8_workspace_bytes(M, K, N) bytes runs the two-pass path (fp16
+    operand copies, then the SM-pair GEMM) where it applies; None runs the
+    single-pass kernels."""
     _need(A, (torch.int8,), "A")
     _need(B, (torch.int8,), "B")
     _need(act_scale, (torch.float32,), "act_scale")
@@ -187,7 +190,32 @@ def qmm_a8w8(A, B, act_scale, weight_scale, out=None, out_dtype=torch.bfloat16, 
     return out
 
 
-def matmul_integer(A, B, a_zero_point=None, b_zero_point=None, out=None, stream=None, workspace=None):
+def qmm_a8w8_pack(A, B, workspace, stream=None):
+    """First pass of qmm_a8w8's two-pass path: fp16 copies of A and B into workspace."""
+    _need(A, (torch.int8,), "A")
+    _need(B, (torch.int8,), "B")
+    M, K = A.shape
+    N = B.shape[1]
+    st = _lib.qmm_a8w8_pack(_ptr(A), _ptr(B), M, K, N, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                            _stream(stream))
+    _check("qmm_a8w8_pack", st)
+
+
+def qmm_a8w8_packed(M, K, N, act_scale, weight_scale, workspace, out=None, out_dtype=torch.bfloat16, stream=None):
+    """Second pass: the SM-pair GEMM and fused scaling on operands packed by qmm_a8w8_pack."""
+    _need(act_scale, (torch.float32,), "act_scale")
+    _need(weight_scale, (torch.float32,), "weight_scale")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=workspace.device)
+    _need(out, (torch.float32, torch.bfloat16), "out")
+    st = _lib.qmm_a8w8_packed(M, K, N, _ptr(act_scale), act_scale.numel(), _ptr(weight_scale), weight_scale.numel(),
+                              _ptr(out), _TORCH_TO_QMM[out.dtype], _ptr(workspace),
+                              workspace.numel() * workspace.element_size(), _stream(stream))
+    _check("qmm_a8w8_packed", st)
+    return out
+
+
+def matmul_integer(A, B, a_zero_point=None, b_zero_point=None, out=None, stream=None, workspace="auto"):
     """Form (c): int32 C = (A - a_zp) @ (B - b_zp), A [...,M,K], B [K,N] (shared) or [...,K,N].
 
     workspace: as for qmm_a8w8 (None: single pass; "auto" or a tensor: two-pass

@@ -114,28 +114,37 @@ void fold_batch(int64_t batch, int64_t M, int64_t K, int64_t a_bstride, int64_t 
   }
 }
 
-cudaError_t run_prepass_gemm(const PrepassPlan& pl, const void* A, bool au, const void* B, bool bu, bool need_rs,
-                             bool need_cs, void* ws, GemmF16Args& f, bool mmi, int chunk, cudaStream_t s,
-                             const char** name) {
+// The pre-pass: fp16 copies of A and B (and the sums the zero points need).
+cudaError_t run_pack(const PrepassPlan& pl, const void* A, bool au, const void* B, bool bu, bool need_rs,
+                     bool need_cs, void* ws, int K, int N, cudaStream_t s) {
   uint8_t* base = static_cast<uint8_t*>(ws);
   __half* a16 = reinterpret_cast<__half*>(base);
   __half* b16 = reinterpret_cast<__half*>(base + pl.off_b);
   int* rs = reinterpret_cast<int*>(base + pl.off_rs);
   int* cs = reinterpret_cast<int*>(base + pl.off_cs);
-  cudaError_t e = launch_convert_rows(A, au, a16, pl.rowsA, f.K, need_rs ? rs : nullptr, s);
+  cudaError_t e = launch_convert_rows(A, au, a16, pl.rowsA, K, need_rs ? rs : nullptr, s);
   if (e != cudaSuccess) return e;
-  if (need_cs) e = launch_convert_cols(B, bu, b16, (int)pl.matsB, f.K, f.N, cs, s);
-  else e = launch_convert_rows(B, bu, b16, pl.matsB * f.K, f.N, nullptr, s);
-  if (e != cudaSuccess) return e;
-  f.A16 = a16;
-  f.B16 = b16;
-  f.rowsum = rs;
-  f.colsum = cs;
-  const char* gname = "none";
-  e = launch_gemm_f16pair(f, au, bu, mmi, chunk, s, &gname);
-  *name = mmi ? "f16_prepass+gemm_tc05_pair_f16ops_matmul_integer" : "f16_prepass+gemm_tc05_pair_f16ops_a8w8";
-  return e;
+  if (need_cs) return launch_convert_cols(B, bu, b16, (int)pl.matsB, K, N, cs, s);
+  return launch_convert_rows(B, bu, b16, pl.matsB * K, N, nullptr, s);
 }
+
+// The GEMM on packed operands.
+cudaError_t run_packed_gemm(const PrepassPlan& pl, const void* ws, GemmF16Args& f, bool au, bool bu, bool mmi,
+                            int chunk, cudaStream_t s) {
+  const uint8_t* base = static_cast<const uint8_t*>(ws);
+  f.A16 = base;
+  f.B16 = base + pl.off_b;
+  f.rowsum = reinterpret_cast<const int*>(base + pl.off_rs);
+  f.colsum = reinterpret_cast<const int*>(base + pl.off_cs);
+  const char* gname = "none";
+  return launch_gemm_f16pair(f, au, bu, mmi, chunk, s, &gname);
+}
+
+const char* kPackName = "f16_prepass";
+const char* kPackedA8W8 = "gemm_tc05_pair_f16ops_a8w8";
+const char* kPackedMMI = "gemm_tc05_pair_f16ops_matmul_integer";
+const char* kTwoPassA8W8 = "f16_prepass+gemm_tc05_pair_f16ops_a8w8";
+const char* kTwoPassMMI = "f16_prepass+gemm_tc05_pair_f16ops_matmul_integer";
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) % 16) == 0; }
 }  // namespace
@@ -377,10 +386,9 @@ qmm_status qmm_a8w8_ws(const int8_t* A, const int8_t* B, int64_t M, int64_t K, i
   f.w_count = (int)w_count;
   f.zp_row_mod = (int)M;
   f.err = err;
-  const char* name = "none";
-  return finish_launch(run_prepass_gemm(pl, A, false, B, false, false, false, workspace, f, false,
-                                        chunk_k_for(false, false), s, &name),
-                       name);
+  cudaError_t e = run_pack(pl, A, false, B, false, false, false, workspace, (int)K, (int)N, s);
+  if (e == cudaSuccess) e = run_packed_gemm(pl, workspace, f, false, false, false, chunk_k_for(false, false), s);
+  return finish_launch(e, kTwoPassA8W8);
 }
 
 size_t matmul_integer_workspace_bytes(int64_t batch, int64_t M, int64_t K, int64_t N, int64_t a_batch_stride,
@@ -433,10 +441,53 @@ qmm_status matmul_integer_ws(const void* A, int a_dtype, const void* B, int b_dt
   f.zp_row_mod = (int)M;
   f.err = err;
   const bool au = a_dtype == QMM_U8, bu = b_dtype == QMM_U8;
-  const char* name = "none";
-  return finish_launch(run_prepass_gemm(pl, A, au, B, bu, b_zp_count > 0, a_zp_count > 0, workspace, f, true,
-                                        chunk_k_for(au, bu), s, &name),
-                       name);
+  cudaError_t e = run_pack(pl, A, au, B, bu, b_zp_count > 0, a_zp_count > 0, workspace, (int)K, (int)N, s);
+  if (e == cudaSuccess) e = run_packed_gemm(pl, workspace, f, au, bu, true, chunk_k_for(au, bu), s);
+  return finish_launch(e, kTwoPassMMI);
+}
+
+qmm_status qmm_a8w8_pack(const int8_t* A, const int8_t* B, int64_t M, int64_t K, int64_t N, void* workspace,
+                         size_t workspace_bytes, void* stream) {
+  if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return QMM_ERR_INVALID_ARG;
+  const PrepassPlan pl = prepass_plan(1, M, K, N, 0, 0, M);
+  if (!pl.use) return QMM_ERR_UNSUPPORTED;
+  if (!A || !B || !aligned16(A) || !aligned16(B)) return QMM_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < pl.bytes) return QMM_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  return finish_launch(run_pack(pl, A, false, B, false, false, false, workspace, (int)K, (int)N, s), kPackName);
+}
+
+qmm_status qmm_a8w8_packed(int64_t M, int64_t K, int64_t N, const float* act_scale, int64_t act_count,
+                           const float* weight_scale, int64_t w_count, void* C, int c_dtype, const void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return QMM_ERR_INVALID_ARG;
+  const PrepassPlan pl = prepass_plan(1, M, K, N, 0, 0, M);
+  if (!pl.use) return QMM_ERR_UNSUPPORTED;
+  if (c_dtype != QMM_F32 && c_dtype != QMM_BF16) return QMM_ERR_INVALID_ARG;
+  if (act_count != 1 && act_count != M) return QMM_ERR_INVALID_ARG;
+  if (w_count != 1 && w_count != N) return QMM_ERR_INVALID_ARG;
+  if (!act_scale || !weight_scale || !C) return QMM_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < pl.bytes) return QMM_ERR_INVALID_ARG;
+  unsigned* err = err_word();
+  if (!err) return QMM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  GemmF16Args f{};
+  f.batch = 1;
+  f.M = (int)M;
+  f.K = (int)K;
+  f.N = (int)N;
+  f.C = C;
+  f.c_f32 = c_dtype == QMM_F32;
+  f.act_scale = act_scale;
+  f.act_count = (int)act_count;
+  f.w_scale = weight_scale;
+  f.w_count = (int)w_count;
+  f.zp_row_mod = (int)M;
+  f.err = err;
+  return finish_launch(run_packed_gemm(pl, workspace, f, false, false, false, chunk_k_for(false, false), s),
+                       kPackedA8W8);
 }
 
 size_t dynamic_quantize_linear_workspace_bytes(int64_t n) {

@@ -19,7 +19,7 @@ SHAPES = [(1, 16, 16), (3, 31, 7), (128, 64, 256), (129, 258, 200), (17, 1040, 3
 
 def run(A, B, a_s, w_s, out):
     dt = torch.bfloat16 if out == "bf16" else torch.float32
-    C = q.qmm_a8w8(dev(A), dev(B), dev(a_s), dev(w_s), out_dtype=dt)
+    C = q.qmm_a8w8(dev(A), dev(B), dev(a_s), dev(w_s), out_dtype=dt, workspace=None)
     q.check_device_error()
     return host(C)
 

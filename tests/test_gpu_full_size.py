@@ -27,18 +27,23 @@ def test_w8_dequant_f32_64x256x192():
     assert_within(host(C).astype(np.float64), exact, bound, 23, "w8 64x256x192")
 
 
-def test_a8w8_4096():
+@pytest.mark.parametrize("workspace,kernel", [("auto", "f16_prepass+gemm_tc05_pair_f16ops_a8w8"),
+                                              (None, "gemm_tc05_pair_exact_a8w8")])
+def test_a8w8_4096(workspace, kernel):
     w = W.a8w8_4096()
-    C = q.qmm_a8w8(dev(w.A), dev(w.B), dev(w.act_scale), dev(w.weight_scale), out_dtype=torch.bfloat16)
+    C = q.qmm_a8w8(dev(w.A), dev(w.B), dev(w.act_scale), dev(w.weight_scale), out_dtype=torch.bfloat16,
+                   workspace=workspace)
     q.check_device_error()
-    assert q.last_kernel() == "gemm_tc05_pair_exact_a8w8"
+    assert q.last_kernel() == kernel
     got = host(C)
     rows = sample(4096, 40, 1)
     want = O.a8w8(w.A[rows], w.B, w.act_scale[rows], w.weight_scale, "bf16")
     assert_equal(got[rows], want, "a8w8 4096^3 sampled rows")
 
 
-def test_dql_then_matmul_integer_8192x4096x11008():
+@pytest.mark.parametrize("workspace,kernel", [("auto", "f16_prepass+gemm_tc05_pair_f16ops_matmul_integer"),
+                                              (None, "gemm_tc05_pair_exact_matmul_integer")])
+def test_dql_then_matmul_integer_8192x4096x11008(workspace, kernel):
     w = W.dql_matmul_integer_8192x4096x11008()
     y, s, zp, rs = q.dynamic_quantize_linear(dev(w.x), row_len=4096)
     assert q.last_kernel() == "dql_minmax+dql_quantize_rows"
@@ -47,9 +52,9 @@ def test_dql_then_matmul_integer_8192x4096x11008():
     assert_equal(host(y), wy, "DQL 8192x4096")
     assert_equal(host(rs), O.row_sums(wy, 4096), "DQL row sums")
     # the zero point stays on the device between the two calls
-    C = q.matmul_integer(y, dev(w.B), a_zero_point=zp, b_zero_point=dev(w.b_zp))
+    C = q.matmul_integer(y, dev(w.B), a_zero_point=zp, b_zero_point=dev(w.b_zp), workspace=workspace)
     q.check_device_error()
-    assert q.last_kernel() == "gemm_tc05_pair_exact_matmul_integer"
+    assert q.last_kernel() == kernel
     rows = sample(8192, 16, 2)
     want = O.matmul_integer(wy[rows], w.B, int(wzp), w.b_zp)
     assert_equal(host(C)[rows], want, "MatMulInteger 8192x4096x11008 sampled rows")
@@ -74,6 +79,7 @@ def test_batched_matmul_integer_shared_b():
     C = q.matmul_integer(dev(w.A), dev(w.B), a_zero_point=dev(np.array([w.a_zp], np.int8)),
                          b_zero_point=dev(np.array([w.b_zp], np.int8)))
     q.check_device_error()
+    assert q.last_kernel() == "f16_prepass+gemm_tc05_pair_f16ops_matmul_integer"
     assert C.shape == (8, 16, 512, 1024)
     got = host(C).reshape(-1, 1024)
     rows = sample(8 * 16 * 512, 48, 4)

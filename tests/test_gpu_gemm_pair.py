@@ -27,13 +27,14 @@ def rand(rng, dt, shape):
 def a8w8(A, B, a_s, w_s, out="f32"):
     import torch
     dt = torch.bfloat16 if out == "bf16" else torch.float32
-    C = q.qmm_a8w8(dev(A), dev(B), dev(a_s), dev(w_s), out_dtype=dt)
+    C = q.qmm_a8w8(dev(A), dev(B), dev(a_s), dev(w_s), out_dtype=dt, workspace=None)
     q.check_device_error()
     return host(C)
 
 
 def mmi(A, B, a_zp=None, b_zp=None):
-    C = q.matmul_integer(dev(A), dev(B), None if a_zp is None else dev(a_zp), None if b_zp is None else dev(b_zp))
+    C = q.matmul_integer(dev(A), dev(B), None if a_zp is None else dev(a_zp), None if b_zp is None else dev(b_zp),
+                         workspace=None)
     q.check_device_error()
     return host(C)
 

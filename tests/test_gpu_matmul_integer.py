@@ -23,7 +23,8 @@ def rand(rng, dt, shape):
 
 
 def run(A, B, a_zp=None, b_zp=None):
-    C = q.matmul_integer(dev(A), dev(B), None if a_zp is None else dev(a_zp), None if b_zp is None else dev(b_zp))
+    C = q.matmul_integer(dev(A), dev(B), None if a_zp is None else dev(a_zp), None if b_zp is None else dev(b_zp),
+                         workspace=None)
     q.check_device_error()
     return host(C)
 

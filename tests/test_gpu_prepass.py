@@ -164,3 +164,27 @@ def test_workspace_too_small_is_rejected():
     small = torch.empty(need - 256, dtype=torch.uint8, device="cuda")
     with pytest.raises(q.QmmError):
         a8w8(w.A, w.B, w.act_scale, w.weight_scale, "bf16", workspace=small)
+
+
+def test_pack_then_packed_equals_one_call_and_reuses_the_pack():
+    w = W.a8w8(512, 1024, 384, seed=3)
+    A, B = dev(w.A), dev(w.B)
+    ws = torch.empty(q.qmm_a8w8_workspace_bytes(512, 1024, 384), dtype=torch.uint8, device="cuda")
+    q.qmm_a8w8_pack(A, B, ws)
+    assert q.last_kernel() == "f16_prepass"
+    for seed in (0, 1):
+        rng = np.random.default_rng(seed)
+        a_s = rng.uniform(0.005, 0.02, 512).astype(np.float32)
+        w_s = rng.uniform(0.001, 0.01, 384).astype(np.float32)
+        C = q.qmm_a8w8_packed(512, 1024, 384, dev(a_s), dev(w_s), ws)
+        q.check_device_error()
+        assert q.last_kernel() == "gemm_tc05_pair_f16ops_a8w8"
+        assert_equal(host(C), O.a8w8(w.A, w.B, a_s, w_s, "bf16"), f"packed, scales {seed}")
+
+
+def test_pack_rejects_shapes_outside_the_path():
+    A = torch.zeros((100, 64), dtype=torch.int8, device="cuda")
+    B = torch.zeros((64, 64), dtype=torch.int8, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    with pytest.raises(q.QmmError):
+        q.qmm_a8w8_pack(A, B, ws)
