@@ -33,6 +33,40 @@ __device__ __forceinline__ int dp4a_sum(uint32_t w, int acc) {
   return __dp4a((int)w, 0x01010101, acc);
 }
 
+// A and B together, no sums: 16-byte chunks [0, nA) of A then [0, nB) of B,
+// grid-stride with four chunks (four loads) in flight per thread.
+template <bool UA, bool UB>
+__global__ void __launch_bounds__(256) convert_flat_kernel(const uint8_t* __restrict__ A, __half* __restrict__ A16,
+                                                           long long nA, const uint8_t* __restrict__ B,
+                                                           __half* __restrict__ B16, long long nB) {
+  const long long total = nA + nB;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const long long c = i + j * stride;
+      if (c < total) v[j] = ldg_nc_v4(c < nA ? A + 16 * c : B + 16 * (c - nA));
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const long long c = i + j * stride;
+      if (c >= total) break;
+      uint32_t h[8];
+      __half* d;
+      if (c < nA) {
+        convert16<UA>(v[j], h);
+        d = A16 + 16 * c;
+      } else {
+        convert16<UB>(v[j], h);
+        d = B16 + 16 * (c - nA);
+      }
+      st_global_v4(d, h[0], h[1], h[2], h[3]);
+      st_global_v4(d + 8, h[4], h[5], h[6], h[7]);
+    }
+  }
+}
+
 // One warp per row (grid-stride over rows): row r of `rows` rows of
 // `row_bytes` bytes (a multiple of 16, rows 16-byte aligned) becomes fp16 in
 // dst; with ROWSUM, rowsum[r] = sum of the row's values (int32, wrapping).
@@ -47,17 +81,25 @@ __global__ void __launch_bounds__(256) convert_rows_kernel(const uint8_t* __rest
     const uint8_t* s = src + r * row_bytes;
     __half* d = dst + r * row_bytes;
     int acc = 0;
-    for (int c = lane; c < chunks; c += 32) {
-      const uint4 v = ldg_nc_v4(s + 16 * c);
-      uint32_t h[8];
-      convert16<U>(v, h);
-      st_global_v4(d + 16 * c, h[0], h[1], h[2], h[3]);
-      st_global_v4(d + 16 * c + 8, h[4], h[5], h[6], h[7]);
-      if (ROWSUM) {
-        acc = dp4a_sum<U>(v.x, acc);
-        acc = dp4a_sum<U>(v.y, acc);
-        acc = dp4a_sum<U>(v.z, acc);
-        acc = dp4a_sum<U>(v.w, acc);
+    for (int c0 = lane; c0 < chunks; c0 += 128) {   // four chunks (loads) in flight per lane
+      uint4 v[4];
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if (c0 + 32 * j < chunks) v[j] = ldg_nc_v4(s + 16 * (c0 + 32 * j));
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = c0 + 32 * j;
+        if (c >= chunks) break;
+        uint32_t h[8];
+        convert16<U>(v[j], h);
+        st_global_v4(d + 16 * c, h[0], h[1], h[2], h[3]);
+        st_global_v4(d + 16 * c + 8, h[4], h[5], h[6], h[7]);
+        if (ROWSUM) {
+          acc = dp4a_sum<U>(v[j].x, acc);
+          acc = dp4a_sum<U>(v[j].y, acc);
+          acc = dp4a_sum<U>(v[j].z, acc);
+          acc = dp4a_sum<U>(v[j].w, acc);
+        }
       }
     }
     if (ROWSUM) {
@@ -91,6 +133,7 @@ __global__ void __launch_bounds__(256) convert_cols_kernel(const uint8_t* __rest
 #pragma unroll
     for (int i = 0; i < 16; ++i) sum[i] = 0;
     const int r_end = min(rows, (rb + 1) * kColRows);
+#pragma unroll 4
     for (int r = rb * kColRows; r < r_end; ++r) {
       const size_t off = base + (size_t)r * cols + 16 * (size_t)cc;
       const uint4 v = ldg_nc_v4(src + off);
@@ -131,6 +174,21 @@ cudaError_t launch_convert_rows(const void* src, bool u8, __half* dst, long long
     if (u8) convert_rows_kernel<true, false><<<grid, 256, 0, s>>>(p, dst, rows, row_bytes, nullptr);
     else convert_rows_kernel<false, false><<<grid, 256, 0, s>>>(p, dst, rows, row_bytes, nullptr);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert_flat(const void* A, bool au, __half* A16, long long a_bytes, const void* B, bool bu,
+                                __half* B16, long long b_bytes, cudaStream_t s) {
+  using namespace conv;
+  const long long nA = a_bytes / 16, nB = b_bytes / 16;
+  if (nA + nB <= 0) return cudaSuccess;
+  const int grid = grid_for((nA + nB + 3) / 4, 256);
+  const uint8_t* a = static_cast<const uint8_t*>(A);
+  const uint8_t* b = static_cast<const uint8_t*>(B);
+  if (au && bu) convert_flat_kernel<true, true><<<grid, 256, 0, s>>>(a, A16, nA, b, B16, nB);
+  else if (au) convert_flat_kernel<true, false><<<grid, 256, 0, s>>>(a, A16, nA, b, B16, nB);
+  else if (bu) convert_flat_kernel<false, true><<<grid, 256, 0, s>>>(a, A16, nA, b, B16, nB);
+  else convert_flat_kernel<false, false><<<grid, 256, 0, s>>>(a, A16, nA, b, B16, nB);
   return cudaGetLastError();
 }
 

@@ -122,10 +122,13 @@ cudaError_t run_pack(const PrepassPlan& pl, const void* A, bool au, const void* 
   __half* b16 = reinterpret_cast<__half*>(base + pl.off_b);
   int* rs = reinterpret_cast<int*>(base + pl.off_rs);
   int* cs = reinterpret_cast<int*>(base + pl.off_cs);
-  cudaError_t e = launch_convert_rows(A, au, a16, pl.rowsA, K, need_rs ? rs : nullptr, s);
+  if (!need_rs && !need_cs)   // one launch for both operands
+    return launch_convert_flat(A, au, a16, pl.rowsA * K, B, bu, b16, pl.matsB * K * N, s);
+  cudaError_t e = need_rs ? launch_convert_rows(A, au, a16, pl.rowsA, K, rs, s)
+                          : launch_convert_flat(A, au, a16, pl.rowsA * K, nullptr, bu, nullptr, 0, s);
   if (e != cudaSuccess) return e;
   if (need_cs) return launch_convert_cols(B, bu, b16, (int)pl.matsB, K, N, cs, s);
-  return launch_convert_rows(B, bu, b16, pl.matsB * K, N, nullptr, s);
+  return launch_convert_flat(nullptr, au, nullptr, 0, B, bu, b16, pl.matsB * K * N, s);
 }
 
 // The GEMM on packed operands.
