@@ -38,17 +38,19 @@
 namespace qmm {
 namespace gemmf {
 
+// Pair tile: 256 rows x BN columns, BN = 256 or 224 (a template parameter,
+// chosen per problem by the launcher to fill the last wave of tiles). Each
+// CTA stages two 64-column B boxes (128 columns) and the MMA reads BN/2.
 constexpr int BM = 128;
 constexpr int BMP = 2 * BM;
-constexpr int BN = 256;
-constexpr int BNH = BN / 2;
+constexpr int BN_MAX = 256;
 constexpr int BK = 64;
 constexpr int NS = 6;                   // stages in the ring
 constexpr int NEW = 8;                  // drain / epilogue warps
 constexpr int NT = NEW * 32 + 64;       // + MMA warp + producer warp
-constexpr int CPW = 1024 / NEW;         // accumulator columns per drain warp (128)
+constexpr int CPW_MAX = BN_MAX / 2;     // accumulator columns per drain warp (two warps per TMEM lane quarter)
 constexpr int A_BYTES = BM * BK * 2;    // 16 KB
-constexpr int B_BYTES = BK * BNH * 2;   // 16 KB
+constexpr int B_BYTES = BK * 128 * 2;   // two 64-column boxes: 16 KB
 constexpr int B_BOX = 64 * BK * 2;      // one 64-column B box: 8 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr uint32_t TMEM_COLS = 512;
@@ -65,8 +67,8 @@ struct Shared {
   int abort_flag;
   // per drain warp, the current tile's operands of its CPW columns:
   // A8W8 weight_scale (float bits) / MatMulInteger b_zp, and colsum(B)
-  uint32_t col_op[NEW][CPW];
-  int col_sum[NEW][CPW];
+  uint32_t col_op[NEW][CPW_MAX];
+  int col_sum[NEW][CPW_MAX];
 };
 
 constexpr size_t SMEM_BYTES = (size_t)NS * STAGE_BYTES + sizeof(Shared) + 1024;
@@ -81,6 +83,7 @@ struct TileCoord {
   int b, m0, n0;   // m0: this CTA's first row; n0: the pair tile's first column
 };
 
+template <int BN>
 __device__ __forceinline__ TileCoord tile_coord(const GemmF16Args& p, int tile_local, int cid, int ncl, int rank) {
   const int m_tiles = (p.M + BMP - 1) / BMP;
   const int n_tiles = (p.N + BN - 1) / BN;
@@ -105,14 +108,12 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
 }
 
 // Per-tile operands of this warp's CPW columns, staged in shared memory by
-// the warp itself (4 columns per lane).
-template <bool BU, bool MMI>
+// the warp itself.
+template <int CPW, bool BU, bool MMI>
 __device__ __forceinline__ void stage_columns(const GemmF16Args& p, Shared& sm, const TileCoord tc, int warp, int h,
                                               int lane) {
   const int* colsum = (MMI && p.a_zp_count > 0) ? p.colsum + (p.b_bstride ? (size_t)tc.b * p.N : 0) : nullptr;
-#pragma unroll
-  for (int j = 0; j < CPW / 32; ++j) {
-    const int col = lane * (CPW / 32) + j;
+  for (int col = lane; col < CPW; col += 32) {
     const int n = tc.n0 + h * CPW + col;
     uint32_t op = 0u;
     int cs = 0;
@@ -136,7 +137,7 @@ __device__ __forceinline__ void stage_columns(const GemmF16Args& p, Shared& sm, 
 // Epilogue of one tile from the int32 sums in registers (this thread: one row,
 // this warp's CPW columns): dequantise (A8W8) or apply the zero-point
 // expansion (MatMulInteger), store C.
-template <bool AU, bool BU, bool MMI>
+template <int CPW, bool AU, bool BU, bool MMI>
 __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm, uint32_t (&sums)[CPW],
                                          const TileCoord tc, int warp, int q, int h, int lane, int c_vec) {
   const int row = tc.m0 + q * 32 + lane;
@@ -213,10 +214,13 @@ __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm,
   }
 }
 
-template <bool AU, bool BU, bool MMI>
+template <int BN, bool AU, bool BU, bool MMI>
 __global__ void __launch_bounds__(NT, 1)
     gemm_f16pair_kernel(const GemmF16Args p, const int cs, const int c_vec, const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB) {
+  constexpr int BNH = BN / 2;   // B columns of each CTA
+  constexpr int CPW = BN / 2;   // accumulator columns per drain warp
+  static_assert(BN % 32 == 0 && BN <= BN_MAX && BNH <= 128, "pair tile width");
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
@@ -309,7 +313,7 @@ __global__ void __launch_bounds__(NT, 1)
       prefetch_tmap(&tmB);
       const uint32_t full_leader0 = mapa_shared(smem_u32(&sm.full[0]), 0);
       int tl = 0, s = 0;
-      TileCoord tc = tile_coord(p, 0, cid, ncl, (int)rank);
+      TileCoord tc = tile_coord<BN>(p, 0, cid, ncl, (int)rank);
       int g = 0;
       for (; g < total_stages; ++g) {
         const int slot = g % NS;
@@ -326,7 +330,7 @@ __global__ void __launch_bounds__(NT, 1)
         tma_load_3d_pair(dst + A_BYTES + B_BOX, &tmB, nc + 64, s * BK, bb, bar);
         if (++s == spt) {
           s = 0;
-          tc = tile_coord(p, ++tl, cid, ncl, (int)rank);
+          tc = tile_coord<BN>(p, ++tl, cid, ncl, (int)rank);
         }
       }
       // The even CTA's `full` barriers count both CTAs' bytes: once the phases
@@ -344,8 +348,8 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     uint32_t sums[CPW];
     int tl = 0, c = 0;
-    TileCoord tc = tile_coord(p, 0, cid, ncl, (int)rank);
-    if (my_tiles > 0) stage_columns<BU, MMI>(p, sm, tc, warp, h, lane);
+    TileCoord tc = tile_coord<BN>(p, 0, cid, ncl, (int)rank);
+    if (my_tiles > 0) stage_columns<CPW, BU, MMI>(p, sm, tc, warp, h, lane);
     for (int d = 0; d < total_chunks; ++d) {
       const int ab = d & 1;
       if (!mbar_wait_cluster(&sm.acc_full[ab], (uint32_t)((d >> 1) & 1), &sm.abort_flag, p.err, SITE_ACC_FULL))
@@ -367,14 +371,15 @@ __global__ void __launch_bounds__(NT, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_remote_cta(acc_empty_leader0 + (uint32_t)ab * 8u);
       if (c == cpt - 1) {
-        epilogue<AU, BU, MMI>(p, sm, sums, tc, warp, q, h, lane, c_vec);
+        epilogue<CPW, AU, BU, MMI>(p, sm, sums, tc, warp, q, h, lane, c_vec);
         __syncwarp();   // the warp's staged operands are read: restage for the next tile
-        if (tl + 1 < my_tiles) stage_columns<BU, MMI>(p, sm, tile_coord(p, tl + 1, cid, ncl, (int)rank), warp, h, lane);
+        if (tl + 1 < my_tiles)
+          stage_columns<CPW, BU, MMI>(p, sm, tile_coord<BN>(p, tl + 1, cid, ncl, (int)rank), warp, h, lane);
       }
       if (++c == cpt) {
         c = 0;
         ++tl;
-        tc = tile_coord(p, tl, cid, ncl, (int)rank);
+        tc = tile_coord<BN>(p, tl, cid, ncl, (int)rank);
       }
     }
     tc_fence_before();
@@ -404,10 +409,10 @@ struct DeviceLaunchInfo {
   int max_clusters = 0;
 };
 
-template <bool AU, bool BU, bool MMI>
+template <int BN, bool AU, bool BU, bool MMI>
 cudaError_t launch_one(const GemmF16Args& a, int cs, int c_vec, const CUtensorMap& ta, const CUtensorMap& tb,
                        cudaStream_t s) {
-  auto kern = gemm_f16pair_kernel<AU, BU, MMI>;
+  auto kern = gemm_f16pair_kernel<BN, AU, BU, MMI>;
   static std::mutex mu;
   static DeviceLaunchInfo info[64];
   int dev = 0;
@@ -461,6 +466,38 @@ cudaError_t make_maps(const GemmF16Args& a, CUtensorMap* ta, CUtensorMap* tb) {
                       64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+
+// Pair-tile width: the one whose tiles fill the last wave best. The cost of a
+// width is its number of waves (tiles over the pairs that run at once) times
+// the tile width plus a fixed per-tile overhead (about 16 columns' worth of
+// MMA time: pipeline fill, the last drain and epilogue).
+int choose_tile_width(const GemmF16Args& a) {
+  const long long clusters = std::max(1, num_sms() / 2);
+  const long long m_tiles = (a.M + BMP - 1) / BMP;
+  int best = 256;
+  long long best_cost = -1;
+  for (int bn : {256, 224}) {
+    const long long tiles = (long long)a.batch * m_tiles * ((a.N + bn - 1) / bn);
+    const long long waves = (tiles + clusters - 1) / clusters;
+    const long long cost = waves * (bn + 16);
+    if (best_cost < 0 || cost < best_cost) {
+      best = bn;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
+template <int BN>
+cudaError_t dispatch(const GemmF16Args& a, bool a_u8, bool b_u8, bool mmi, int cs, int c_vec, const CUtensorMap& ta,
+                     const CUtensorMap& tb, cudaStream_t s) {
+  if (!mmi) return launch_one<BN, false, false, false>(a, cs, c_vec, ta, tb, s);
+  if (!a_u8 && !b_u8) return launch_one<BN, false, false, true>(a, cs, c_vec, ta, tb, s);
+  if (a_u8 && !b_u8) return launch_one<BN, true, false, true>(a, cs, c_vec, ta, tb, s);
+  if (!a_u8 && b_u8) return launch_one<BN, false, true, true>(a, cs, c_vec, ta, tb, s);
+  return launch_one<BN, true, true, true>(a, cs, c_vec, ta, tb, s);
+}
+
 }  // namespace gemmf
 
 cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool mmi, int chunk_k, cudaStream_t s,
@@ -472,15 +509,9 @@ cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool
   CUtensorMap ta{}, tb{};
   cudaError_t e = make_maps(a, &ta, &tb);
   if (e != cudaSuccess) return e;
-  if (!mmi) {
-    *kernel_name = "gemm_tc05_pair_f16ops_a8w8";
-    return launch_one<false, false, false>(a, cs, c_vec, ta, tb, s);
-  }
-  *kernel_name = "gemm_tc05_pair_f16ops_matmul_integer";
-  if (!a_u8 && !b_u8) return launch_one<false, false, true>(a, cs, c_vec, ta, tb, s);
-  if (a_u8 && !b_u8) return launch_one<true, false, true>(a, cs, c_vec, ta, tb, s);
-  if (!a_u8 && b_u8) return launch_one<false, true, true>(a, cs, c_vec, ta, tb, s);
-  return launch_one<true, true, true>(a, cs, c_vec, ta, tb, s);
+  *kernel_name = mmi ? "gemm_tc05_pair_f16ops_matmul_integer" : "gemm_tc05_pair_f16ops_a8w8";
+  if (choose_tile_width(a) == 224) return dispatch<224>(a, a_u8, b_u8, mmi, cs, c_vec, ta, tb, s);
+  return dispatch<256>(a, a_u8, b_u8, mmi, cs, c_vec, ta, tb, s);
 }
 
 }  // namespace qmm
