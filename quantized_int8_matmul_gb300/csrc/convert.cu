@@ -33,6 +33,131 @@ __device__ __forceinline__ int dp4a_sum(uint32_t w, int acc) {
   return __dp4a((int)w, 0x01010101, acc);
 }
 
+// ---------------------------------------------------------------------------
+// A and B together, no sums, staged through shared memory by bulk copies: each
+// CTA (one per SM) walks 16 KB input blocks of the concatenation [A | B]; one
+// thread copies a block in with cp.async.bulk (completion counted on an
+// mbarrier), all threads convert it to a 32 KB fp16 block in shared memory, and
+// one thread copies that out with cp.async.bulk. Three blocks are in flight per
+// SM, which keeps HBM busy without per-thread loads.
+constexpr int kBlkIn = 16384;
+constexpr int kBlkOut = 2 * kBlkIn;
+constexpr int kBulkStages = 3;
+constexpr int kBulkThreads = 256;
+constexpr size_t kBulkSmem = (size_t)kBulkStages * (kBlkIn + kBlkOut) + 1024;
+enum : unsigned { SITE_BULK_FULL = 0x500 };
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+// Block `blk` of the concatenation: source, destination and byte count.
+struct BulkBlock {
+  const uint8_t* src;
+  __half* dst;
+  uint32_t bytes;
+  bool second;
+};
+__device__ __forceinline__ BulkBlock bulk_block(long long blk, const uint8_t* A, __half* A16, long long a_bytes,
+                                                long long a_blocks, const uint8_t* B, __half* B16, long long b_bytes) {
+  BulkBlock r;
+  const bool sec = blk >= a_blocks;
+  const long long off = (sec ? blk - a_blocks : blk) * kBlkIn;
+  const long long total = sec ? b_bytes : a_bytes;
+  r.src = (sec ? B : A) + off;
+  r.dst = (sec ? B16 : A16) + off;
+  r.bytes = (uint32_t)min((long long)kBlkIn, total - off);
+  r.second = sec;
+  return r;
+}
+
+template <bool UA, bool UB>
+__global__ void __launch_bounds__(kBulkThreads, 1)
+    convert_bulk_kernel(const uint8_t* __restrict__ A, __half* __restrict__ A16, long long a_bytes,
+                        const uint8_t* __restrict__ B, __half* __restrict__ B16, long long b_bytes, unsigned* err) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ uint64_t full[kBulkStages];
+  __shared__ int abort_flag;
+  const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+  const uint32_t in0 = base, out0 = base + kBulkStages * kBlkIn;
+  const int t = threadIdx.x;
+  const long long a_blocks = (a_bytes + kBlkIn - 1) / kBlkIn;
+  const long long nblocks = a_blocks + (b_bytes + kBlkIn - 1) / kBlkIn;
+  const long long my = (blockIdx.x < nblocks) ? (nblocks - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  if (t == 0) {
+    for (int i = 0; i < kBulkStages; ++i) mbar_init(&full[i], 1);
+    abort_flag = 0;
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  auto issue_load = [&](long long i) {
+    const int s = (int)(i % kBulkStages);
+    const BulkBlock b = bulk_block(blockIdx.x + i * gridDim.x, A, A16, a_bytes, a_blocks, B, B16, b_bytes);
+    mbar_arrive_expect_tx(&full[s], b.bytes);
+    bulk_load(in0 + (uint32_t)s * kBlkIn, b.src, b.bytes, &full[s]);
+  };
+  if (t == 0)
+    for (long long i = 0; i < my && i < kBulkStages; ++i) issue_load(i);
+  for (long long i = 0; i < my; ++i) {
+    const int s = (int)(i % kBulkStages);
+    const BulkBlock b = bulk_block(blockIdx.x + i * gridDim.x, A, A16, a_bytes, a_blocks, B, B16, b_bytes);
+    const bool ok = mbar_wait(&full[s], (uint32_t)((i / kBulkStages) & 1), &abort_flag, err, SITE_BULK_FULL);
+    // the output buffer of this stage was last stored kBulkStages blocks ago
+    if (t == 0) bulk_wait_read<kBulkStages - 1>();
+    __syncthreads();
+    if (ok) {
+      const uint32_t src = in0 + (uint32_t)s * kBlkIn, dst = out0 + (uint32_t)s * kBlkOut;
+      // 8 input bytes per thread and step: conflict-free 8-byte loads and 16-byte stores
+#pragma unroll 4
+      for (uint32_t o = (uint32_t)t * 8u; o < b.bytes; o += kBulkThreads * 8u) {
+        const uint2 v = ld_shared_v2(src + o);
+        uint32_t h[4];
+        if (b.second) {
+          bytes_to_half4<UB>(v.x, h[0], h[1]);
+          bytes_to_half4<UB>(v.y, h[2], h[3]);
+        } else {
+          bytes_to_half4<UA>(v.x, h[0], h[1]);
+          bytes_to_half4<UA>(v.y, h[2], h[3]);
+        }
+        st_shared_v4(dst + 2u * o, h[0], h[1], h[2], h[3]);
+      }
+    }
+    fence_proxy_async_smem();
+    __syncthreads();
+    if (t == 0) {
+      if (ok) {
+        bulk_store(b.dst, out0 + (uint32_t)s * kBlkOut, 2u * b.bytes);
+        bulk_commit();
+      }
+      if (i + kBulkStages < my) issue_load(i + kBulkStages);
+    }
+  }
+  if (t == 0) {
+    bulk_wait_all();
+    // a load issued but not consumed (only after an abort) must land before exit
+    for (long long i = (my > kBulkStages ? my - kBulkStages : 0); i < my; ++i)
+      mbar_wait(&full[i % kBulkStages], (uint32_t)((i / kBulkStages) & 1), nullptr, err, SITE_BULK_FULL);
+  }
+}
+
 // A and B together, no sums: 16-byte chunks [0, nA) of A then [0, nB) of B,
 // grid-stride with four chunks (four loads) in flight per thread.
 template <bool UA, bool UB>
@@ -190,6 +315,40 @@ cudaError_t launch_convert_flat(const void* A, bool au, __half* A16, long long a
   else if (bu) convert_flat_kernel<false, true><<<grid, 256, 0, s>>>(a, A16, nA, b, B16, nB);
   else convert_flat_kernel<false, false><<<grid, 256, 0, s>>>(a, A16, nA, b, B16, nB);
   return cudaGetLastError();
+}
+
+namespace conv {
+// Launch one instantiation; the dynamic shared-memory opt-in is recorded per
+// instantiation and device.
+template <bool UA, bool UB>
+cudaError_t launch_bulk(int grid, const uint8_t* a, __half* A16, long long a_bytes, const uint8_t* b, __half* B16,
+                        long long b_bytes, unsigned* err, cudaStream_t s) {
+  static unsigned attr_dev_mask = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 32 || !(attr_dev_mask & (1u << dev))) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(convert_bulk_kernel<UA, UB>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kBulkSmem);
+    if (e != cudaSuccess) return e;
+    if (dev < 32) attr_dev_mask |= 1u << dev;
+  }
+  convert_bulk_kernel<UA, UB><<<grid, kBulkThreads, kBulkSmem, s>>>(a, A16, a_bytes, b, B16, b_bytes, err);
+  return cudaGetLastError();
+}
+}  // namespace conv
+
+cudaError_t launch_convert_bulk(const void* A, bool au, __half* A16, long long a_bytes, const void* B, bool bu,
+                                __half* B16, long long b_bytes, unsigned* err, cudaStream_t s) {
+  using namespace conv;
+  if (a_bytes + b_bytes <= 0) return cudaSuccess;
+  const long long nblocks = (a_bytes + kBlkIn - 1) / kBlkIn + (b_bytes + kBlkIn - 1) / kBlkIn;
+  const int grid = (int)std::max<long long>(1, std::min<long long>(nblocks, (long long)num_sms()));
+  const uint8_t* a = static_cast<const uint8_t*>(A);
+  const uint8_t* b = static_cast<const uint8_t*>(B);
+  if (au && bu) return launch_bulk<true, true>(grid, a, A16, a_bytes, b, B16, b_bytes, err, s);
+  if (au) return launch_bulk<true, false>(grid, a, A16, a_bytes, b, B16, b_bytes, err, s);
+  if (bu) return launch_bulk<false, true>(grid, a, A16, a_bytes, b, B16, b_bytes, err, s);
+  return launch_bulk<false, false>(grid, a, A16, a_bytes, b, B16, b_bytes, err, s);
 }
 
 cudaError_t launch_convert_cols(const void* src, bool u8, __half* dst, int mats, int rows, int cols, int* colsum,

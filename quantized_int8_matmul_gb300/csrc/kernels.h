@@ -66,6 +66,10 @@ cudaError_t launch_convert_rows(const void* src, bool u8, __half* dst, long long
                                 cudaStream_t s);
 cudaError_t launch_convert_cols(const void* src, bool u8, __half* dst, int mats, int rows, int cols, int* colsum,
                                 cudaStream_t s);
+// Both operands without sums in one launch, staged through shared memory by
+// bulk asynchronous copies (byte counts multiples of 16, 16-byte aligned).
+cudaError_t launch_convert_bulk(const void* A, bool au, __half* A16, long long a_bytes, const void* B, bool bu,
+                                __half* B16, long long b_bytes, unsigned* err, cudaStream_t s);
 // Both operands without sums in one launch (byte counts multiples of 16).
 cudaError_t launch_convert_flat(const void* A, bool au, __half* A16, long long a_bytes, const void* B, bool bu,
                                 __half* B16, long long b_bytes, cudaStream_t s);

@@ -122,8 +122,8 @@ cudaError_t run_pack(const PrepassPlan& pl, const void* A, bool au, const void* 
   __half* b16 = reinterpret_cast<__half*>(base + pl.off_b);
   int* rs = reinterpret_cast<int*>(base + pl.off_rs);
   int* cs = reinterpret_cast<int*>(base + pl.off_cs);
-  if (!need_rs && !need_cs)   // one launch for both operands
-    return launch_convert_flat(A, au, a16, pl.rowsA * K, B, bu, b16, pl.matsB * K * N, s);
+  if (!need_rs && !need_cs)   // one launch for both operands, staged by bulk copies
+    return launch_convert_bulk(A, au, a16, pl.rowsA * K, B, bu, b16, pl.matsB * K * N, err_word(), s);
   cudaError_t e = need_rs ? launch_convert_rows(A, au, a16, pl.rowsA, K, rs, s)
                           : launch_convert_flat(A, au, a16, pl.rowsA * K, nullptr, bu, nullptr, 0, s);
   if (e != cudaSuccess) return e;
