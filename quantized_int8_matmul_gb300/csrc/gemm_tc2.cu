@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
     for (int i = 0; i < NI; ++i) {
       mbar_init(&sm.i8_full[i], 1);
-      mbar_init(&sm.i8_empty[i], NW);
+      mbar_init(&sm.i8_empty[i], NWW);
     }
     for (int i = 0; i < SUM_RING; ++i) {
       mbar_init(&sm.cs_full[i], 2 * BNH);
@@ -507,8 +507,10 @@ __global__ void __launch_bounds__(NT, 1)
       store_stage<AU, BU>(sbase + (uint32_t)slot * STAGE_BYTES, so, cur);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0) mbar_arrive_remote_cta(full_leader0 + (uint32_t)slot * 8u);
-      mbar_arrive(&sm.i8_empty[is]);   // int8 bytes consumed: TMA may refill the slot
+      if (lane == 0) {
+        mbar_arrive_remote_cta(full_leader0 + (uint32_t)slot * 8u);
+        mbar_arrive(&sm.i8_empty[is]);   // the warp's int8 bytes are consumed: TMA may refill the slot
+      }
 
       if (st_s == 0) {
         const TileCoord tc = tile_coord(p, st_tl, cid, ncl, (int)rank);
