@@ -463,6 +463,22 @@ def case_setups(q, torch, peaks):
         return (lambda: q.matmul_integer(Ab, Bb, a_zero_point=za, b_zero_point=zb, out=Cb, workspace=wsb)), False, \
             report
 
+    def w8_prefill():
+        g = W.decode_gemv(4096)   # A bf16 [4096, 8192], W int8 [8192, 28672], per-column scale
+        Ad = torch.from_numpy(g.A_bits.view(np.int16)).view(torch.bfloat16).cuda()
+        Wd = torch.from_numpy(g.W).cuda()
+        sd = torch.from_numpy(g.scale).cuda()
+        Cd = torch.empty((4096, 28672), dtype=torch.bfloat16, device="cuda")
+        wsp = torch.empty(q.qmm_w8_dequant_workspace_bytes(torch.bfloat16, 4096, 8192, 28672), dtype=torch.uint8,
+                          device="cuda")
+        ops = 2.0 * 4096 * 8192 * 28672
+
+        def report(ms):
+            tops = ops / (ms * 1e-3) / 1e12
+            return {"us": ms * 1e3, "value": tops, "unit": "TOPS", "bound": "tensor", "frac": tops / tc,
+                    "note": "bf16 x int8 weight (weight pre-pass to bf16 + SM-pair GEMM), fp32 accumulation"}
+        return (lambda: q.qmm_w8_dequant(Ad, Wd, sd, None, out=Cd, workspace=wsp)), False, report
+
     def w8():
         sw = W.w8_dequant_f32_64x256x192()
         As, Bs = torch.from_numpy(sw.A).cuda(), torch.from_numpy(sw.B).cuda()
@@ -473,6 +489,7 @@ def case_setups(q, torch, peaks):
 
     return {"a8w8_4096x4096x4096_bf16": a8w8,
             "a8w8_4096x4096x4096_bf16_single_pass": a8w8_single_pass,
+            "w8_prefill_bf16_4096x8192x28672": w8_prefill,
             "decode_gemv_M1": gemv(1), "decode_gemv_M4": gemv(4), "decode_gemv_M16": gemv(16),
             "dql_8192x4096": dql, "matmul_integer_8192x4096x11008": mmi,
             "batched_matmul_integer_65536x1024x1024": batched, "w8_dequant_f32_64x256x192": w8}
@@ -480,7 +497,7 @@ def case_setups(q, torch, peaks):
 
 SECONDARY = ["a8w8_4096x4096x4096_bf16_single_pass", "decode_gemv_M1", "decode_gemv_M4", "decode_gemv_M16", "dql_8192x4096",
              "matmul_integer_8192x4096x11008", "batched_matmul_integer_65536x1024x1024",
-             "w8_dequant_f32_64x256x192"]
+             "w8_prefill_bf16_4096x8192x28672", "w8_dequant_f32_64x256x192"]
 
 
 def secondary(q, torch, flush, clocks, peaks):

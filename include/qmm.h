@@ -85,6 +85,27 @@ qmm_status qmm_w8_dequant(const void* A, int a_dtype, const int8_t* B, int64_t M
                           void* C, int c_dtype, void* stream);
 
 /*
+ * qmm_w8_dequant_ws: the same operation, for large M (prefill) on the
+ * tensor cores when a workspace is supplied. A pre-pass writes the int8
+ * weight as exact bf16 into the workspace once (and the activations' row sums
+ * when there is a zero point); an SM-pair GEMM (tcgen05 cta_group::2) then
+ * multiplies bf16 activations by it with one fp32 accumulation over K and
+ * applies scale_n * (acc - zp_n * rowsum(A)[m]) in its epilogue. fp32
+ * activations are split into two bf16 parts (hi + lo, about 2^-16 relative)
+ * along a doubled K that rereads the weight. Same accuracy bound as above.
+ *
+ *  workspace   at least qmm_w8_dequant_workspace_bytes(a_dtype, M, K, N) bytes,
+ *              16-byte aligned, caller-owned.
+ * The size function returns 0 when the path does not apply (M < 64, K or N
+ * not a multiple of 16); the call then runs qmm_w8_dequant and ignores the
+ * workspace. The same happens for an unaligned A (bf16: 16 bytes) or B.
+ */
+size_t qmm_w8_dequant_workspace_bytes(int a_dtype, int64_t M, int64_t K, int64_t N);
+qmm_status qmm_w8_dequant_ws(const void* A, int a_dtype, const int8_t* B, int64_t M, int64_t K, int64_t N,
+                             const float* scale, int64_t scale_count, const int32_t* zero_point, int64_t zp_count,
+                             void* C, int c_dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Form (b): A8W8 matmul-dequant. PyPTO PR #1920, "Feature/a8w8 matmul dequant
  * fusion", the walkthrough's sequence diagram (INT8 matmul into an INT32
  * accumulator, cast to FP32, act_scale on rows, weight_scale on columns, cast

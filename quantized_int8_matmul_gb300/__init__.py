@@ -47,6 +47,9 @@ def _load() -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     i64, vp, ci = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
     lib.qmm_w8_dequant.argtypes = [vp, ci, vp, i64, i64, i64, vp, i64, vp, i64, vp, ci, vp]
+    lib.qmm_w8_dequant_workspace_bytes.argtypes = [ci, i64, i64, i64]
+    lib.qmm_w8_dequant_workspace_bytes.restype = ctypes.c_size_t
+    lib.qmm_w8_dequant_ws.argtypes = [vp, ci, vp, i64, i64, i64, vp, i64, vp, i64, vp, ci, vp, ctypes.c_size_t, vp]
     lib.qmm_a8w8.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, i64, vp, ci, vp]
     lib.matmul_integer.argtypes = [vp, ci, vp, ci, i64, i64, i64, i64, i64, i64, vp, i64, vp, i64, vp, vp]
     sz = ctypes.c_size_t
@@ -61,7 +64,7 @@ def _load() -> ctypes.CDLL:
     lib.dynamic_quantize_linear_workspace_bytes.argtypes = [i64]
     lib.dynamic_quantize_linear_workspace_bytes.restype = ctypes.c_size_t
     lib.dynamic_quantize_linear.argtypes = [vp, i64, vp, vp, vp, vp, i64, vp, ctypes.c_size_t, vp]
-    for fn in ("qmm_w8_dequant", "qmm_a8w8", "qmm_a8w8_ws", "qmm_a8w8_pack", "qmm_a8w8_packed", "matmul_integer",
+    for fn in ("qmm_w8_dequant", "qmm_w8_dequant_ws", "qmm_a8w8", "qmm_a8w8_ws", "qmm_a8w8_pack", "qmm_a8w8_packed", "matmul_integer",
                "matmul_integer_ws", "dynamic_quantize_linear"):
         getattr(lib, fn).restype = ci
     lib.qmm_status_string.argtypes = [ci]
@@ -117,8 +120,17 @@ def check_device_error(stream=None) -> None:
     _check("qmm_check_device_error", _lib.qmm_check_device_error(_stream(stream)))
 
 
-def qmm_w8_dequant(A, B, scale, zero_point=None, out=None, out_dtype=torch.float32, stream=None):
-    """Form (a): C = scale_n * (A @ B - zp_n * rowsum(A)); A f32/bf16 [M,K], B int8 [K,N]."""
+def qmm_w8_dequant_workspace_bytes(a_dtype, M: int, K: int, N: int) -> int:
+    return int(_lib.qmm_w8_dequant_workspace_bytes(_TORCH_TO_QMM[a_dtype], M, K, N))
+
+
+def qmm_w8_dequant(A, B, scale, zero_point=None, out=None, out_dtype=torch.float32, stream=None, workspace="auto"):
+    """Form (a): C = scale_n * (A @ B - zp_n * rowsum(A)); A f32/bf16 [M,K], B int8 [K,N].
+
+    workspace: "auto" (default) or a device tensor of at least
+    qmm_w8_dequant_workspace_bytes(A.dtype, M, K, N) bytes runs large M on the
+    SM-pair tensor-core GEMM (bf16 weight copy in the workspace) where it
+    applies; None keeps the GEMV / CUDA-core kernels."""
     _need(A, (torch.float32, torch.bfloat16), "A")
     _need(B, (torch.int8,), "B")
     _need(scale, (torch.float32,), "scale")
@@ -133,9 +145,16 @@ def qmm_w8_dequant(A, B, scale, zero_point=None, out=None, out_dtype=torch.float
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=A.device)
     _need(out, (torch.float32, torch.bfloat16), "out")
-    st = _lib.qmm_w8_dequant(_ptr(A), _TORCH_TO_QMM[A.dtype], _ptr(B), M, K, N, _ptr(scale), scale.numel(),
-                             _ptr(zero_point), zp_count, _ptr(out), _TORCH_TO_QMM[out.dtype], _stream(stream))
-    _check("qmm_w8_dequant", st)
+    ws, wsb = _workspace(workspace, qmm_w8_dequant_workspace_bytes(A.dtype, M, K, N), A.device)
+    if ws is None:
+        st = _lib.qmm_w8_dequant(_ptr(A), _TORCH_TO_QMM[A.dtype], _ptr(B), M, K, N, _ptr(scale), scale.numel(),
+                                 _ptr(zero_point), zp_count, _ptr(out), _TORCH_TO_QMM[out.dtype], _stream(stream))
+        _check("qmm_w8_dequant", st)
+    else:
+        st = _lib.qmm_w8_dequant_ws(_ptr(A), _TORCH_TO_QMM[A.dtype], _ptr(B), M, K, N, _ptr(scale), scale.numel(),
+                                    _ptr(zero_point), zp_count, _ptr(out), _TORCH_TO_QMM[out.dtype], _ptr(ws), wsb,
+                                    _stream(stream))
+        _check("qmm_w8_dequant_ws", st)
     return out
 
 

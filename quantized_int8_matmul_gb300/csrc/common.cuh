@@ -159,6 +159,11 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn_maj
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// The same for bf16 A and B (format 1 in both fields).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return idesc_f16_f32(M, N, a_mn_major, b_mn_major) | (1u << 7) | (1u << 10);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle. Addresses in bytes.
 // Bits: [0,14) start>>4; [16,30) leading-dimension byte offset>>4;
 // [32,46) stride-dimension byte offset>>4; [46,48) version (1);

@@ -343,4 +343,126 @@ cudaError_t launch_convert_cols(const void* src, bool u8, __half* dst, int mats,
   return cudaGetLastError();
 }
 
+
+// ---------------------------------------------------------------------------
+// Form (a) pre-pass: the int8 weight as exact bf16, and the activations' row
+// sums (the zero-point correction of TrainDeeploy PR #53, "The kernel") or,
+// for fp32 activations, a split into two bf16 parts.
+// ---------------------------------------------------------------------------
+namespace conv {
+
+// Four int8 (bytes of w) -> four exact bf16, as two bf16x2 words: the byte,
+// biased to unsigned, sits in the low mantissa bits of 2^23 (fp32 0x4B000000),
+// the bias is subtracted in fp32 (exact), and the top halves of the fp32 words
+// are the bf16 values (integers of magnitude <= 256 have at most 8 significant
+// bits, so dropping the low half loses nothing).
+__device__ __forceinline__ void s8_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = w ^ 0x80808080u;
+  float f[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) f[i] = __uint_as_float(0x4B000000u | ((u >> (8 * i)) & 0xFFu)) - 8388736.0f;
+  lo = prmt(__float_as_uint(f[0]), __float_as_uint(f[1]), 0x7632u);
+  hi = prmt(__float_as_uint(f[2]), __float_as_uint(f[3]), 0x7632u);
+}
+
+__global__ void __launch_bounds__(256) convert_s8_bf16_kernel(const uint8_t* __restrict__ src,
+                                                              uint32_t* __restrict__ dst, long long n16) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += 4 * stride) {
+    uint4 v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      if (i + j * stride < n16) v[j] = ldg_nc_v4(src + 16 * (i + j * stride));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const long long c = i + j * stride;
+      if (c >= n16) break;
+      uint32_t h[8];
+      s8_to_bf16x4(v[j].x, h[0], h[1]);
+      s8_to_bf16x4(v[j].y, h[2], h[3]);
+      s8_to_bf16x4(v[j].z, h[4], h[5]);
+      s8_to_bf16x4(v[j].w, h[6], h[7]);
+      st_global_v4(dst + 8 * c, h[0], h[1], h[2], h[3]);
+      st_global_v4(dst + 8 * c + 4, h[4], h[5], h[6], h[7]);
+    }
+  }
+}
+
+// fp32 row sums of bf16 rows (one warp per row).
+__global__ void __launch_bounds__(256) rowsum_bf16_kernel(const uint16_t* __restrict__ A, long long rows, int K,
+                                                          float* __restrict__ rowsum) {
+  const int lane = threadIdx.x & 31;
+  const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long r = warp0; r < rows; r += nwarps) {
+    const uint16_t* a = A + r * K;
+    float acc = 0.f;
+    for (int k = lane * 8; k < K; k += 256) {   // 16-byte loads (K % 8 == 0)
+      const uint4 v = ldg_nc_v4(a + k);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc += __uint_as_float(w[i] << 16) + __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) rowsum[r] = acc;
+  }
+}
+
+// fp32 rows [M][K] -> bf16 [M][2*Kp]: the first Kp columns hold hi = RN_bf16(a),
+// the next Kp columns lo = RN_bf16(a - hi) (zero padded from K to Kp, a multiple
+// of 64), so that hi + lo equals a to about 2^-16 relative; with rowsum, the fp32
+// row sums of a (one warp per row).
+__global__ void __launch_bounds__(256) split_f32_kernel(const float* __restrict__ A, long long rows, int K, int Kp,
+                                                        uint16_t* __restrict__ out, float* __restrict__ rowsum) {
+  const int lane = threadIdx.x & 31;
+  const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long r = warp0; r < rows; r += nwarps) {
+    const float* a = A + r * K;
+    uint16_t* hi = out + r * 2 * (long long)Kp;
+    uint16_t* lo = hi + Kp;
+    float acc = 0.f;
+    for (int k = lane; k < Kp; k += 32) {
+      const float x = k < K ? __ldg(a + k) : 0.f;
+      const __nv_bfloat16 h = __float2bfloat16_rn(x);
+      const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
+      hi[k] = *reinterpret_cast<const uint16_t*>(&h);
+      lo[k] = *reinterpret_cast<const uint16_t*>(&l);
+      acc += x;
+    }
+    if (rowsum) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (lane == 0) rowsum[r] = acc;
+    }
+  }
+}
+
+}  // namespace conv
+
+cudaError_t launch_convert_s8_bf16(const void* src, void* dst, long long bytes, cudaStream_t s) {
+  using namespace conv;
+  const long long n16 = bytes / 16;
+  if (n16 <= 0) return cudaSuccess;
+  convert_s8_bf16_kernel<<<grid_for((n16 + 3) / 4, 256), 256, 0, s>>>(static_cast<const uint8_t*>(src),
+                                                                       static_cast<uint32_t*>(dst), n16);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rowsum_bf16(const void* A, long long rows, int K, float* rowsum, cudaStream_t s) {
+  using namespace conv;
+  if (rows <= 0) return cudaSuccess;
+  rowsum_bf16_kernel<<<grid_for(rows * 32, 256), 256, 0, s>>>(static_cast<const uint16_t*>(A), rows, K, rowsum);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_split_f32(const float* A, long long rows, int K, int Kp, void* out, float* rowsum,
+                             cudaStream_t s) {
+  using namespace conv;
+  if (rows <= 0) return cudaSuccess;
+  split_f32_kernel<<<grid_for(rows * 32, 256), 256, 0, s>>>(A, rows, K, Kp, static_cast<uint16_t*>(out), rowsum);
+  return cudaGetLastError();
+}
+
 }  // namespace qmm

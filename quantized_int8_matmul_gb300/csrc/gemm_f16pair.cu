@@ -109,7 +109,7 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
 
 // Per-tile operands of this warp's CPW columns, staged in shared memory by
 // the warp itself.
-template <int CPW, bool BU, bool MMI>
+template <int CPW, bool BU, bool MMI, bool FA>
 __device__ __forceinline__ void stage_columns(const GemmF16Args& p, Shared& sm, const TileCoord tc, int warp, int h,
                                               int lane) {
   const int* colsum = (MMI && p.a_zp_count > 0) ? p.colsum + (p.b_bstride ? (size_t)tc.b * p.N : 0) : nullptr;
@@ -118,7 +118,10 @@ __device__ __forceinline__ void stage_columns(const GemmF16Args& p, Shared& sm, 
     uint32_t op = 0u;
     int cs = 0;
     if (n < p.N) {
-      if (!MMI) {
+      if (FA) {
+        op = __float_as_uint(__ldg(p.w_scale + (p.w_count == 1 ? 0 : n)));
+        if (p.b_zp_count > 0) cs = __ldg((const int*)p.b_zp + (p.b_zp_count == 1 ? 0 : n));
+      } else if (!MMI) {
         op = __float_as_uint(__ldg(p.w_scale + (p.w_count == 1 ? 0 : n)));
       } else {
         if (p.b_zp_count > 0) {
@@ -137,7 +140,7 @@ __device__ __forceinline__ void stage_columns(const GemmF16Args& p, Shared& sm, 
 // Epilogue of one tile from the int32 sums in registers (this thread: one row,
 // this warp's CPW columns): dequantise (A8W8) or apply the zero-point
 // expansion (MatMulInteger), store C.
-template <int CPW, bool AU, bool BU, bool MMI>
+template <int CPW, bool AU, bool BU, bool MMI, bool FA>
 __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm, uint32_t (&sums)[CPW],
                                          const TileCoord tc, int warp, int q, int h, int lane, int c_vec) {
   const int row = tc.m0 + q * 32 + lane;
@@ -147,6 +150,49 @@ __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm,
   const int mz = row % p.zp_row_mod;
   float as = 0.f;
   uint32_t za = 0u, rs = 0u;
+  if (FA) {
+    // form (a): scale_n * (sum_k a*w - zp_n * sum_k a), in fp32
+    const float rsum = p.b_zp_count > 0 ? __ldg(reinterpret_cast<const float*>(p.rowsum) + row) : 0.f;
+#pragma unroll
+    for (int g = 0; g < CPW / 16; ++g) {
+      const int nb = tc.n0 + h * CPW + g * 16;
+      if (nb >= p.N) break;
+      const bool full = (nb + 16 <= p.N) && c_vec;
+      uint32_t* o = &sums[g * 16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float zp = (float)sm.col_sum[warp][g * 16 + i];
+        const float v = __fmaf_rn(-zp, rsum, __uint_as_float(o[i]));
+        o[i] = __float_as_uint(__fmul_rn(v, __uint_as_float(sm.col_op[warp][g * 16 + i])));
+      }
+      if (p.c_f32) {
+        float* out = reinterpret_cast<float*>(p.C) + crow + nb;
+        if (full) {
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) st_global_v4_hint(out + i, o[i], o[i + 1], o[i + 2], o[i + 3], pol);
+        } else {
+          for (int i = 0; i < 16; ++i)
+            if (nb + i < p.N) out[i] = __uint_as_float(o[i]);
+        }
+      } else {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C) + crow + nb;
+        uint32_t pk[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(o[2 * i]), __uint_as_float(o[2 * i + 1]));
+          pk[i] = *reinterpret_cast<uint32_t*>(&b2);
+        }
+        if (full) {
+          st_global_v4_hint(out, pk[0], pk[1], pk[2], pk[3], pol);
+          st_global_v4_hint(out + 8, pk[4], pk[5], pk[6], pk[7], pol);
+        } else {
+          for (int i = 0; i < 16; ++i)
+            if (nb + i < p.N) out[i] = __float2bfloat16_rn(__uint_as_float(o[i]));
+        }
+      }
+    }
+    return;
+  }
   if (!MMI) {
     as = __ldg(p.act_scale + (p.act_count == 1 ? 0 : mz));
   } else {
@@ -214,7 +260,7 @@ __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm,
   }
 }
 
-template <int BN, bool AU, bool BU, bool MMI>
+template <int BN, bool AU, bool BU, bool MMI, bool FA>
 __global__ void __launch_bounds__(NT, 1)
     gemm_f16pair_kernel(const GemmF16Args p, const int cs, const int c_vec, const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB) {
@@ -268,7 +314,7 @@ __global__ void __launch_bounds__(NT, 1)
   if (warp == NEW) {
     // ---------------- pair MMA issuer (even CTA) ----------------
     if (rank == 0 && lane == 0) {
-      const uint32_t idesc = idesc_f16_f32(BMP, BN, false, true);
+      const uint32_t idesc = FA ? idesc_bf16_f32(BMP, BN, false, true) : idesc_f16_f32(BMP, BN, false, true);
       int g = 0, d = 0;
       bool ok = true;
       for (int tl = 0; tl < my_tiles && ok; ++tl) {
@@ -326,8 +372,9 @@ __global__ void __launch_bounds__(NT, 1)
         const int ab = p.a_bstride ? tc.b : 0, bb = p.b_bstride ? tc.b : 0;
         const int nc = tc.n0 + (int)rank * BNH;
         tma_load_3d_pair(dst, &tmA, s * BK, tc.m0, ab, bar);
-        tma_load_3d_pair(dst + A_BYTES, &tmB, nc, s * BK, bb, bar);
-        tma_load_3d_pair(dst + A_BYTES + B_BOX, &tmB, nc + 64, s * BK, bb, bar);
+        const int kb = (FA && p.fa_kwrap) ? (s * BK) % p.fa_kwrap : s * BK;   // [hi | lo] halves reread W
+        tma_load_3d_pair(dst + A_BYTES, &tmB, nc, kb, bb, bar);
+        tma_load_3d_pair(dst + A_BYTES + B_BOX, &tmB, nc + 64, kb, bb, bar);
         if (++s == spt) {
           s = 0;
           tc = tile_coord<BN>(p, ++tl, cid, ncl, (int)rank);
@@ -349,7 +396,7 @@ __global__ void __launch_bounds__(NT, 1)
     uint32_t sums[CPW];
     int tl = 0, c = 0;
     TileCoord tc = tile_coord<BN>(p, 0, cid, ncl, (int)rank);
-    if (my_tiles > 0) stage_columns<CPW, BU, MMI>(p, sm, tc, warp, h, lane);
+    if (my_tiles > 0) stage_columns<CPW, BU, MMI, FA>(p, sm, tc, warp, h, lane);
     for (int d = 0; d < total_chunks; ++d) {
       const int ab = d & 1;
       if (!mbar_wait_cluster(&sm.acc_full[ab], (uint32_t)((d >> 1) & 1), &sm.abort_flag, p.err, SITE_ACC_FULL))
@@ -363,18 +410,22 @@ __global__ void __launch_bounds__(NT, 1)
         tmem_ld16(t_acc + g * 16, acc);
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const uint32_t v = (uint32_t)__float2int_rn(__uint_as_float(acc[i]));
-          sums[g * 16 + i] = (c == 0) ? v : sums[g * 16 + i] + v;
+          if (FA) {   // form (a): one fp32 accumulation over all of K; the launcher makes it one chunk
+            sums[g * 16 + i] = acc[i];
+          } else {
+            const uint32_t v = (uint32_t)__float2int_rn(__uint_as_float(acc[i]));
+            sums[g * 16 + i] = (c == 0) ? v : sums[g * 16 + i] + v;
+          }
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_remote_cta(acc_empty_leader0 + (uint32_t)ab * 8u);
       if (c == cpt - 1) {
-        epilogue<CPW, AU, BU, MMI>(p, sm, sums, tc, warp, q, h, lane, c_vec);
+        epilogue<CPW, AU, BU, MMI, FA>(p, sm, sums, tc, warp, q, h, lane, c_vec);
         __syncwarp();   // the warp's staged operands are read: restage for the next tile
         if (tl + 1 < my_tiles)
-          stage_columns<CPW, BU, MMI>(p, sm, tile_coord<BN>(p, tl + 1, cid, ncl, (int)rank), warp, h, lane);
+          stage_columns<CPW, BU, MMI, FA>(p, sm, tile_coord<BN>(p, tl + 1, cid, ncl, (int)rank), warp, h, lane);
       }
       if (++c == cpt) {
         c = 0;
@@ -409,10 +460,10 @@ struct DeviceLaunchInfo {
   int max_clusters = 0;
 };
 
-template <int BN, bool AU, bool BU, bool MMI>
+template <int BN, bool AU, bool BU, bool MMI, bool FA = false>
 cudaError_t launch_one(const GemmF16Args& a, int cs, int c_vec, const CUtensorMap& ta, const CUtensorMap& tb,
                        cudaStream_t s) {
-  auto kern = gemm_f16pair_kernel<BN, AU, BU, MMI>;
+  auto kern = gemm_f16pair_kernel<BN, AU, BU, MMI, FA>;
   static std::mutex mu;
   static DeviceLaunchInfo info[64];
   int dev = 0;
@@ -512,6 +563,25 @@ cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool
   *kernel_name = mmi ? "gemm_tc05_pair_f16ops_matmul_integer" : "gemm_tc05_pair_f16ops_a8w8";
   if (choose_tile_width(a) == 224) return dispatch<224>(a, a_u8, b_u8, mmi, cs, c_vec, ta, tb, s);
   return dispatch<256>(a, a_u8, b_u8, mmi, cs, c_vec, ta, tb, s);
+}
+
+cudaError_t launch_gemm_w8_bf16pair(const GemmF16Args& a, int w_k, cudaStream_t s, const char** kernel_name) {
+  using namespace gemmf;
+  const int cs = (a.K + BK - 1) / BK;   // one chunk: fp32 accumulation over all of K
+  const int celem = a.c_f32 ? 4 : 2;
+  const int c_vec = ((reinterpret_cast<uintptr_t>(a.C) % 16) == 0) && (((long long)a.N * celem) % 16 == 0);
+  // A: {K_eff, M} with K_eff = a.K; W: {N, w_k} (its true K rows: coordinates
+  // past them, in the padding of split activations, read as zeros)
+  CUtensorMap ta{}, tb{};
+  GemmF16Args wa = a;
+  wa.K = w_k;
+  cudaError_t e = make_maps(a, &ta, &tb);
+  CUtensorMap unused{};
+  if (e == cudaSuccess) e = make_maps(wa, &unused, &tb);
+  if (e != cudaSuccess) return e;
+  *kernel_name = "gemm_tc05_pair_w8_bf16";
+  if (choose_tile_width(a) == 224) return launch_one<224, false, false, false, true>(a, cs, c_vec, ta, tb, s);
+  return launch_one<256, false, false, false, true>(a, cs, c_vec, ta, tb, s);
 }
 
 }  // namespace qmm

@@ -52,13 +52,29 @@ struct GemmF16Args {
   const float* w_scale;    int w_count;
   const void* a_zp;        int a_zp_count;
   const void* b_zp;        int b_zp_count;
-  const int* rowsum;       // MatMulInteger with b_zp: rowsum(A), [batch or 1][M]
+  const int* rowsum;       // MatMulInteger with b_zp: rowsum(A), [batch or 1][M]; form (a): fp32 row sums
   const int* colsum;       // MatMulInteger with a_zp: colsum(B), [batch or 1][N]
   int zp_row_mod;
   unsigned* err;
+  // form (a) (bf16 A x bf16 copy of the int8 weight, fp32 accumulation): the
+  // weight's K coordinate wraps at fa_kwrap when A holds [hi | lo] halves of
+  // fp32 activations (0: no wrap); scale = w_scale/w_count, zp = b_zp (int32)
+  int fa_kwrap;
 };
 cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool mmi, int chunk_k, cudaStream_t s,
                                 const char** kernel_name);
+// Form (a) on the same engine: C = scale[n] * (A @ W - zp[n] * rowsum(A)[m]),
+// A bf16 [M][K_eff] (K_eff = a.K: the weight's w_k, or 2*Kp for split fp32
+// activations), W the bf16 copy [w_k][N]; one fp32 accumulation over K_eff.
+cudaError_t launch_gemm_w8_bf16pair(const GemmF16Args& a, int w_k, cudaStream_t s, const char** kernel_name);
+
+// Form (a) pre-pass: int8 -> exact bf16 (byte counts multiples of 16); fp32 row
+// sums of bf16 rows (K % 8 == 0); fp32 rows -> [hi | lo] bf16 halves of width
+// Kp each (optional fp32 row sums).
+cudaError_t launch_convert_s8_bf16(const void* src, void* dst, long long bytes, cudaStream_t s);
+cudaError_t launch_rowsum_bf16(const void* A, long long rows, int K, float* rowsum, cudaStream_t s);
+cudaError_t launch_split_f32(const float* A, long long rows, int K, int Kp, void* out, float* rowsum,
+                             cudaStream_t s);
 
 // Pre-pass: 8-bit rows -> exact fp16 (one warp per row; optional row sums), and
 // 8-bit [mats][rows][cols] -> fp16 with column sums (colsum zeroed here).

@@ -150,6 +150,29 @@ const char* kTwoPassA8W8 = "f16_prepass+gemm_tc05_pair_f16ops_a8w8";
 const char* kTwoPassMMI = "f16_prepass+gemm_tc05_pair_f16ops_matmul_integer";
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) % 16) == 0; }
+
+// Form (a) for large M on the SM-pair GEMM: the int8 weight converted once to
+// exact bf16 in a workspace, the activations' row sums (for a zero point), and
+// for fp32 activations their [hi | lo] bf16 split. Workspace:
+// [W16: K*N bf16][rowsum: M fp32][A': M*2*Kp bf16 (fp32 activations only)].
+struct W8Plan {
+  bool use = false;
+  int Kp = 0;
+  size_t off_rs = 0, off_a = 0, bytes = 0;
+};
+constexpr int64_t kW8PrefillMinM = 64;
+
+W8Plan w8_plan(int a_dtype, int64_t M, int64_t K, int64_t N) {
+  W8Plan pl;
+  if (M < kW8PrefillMinM || K <= 0 || K % 16 != 0 || N % 16 != 0) return pl;
+  if (a_dtype != QMM_F32 && a_dtype != QMM_BF16) return pl;
+  pl.Kp = (int)((K + 63) / 64 * 64);
+  pl.off_rs = round256((size_t)K * N * 2);
+  pl.off_a = pl.off_rs + round256((size_t)M * 4);
+  pl.bytes = pl.off_a + (a_dtype == QMM_F32 ? round256((size_t)M * 2 * pl.Kp * 2) : 0);
+  pl.use = true;
+  return pl;
+}
 }  // namespace
 
 int num_sms() {
@@ -257,6 +280,63 @@ qmm_status qmm_w8_dequant(const void* A, int a_dtype, const int8_t* B, int64_t M
   w.C = C;
   w.c_f32 = c_dtype == QMM_F32;
   return finish_launch(launch_w8_simt(w, s, &name), name);
+}
+
+size_t qmm_w8_dequant_workspace_bytes(int a_dtype, int64_t M, int64_t K, int64_t N) {
+  if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return 0;
+  const W8Plan pl = w8_plan(a_dtype, M, K, N);
+  return pl.use ? pl.bytes : 0;
+}
+
+qmm_status qmm_w8_dequant_ws(const void* A, int a_dtype, const int8_t* B, int64_t M, int64_t K, int64_t N,
+                             const float* scale, int64_t scale_count, const int32_t* zero_point, int64_t zp_count,
+                             void* C, int c_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  const W8Plan pl = (dim_ok(M) && dim_ok(K) && dim_ok(N)) ? w8_plan(a_dtype, M, K, N) : W8Plan{};
+  const bool a_ok = a_dtype == QMM_F32 ? (reinterpret_cast<uintptr_t>(A) % 4) == 0 : aligned16(A);
+  if (!pl.use || N == 0 || !a_ok || !aligned16(B))
+    return qmm_w8_dequant(A, a_dtype, B, M, K, N, scale, scale_count, zero_point, zp_count, C, c_dtype, stream);
+  if (c_dtype != QMM_F32 && c_dtype != QMM_BF16) return QMM_ERR_INVALID_ARG;
+  if (scale_count != 1 && scale_count != N) return QMM_ERR_INVALID_ARG;
+  if (zp_count != 0 && zp_count != 1 && zp_count != N) return QMM_ERR_INVALID_ARG;
+  if (!scale || !C || !A || !B || (zp_count > 0 && !zero_point)) return QMM_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < pl.bytes) return QMM_ERR_INVALID_ARG;
+  unsigned* err = err_word();
+  if (!err) return QMM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  float* rowsum = zp_count > 0 ? reinterpret_cast<float*>(base + pl.off_rs) : nullptr;
+  cudaError_t e = launch_convert_s8_bf16(B, base, K * N, s);
+  GemmF16Args f{};
+  f.batch = 1;
+  f.M = (int)M;
+  f.N = (int)N;
+  f.B16 = base;
+  if (e == cudaSuccess) {
+    if (a_dtype == QMM_F32) {
+      e = launch_split_f32(static_cast<const float*>(A), M, (int)K, pl.Kp, base + pl.off_a, rowsum, s);
+      f.A16 = base + pl.off_a;
+      f.K = 2 * pl.Kp;
+      f.fa_kwrap = pl.Kp;
+    } else {
+      if (rowsum) e = launch_rowsum_bf16(A, M, (int)K, rowsum, s);
+      f.A16 = A;
+      f.K = (int)K;
+      f.fa_kwrap = 0;
+    }
+  }
+  f.C = C;
+  f.c_f32 = c_dtype == QMM_F32;
+  f.w_scale = scale;
+  f.w_count = (int)scale_count;
+  f.b_zp = zero_point;
+  f.b_zp_count = (int)zp_count;
+  f.rowsum = reinterpret_cast<const int*>(rowsum);
+  f.zp_row_mod = (int)M;
+  f.err = err;
+  const char* name = "none";
+  if (e == cudaSuccess) e = launch_gemm_w8_bf16pair(f, (int)K, s, &name);
+  return finish_launch(e, "w8_bf16_prepass+gemm_tc05_pair_w8_bf16");
 }
 
 qmm_status qmm_a8w8(const int8_t* A, const int8_t* B, int64_t M, int64_t K, int64_t N, const float* act_scale,

@@ -18,10 +18,14 @@ def sample(n, k, seed):
     return np.sort(np.random.default_rng(seed).choice(n, size=k, replace=False))
 
 
-def test_w8_dequant_f32_64x256x192():
+@pytest.mark.parametrize("workspace,kernel", [("auto", "w8_bf16_prepass+gemm_tc05_pair_w8_bf16"),
+                                              (None, "w8_dequant_simt")])
+def test_w8_dequant_f32_64x256x192(workspace, kernel):
     w = W.w8_dequant_f32_64x256x192()
-    C = q.qmm_w8_dequant(dev(w.A), dev(w.B), dev(w.scale), dev(w.zero_point), out_dtype=torch.float32)
-    assert q.last_kernel() == "w8_dequant_simt"
+    C = q.qmm_w8_dequant(dev(w.A), dev(w.B), dev(w.scale), dev(w.zero_point), out_dtype=torch.float32,
+                         workspace=workspace)
+    q.check_device_error()
+    assert q.last_kernel() == kernel
     exact = O.w8_dequant(w.A, w.B, w.scale, w.zero_point)
     bound = O.w8_dequant_error_bound(w.A, w.B, w.scale, w.zero_point)
     assert_within(host(C).astype(np.float64), exact, bound, 23, "w8 64x256x192")

@@ -15,7 +15,7 @@ q = pytest.importorskip("quantized_int8_matmul_gb300")
 
 def check(A_dev, A_vals, B, scale, zp, out, kernel):
     zp_dev = None if zp is None else dev(zp.astype(np.int32))
-    C = q.qmm_w8_dequant(A_dev, dev(B), dev(scale), zp_dev, out_dtype=out)
+    C = q.qmm_w8_dequant(A_dev, dev(B), dev(scale), zp_dev, out_dtype=out, workspace=None)
     torch.cuda.synchronize()
     assert q.last_kernel() == kernel
     got = host(C)
