@@ -170,6 +170,35 @@ def a8w8(A: np.ndarray, B: np.ndarray, act_scale, weight_scale, out: str = "f32"
     raise ValueError(out)
 
 
+def a8w8_dequant_acc(acc_in, A: np.ndarray, B: np.ndarray, act_scale, weight_scale, out: str = "f32"):
+    """The accumulating A8W8 variant: the int32 accumulator is acc_in plus the
+    exact int32 product, wrapping, then the same float32 steps as a8w8.
+
+    [P2] names tensor.a8w8_matmul_dequant_acc (an INT32 accumulator input
+    beside the INT8 operands, lowered through tile.matmul_acc / tile.gemv_acc
+    then the cast and the two scale multiplies) without spelling out its
+    arithmetic; this is the plainest reading: matmul_acc adds the product to
+    the accumulator it is given. acc_in is an int32 [M,N] array (or 0).
+    Returns what a8w8 returns for the combined accumulator."""
+    prod = a8w8_acc(A, B)
+    acc = wrap_int32(np.asarray(acc_in, dtype=np.int64) + prod.astype(np.int64))
+    return _a8w8_epilogue(acc, act_scale, weight_scale, out)
+
+
+def _a8w8_epilogue(acc: np.ndarray, act_scale, weight_scale, out: str):
+    M, N = acc.shape
+    a_s = _as_vector(act_scale, M, "act_scale").astype(np.float32)
+    w_s = _as_vector(weight_scale, N, "weight_scale").astype(np.float32)
+    f = acc.astype(np.float32)                 # int32 -> fp32, nearest even
+    f = (f * a_s[:, None]).astype(np.float32)  # rows first
+    f = (f * w_s[None, :]).astype(np.float32)  # then columns
+    if out == "f32":
+        return f
+    if out == "bf16":
+        return f32_to_bf16_bits(f)
+    raise ValueError(out)
+
+
 def a8w8_exact(A: np.ndarray, B: np.ndarray, act_scale, weight_scale) -> np.ndarray:
     """float64 value of act_scale[m] * weight_scale[n] * acc[m,n] (no float32 steps)."""
     acc = a8w8_acc(A, B).astype(np.float64)

@@ -371,3 +371,55 @@ def test_row_and_col_sums_bruteforce():
     B = rng.integers(-128, 128, (9, 5)).astype(np.int8)
     cs = O.col_sums(B)
     assert cs.tolist() == [sum(int(B[k, n]) for k in range(9)) for n in range(5)]
+
+
+# ---------------------------------------------------------------------------
+# The accumulating A8W8 variant
+# ---------------------------------------------------------------------------
+
+def test_a8w8_dequant_acc_with_zero_accumulator_is_a8w8():
+    rng = np.random.default_rng(41)
+    A = rng.integers(-128, 128, (7, 33)).astype(np.int8)
+    B = rng.integers(-128, 128, (33, 5)).astype(np.int8)
+    a_s = rng.uniform(0.01, 0.02, 7).astype(np.float32)
+    w_s = rng.uniform(0.001, 0.01, 5).astype(np.float32)
+    for out in ("f32", "bf16"):
+        assert np.array_equal(O.a8w8_dequant_acc(np.zeros((7, 5), np.int32), A, B, a_s, w_s, out),
+                              O.a8w8(A, B, a_s, w_s, out))
+
+
+def test_a8w8_dequant_acc_chains_a_split_of_k():
+    """Linearity of the sum over K: the product of the first K columns/rows,
+    handed over as the accumulator of the second, gives the whole product."""
+    rng = np.random.default_rng(42)
+    A = rng.integers(-128, 128, (6, 40)).astype(np.int8)
+    B = rng.integers(-128, 128, (40, 9)).astype(np.int8)
+    a_s = rng.uniform(0.01, 0.02, 6).astype(np.float32)
+    w_s = rng.uniform(0.001, 0.01, 9).astype(np.float32)
+    for k1 in (1, 16, 39):
+        first = O.a8w8_acc(A[:, :k1], B[:k1])
+        got = O.a8w8_dequant_acc(first, A[:, k1:], B[k1:], a_s, w_s, "f32")
+        assert np.array_equal(got, O.a8w8(A, B, a_s, w_s, "f32")), k1
+
+
+def test_a8w8_dequant_acc_brute_force_with_wrap():
+    """Python-int brute force, struct-rounded float32 steps; accumulators near
+    the int32 limits so the sum wraps."""
+    rng = np.random.default_rng(43)
+    M, K, N = 3, 4, 2
+    A = rng.integers(-128, 128, (M, K)).astype(np.int8)
+    B = rng.integers(-128, 128, (K, N)).astype(np.int8)
+    acc = np.array([[2**31 - 5, -2**31 + 3], [7, -9], [2**31 - 1, -2**31]], np.int32)
+    a_s = np.array([0.5, 0.25, 3.0], np.float32)
+    w_s = np.array([0.125, 2.0], np.float32)
+    got = O.a8w8_dequant_acc(acc, A, B, a_s, w_s, "f32")
+
+    def f32(x):
+        return struct.unpack("f", struct.pack("f", x))[0]
+
+    for m in range(M):
+        for n in range(N):
+            s = int(acc[m, n]) + sum(int(A[m, k]) * int(B[k, n]) for k in range(K))
+            s = (s + 2**31) % 2**32 - 2**31
+            v = f32(f32(f32(float(s)) * float(a_s[m])) * float(w_s[n]))
+            assert got[m, n] == np.float32(v), (m, n)
