@@ -168,6 +168,41 @@ qmm_status qmm_a8w8_packed(int64_t M, int64_t K, int64_t N, const float* act_sca
                            size_t workspace_bytes, void* stream);
 
 /*
+ * Accumulating A8W8. PyPTO PR #1920, "What Changed", "A8W8 matmul-dequant-acc
+ * op" (an INT32 accumulator input beside the INT8 operands, [M] or [M,1]
+ * activation scales, [N] or [1,N] weight scales, FP32 or BF16 output, a_trans /
+ * b_trans dimension inference), lowered there to matmul_acc (gemv_acc for
+ * M == 1), the cast and the two scale multiplies:
+ *     acc = acc_in[m,n] + sum_k A[m,k]*B[k,n]   (exact, int32, wrapping)
+ *     C   = out( ((float)acc * act_scale[m]) * weight_scale[n] )
+ * the float steps exactly those of qmm_a8w8 (which this equals for acc_in 0).
+ *
+ *  A          int8, [M,K] row-major, or [K,M] when a_trans = 1
+ *  B          int8, [K,N] row-major, or [N,K] when b_trans = 1
+ *  acc_in     device int32 [M,N] row-major, or NULL (zero)
+ *  acc_out    device int32 [M,N] or NULL: receives acc (before any scaling),
+ *             e.g. to pass a partial sum over part of K to the next call;
+ *             may be the same array as acc_in (each element is read before
+ *             it is written), may not overlap it otherwise
+ *  act_scale, act_count, weight_scale, w_count, C, c_dtype   as in qmm_a8w8;
+ *             C may be NULL when acc_out is given (then only acc_out is
+ *             written and the scales are not read)
+ *  workspace  at least qmm_a8w8_acc_workspace_bytes(M, K, N) bytes, 16-byte
+ *             aligned, caller-owned (NULL allowed when that size is 0)
+ * Any M, K, N >= 0 and any alignment of A, B. Kernels: a pre-pass writes
+ * exact fp16 copies of A and B (transposing a transposed operand, rows padded
+ * to 16 bytes), then the SM-pair tensor-core GEMM with the accumulator and the
+ * scaling in its epilogue. K = 0 passes acc_in through (one elementwise kernel).
+ * Errors: QMM_ERR_INVALID_ARG for a bad flag, count, null pointer or too small
+ * a workspace, and when both C and acc_out are NULL.
+ */
+size_t qmm_a8w8_acc_workspace_bytes(int64_t M, int64_t K, int64_t N);
+qmm_status qmm_a8w8_acc(const int8_t* A, int a_trans, const int8_t* B, int b_trans, int64_t M, int64_t K, int64_t N,
+                        const int32_t* acc_in, int32_t* acc_out, const float* act_scale, int64_t act_count,
+                        const float* weight_scale, int64_t w_count, void* C, int c_dtype, void* workspace,
+                        size_t workspace_bytes, void* stream);
+
+/*
  * Form (c): MatMulInteger with zero points. ROCm hip-ep PR #1248,
  * "feat(onnx-to-hip): lower quantized integer conv and matmul", section
  * "What", MatMulInteger paragraph:

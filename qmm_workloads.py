@@ -101,6 +101,31 @@ def a8w8_4096(seed: int = 0) -> A8W8:
 
 
 @dataclass
+class A8W8Acc:
+    A: np.ndarray             # i8, stored [M, K], or [K, M] when a_trans
+    B: np.ndarray             # i8, stored [K, N], or [N, K] when b_trans
+    acc_in: np.ndarray        # i32 [M, N]
+    act_scale: np.ndarray     # f32 [M]
+    weight_scale: np.ndarray  # f32 [N]
+    a_trans: bool
+    b_trans: bool
+
+
+def a8w8_acc(M: int, K: int, N: int, seed: int = 0, a_trans: bool = False, b_trans: bool = False,
+             acc_bound: int = 2**24) -> A8W8Acc:
+    """The accumulating A8W8's inputs: the A8W8 operand recipe, stored in the
+    given layouts, and an int32 accumulator uniform in [-acc_bound, acc_bound)
+    (a partial sum carried in from an earlier part of K; 2**31 spans int32)."""
+    w = a8w8(M, K, N, seed)
+    rng = rng_for(seed + 1)
+    acc = rng.integers(-acc_bound, acc_bound, size=(M, N), dtype=np.int64).astype(np.int32)
+    A = np.ascontiguousarray(w.A.T) if a_trans else w.A
+    B = np.ascontiguousarray(w.B.T) if b_trans else w.B
+    return A8W8Acc(A=A, B=B, acc_in=acc, act_scale=w.act_scale, weight_scale=w.weight_scale, a_trans=a_trans,
+                   b_trans=b_trans)
+
+
+@dataclass
 class DqlMatMulInteger:
     x: np.ndarray      # f32 [M, K]
     B: np.ndarray      # i8 [K, N]

@@ -56,6 +56,9 @@ def _load() -> ctypes.CDLL:
     lib.qmm_a8w8_workspace_bytes.argtypes = [i64, i64, i64]
     lib.qmm_a8w8_workspace_bytes.restype = sz
     lib.qmm_a8w8_ws.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, i64, vp, ci, vp, sz, vp]
+    lib.qmm_a8w8_acc_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.qmm_a8w8_acc_workspace_bytes.restype = sz
+    lib.qmm_a8w8_acc.argtypes = [vp, ci, vp, ci, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, ci, vp, sz, vp]
     lib.qmm_a8w8_pack.argtypes = [vp, vp, i64, i64, i64, vp, sz, vp]
     lib.qmm_a8w8_packed.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, ci, vp, sz, vp]
     lib.matmul_integer_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64]
@@ -234,6 +237,50 @@ def qmm_a8w8_packed(M, K, N, act_scale, weight_scale, workspace, out=None, out_d
     return out
 
 
+def qmm_a8w8_acc_workspace_bytes(M: int, K: int, N: int) -> int:
+    return int(_lib.qmm_a8w8_acc_workspace_bytes(M, K, N))
+
+
+def qmm_a8w8_acc(A, B, act_scale=None, weight_scale=None, acc_in=None, acc_out=None, a_trans=False, b_trans=False,
+                 out=None, out_dtype=torch.bfloat16, stream=None, workspace="auto"):
+    """Accumulating A8W8: acc = acc_in + A @ B (int32, wrapping), then
+    C = out(f32(acc) * act_scale[m] * weight_scale[n]).
+
+    A is [M, K] ([K, M] with a_trans), B is [K, N] ([N, K] with b_trans), both
+    int8; acc_in / acc_out optional int32 [M, N] (acc_out receives acc and may
+    be acc_in). out_dtype None (and no out) writes only acc_out and returns None."""
+    _need(A, (torch.int8,), "A")
+    _need(B, (torch.int8,), "B")
+    if A.dim() != 2 or B.dim() != 2:
+        raise ValueError("A and B must be 2-D")
+    K, M = A.shape if a_trans else A.shape[::-1]
+    N, K2 = B.shape if b_trans else B.shape[::-1]
+    if K2 != K:
+        raise ValueError("inner dimensions differ")
+    for t, name in ((acc_in, "acc_in"), (acc_out, "acc_out")):
+        if t is not None:
+            _need(t, (torch.int32,), name)
+            if tuple(t.shape) != (M, N):
+                raise ValueError(f"{name} must be [{M}, {N}]")
+    if out is None and out_dtype is not None:
+        out = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    if out is not None:
+        _need(out, (torch.float32, torch.bfloat16), "out")
+        _need(act_scale, (torch.float32,), "act_scale")
+        _need(weight_scale, (torch.float32,), "weight_scale")
+    elif acc_out is None:
+        raise ValueError("nothing to write: give out_dtype/out or acc_out")
+    ws, wsb = _workspace(workspace, qmm_a8w8_acc_workspace_bytes(M, K, N), A.device)
+    st = _lib.qmm_a8w8_acc(_ptr(A), int(bool(a_trans)), _ptr(B), int(bool(b_trans)), M, K, N, _ptr(acc_in),
+                           _ptr(acc_out), _ptr(act_scale) if out is not None else None,
+                           act_scale.numel() if out is not None else 0,
+                           _ptr(weight_scale) if out is not None else None,
+                           weight_scale.numel() if out is not None else 0, _ptr(out),
+                           _TORCH_TO_QMM[out.dtype] if out is not None else 0, _ptr(ws), wsb, _stream(stream))
+    _check("qmm_a8w8_acc", st)
+    return out
+
+
 def matmul_integer(A, B, a_zero_point=None, b_zero_point=None, out=None, stream=None, workspace="auto"):
     """Form (c): int32 C = (A - a_zp) @ (B - b_zp), A [...,M,K], B [K,N] (shared) or [...,K,N].
 
@@ -330,7 +377,7 @@ def num_sms() -> int:
 
 
 __all__ = [
-    "qmm_w8_dequant", "qmm_a8w8", "matmul_integer", "dynamic_quantize_linear",
+    "qmm_w8_dequant", "qmm_a8w8", "qmm_a8w8_acc", "matmul_integer", "dynamic_quantize_linear",
     "dynamic_quantize_linear_workspace_bytes", "last_kernel", "check_device_error", "QmmError", "lib",
     "num_sms", "LIB_PATH",
 ]

@@ -10,6 +10,7 @@
 #include "kernels.h"
 
 #include <algorithm>
+#include <climits>
 
 namespace qmm {
 namespace conv {
@@ -340,6 +341,133 @@ cudaError_t launch_convert_cols(const void* src, bool u8, __half* dst, int mats,
   const uint8_t* p = static_cast<const uint8_t*>(src);
   if (u8) convert_cols_kernel<true><<<grid, 256, 0, s>>>(p, dst, mats, rows, cols, colsum);
   else convert_cols_kernel<false><<<grid, 256, 0, s>>>(p, dst, mats, rows, cols, colsum);
+  return cudaGetLastError();
+}
+
+
+// ---------------------------------------------------------------------------
+// General planes: operands at any pitch, stored as they are or transposed
+// (PyPTO PR #1920's a_trans / b_trans: A held as [K][M], B as [N][K]), become
+// fp16 [rows][K] and [K][cols] copies whose rows are padded to 16 bytes. One
+// CTA per 64 x 64 source tile; each thread reads one 16-byte chunk of a source
+// row. A copy converts the chunk and writes it out; a transpose passes the tile
+// through shared memory and each thread writes 16 values of one destination
+// row.
+// ---------------------------------------------------------------------------
+namespace conv {
+
+constexpr int kPT = 64;
+
+// Bytes [c, c+16) of source row r; zero where outside the plane. vec: the
+// plane's base and pitch are 16-byte multiples (c is one already).
+__device__ __forceinline__ uint4 load_chunk(const uint8_t* src, long long pitch, int rows, int cols, int r, int c,
+                                            bool vec) {
+  if (r >= rows || c >= cols) return make_uint4(0u, 0u, 0u, 0u);
+  const uint8_t* p = src + (long long)r * pitch + c;
+  if (vec && c + 16 <= cols) return ldg_nc_v4(p);
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+  for (int i = 0; i < 16 && c + i < cols; ++i) w[i >> 2] |= (uint32_t)__ldg(p + i) << (8 * (i & 3));
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// The first n (<= 16) of 16 fp16 values (h: pairs, element 0 in the low half)
+// to d; a full chunk is two 16-byte stores (d is then 16-byte aligned).
+__device__ __forceinline__ void store_halves(__half* d, const uint32_t (&h)[8], int n) {
+  if (n == 16) {
+    st_global_v4(d, h[0], h[1], h[2], h[3]);
+    st_global_v4(d + 8, h[4], h[5], h[6], h[7]);
+    return;
+  }
+  for (int i = 0; i < n; ++i) d[i] = __ushort_as_half((unsigned short)(h[i >> 1] >> (16 * (i & 1))));
+}
+
+template <bool U>
+__device__ __forceinline__ void plane_tile(const ConvPlane& p, long long tile, uint8_t (*st)[kPT + 4]) {
+  const int ct = (p.cols + kPT - 1) / kPT;
+  const int r0 = (int)(tile / ct) * kPT, c0 = (int)(tile % ct) * kPT;
+  const int t = threadIdx.x;
+  const uint8_t* src = static_cast<const uint8_t*>(p.src);
+  const bool vec = ((reinterpret_cast<uintptr_t>(src) | (uintptr_t)p.src_pitch) & 15u) == 0;
+  const int lr = t >> 2, lc = (t & 3) * 16;
+  const uint4 v = load_chunk(src, p.src_pitch, p.rows, p.cols, r0 + lr, c0 + lc, vec);
+  uint32_t h[8];
+  if (!p.trans) {
+    if (r0 + lr < p.rows && c0 + lc < p.cols) {
+      convert16<U>(v, h);
+      store_halves(p.dst + (long long)(r0 + lr) * p.dst_pitch + c0 + lc, h, min(16, p.cols - c0 - lc));
+    }
+    return;
+  }
+  uint32_t* row = reinterpret_cast<uint32_t*>(&st[lr][lc]);
+  row[0] = v.x;
+  row[1] = v.y;
+  row[2] = v.z;
+  row[3] = v.w;
+  __syncthreads();
+  // destination row c0 + cc (a source column), values from source rows r0 + rg ..
+  const int cc = t & 63, rg = (t >> 6) * 16;
+  if (c0 + cc >= p.cols || r0 + rg >= p.rows) return;
+  uint32_t w[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    w[j] = (uint32_t)st[rg + 4 * j][cc] | ((uint32_t)st[rg + 4 * j + 1][cc] << 8) |
+           ((uint32_t)st[rg + 4 * j + 2][cc] << 16) | ((uint32_t)st[rg + 4 * j + 3][cc] << 24);
+  convert16<U>(make_uint4(w[0], w[1], w[2], w[3]), h);
+  store_halves(p.dst + (long long)(c0 + cc) * p.dst_pitch + r0 + rg, h, min(16, p.rows - r0 - rg));
+}
+
+template <bool UA, bool UB>
+__global__ void __launch_bounds__(256) convert_planes_kernel(const ConvPlane a, const ConvPlane b, long long tiles_a) {
+  __shared__ uint8_t st[kPT][kPT + 4];
+  if ((long long)blockIdx.x < tiles_a) plane_tile<UA>(a, (long long)blockIdx.x, st);
+  else plane_tile<UB>(b, (long long)blockIdx.x - tiles_a, st);
+}
+
+long long plane_tiles(const ConvPlane& p) {
+  if (p.rows <= 0 || p.cols <= 0) return 0;
+  return (long long)((p.rows + kPT - 1) / kPT) * ((p.cols + kPT - 1) / kPT);
+}
+
+// acc = acc_in (or 0) at every output; acc_out and the scaled C from it.
+__global__ void __launch_bounds__(256) acc_only_kernel(const int* __restrict__ acc_in, int* __restrict__ acc_out,
+                                                       int M, int N, const float* __restrict__ as, int ac,
+                                                       const float* __restrict__ ws, int wc, void* C, int c_f32) {
+  const long long total = (long long)M * N;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const int acc = acc_in ? __ldg(acc_in + i) : 0;
+    if (acc_out) acc_out[i] = acc;
+    if (!C) continue;
+    const int m = (int)(i / N), n = (int)(i - (long long)m * N);
+    float v = __int2float_rn(acc);
+    v = __fmul_rn(v, __ldg(as + (ac == 1 ? 0 : m)));
+    v = __fmul_rn(v, __ldg(ws + (wc == 1 ? 0 : n)));
+    if (c_f32) static_cast<float*>(C)[i] = v;
+    else static_cast<__nv_bfloat16*>(C)[i] = __float2bfloat16_rn(v);
+  }
+}
+
+}  // namespace conv
+
+cudaError_t launch_convert_planes(const ConvPlane& a, bool au, const ConvPlane& b, bool bu, cudaStream_t s) {
+  using namespace conv;
+  const long long ta = plane_tiles(a), tb = plane_tiles(b);
+  if (ta + tb == 0) return cudaSuccess;
+  if (ta + tb > INT_MAX) return cudaErrorInvalidValue;
+  const int grid = (int)(ta + tb);
+  if (au && bu) convert_planes_kernel<true, true><<<grid, 256, 0, s>>>(a, b, ta);
+  else if (au) convert_planes_kernel<true, false><<<grid, 256, 0, s>>>(a, b, ta);
+  else if (bu) convert_planes_kernel<false, true><<<grid, 256, 0, s>>>(a, b, ta);
+  else convert_planes_kernel<false, false><<<grid, 256, 0, s>>>(a, b, ta);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_acc_only(const int* acc_in, int* acc_out, int M, int N, const float* act_scale, int act_count,
+                            const float* w_scale, int w_count, void* C, int c_f32, cudaStream_t s) {
+  using namespace conv;
+  if (M <= 0 || N <= 0) return cudaSuccess;
+  conv::acc_only_kernel<<<grid_for((long long)M * N, 256), 256, 0, s>>>(acc_in, acc_out, M, N, act_scale, act_count,
+                                                                        w_scale, w_count, C, c_f32);
   return cudaGetLastError();
 }
 

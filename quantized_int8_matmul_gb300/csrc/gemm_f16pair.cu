@@ -109,7 +109,7 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
 
 // Per-tile operands of this warp's CPW columns, staged in shared memory by
 // the warp itself.
-template <int CPW, bool BU, bool MMI, bool FA>
+template <int CPW, bool BU, bool MMI, bool FA, bool ACC = false>
 __device__ __forceinline__ void stage_columns(const GemmF16Args& p, Shared& sm, const TileCoord tc, int warp, int h,
                                               int lane) {
   const int* colsum = (MMI && p.a_zp_count > 0) ? p.colsum + (p.b_bstride ? (size_t)tc.b * p.N : 0) : nullptr;
@@ -122,7 +122,7 @@ __device__ __forceinline__ void stage_columns(const GemmF16Args& p, Shared& sm, 
         op = __float_as_uint(__ldg(p.w_scale + (p.w_count == 1 ? 0 : n)));
         if (p.b_zp_count > 0) cs = __ldg((const int*)p.b_zp + (p.b_zp_count == 1 ? 0 : n));
       } else if (!MMI) {
-        op = __float_as_uint(__ldg(p.w_scale + (p.w_count == 1 ? 0 : n)));
+        if (!ACC || p.C) op = __float_as_uint(__ldg(p.w_scale + (p.w_count == 1 ? 0 : n)));
       } else {
         if (p.b_zp_count > 0) {
           const int zi = p.b_zp_count == 1 ? 0 : n;
@@ -138,9 +138,11 @@ __device__ __forceinline__ void stage_columns(const GemmF16Args& p, Shared& sm, 
 }
 
 // Epilogue of one tile from the int32 sums in registers (this thread: one row,
-// this warp's CPW columns): dequantise (A8W8) or apply the zero-point
-// expansion (MatMulInteger), store C.
-template <int CPW, bool AU, bool BU, bool MMI, bool FA>
+// this warp's CPW columns): dequantise (A8W8; with ACC, first add acc_in and
+// store the combined int32 sums to acc_out) or apply the zero-point expansion
+// (MatMulInteger), store C. c_vec bit 0: C rows take 16-byte vectors; bit 1:
+// so do acc_in / acc_out rows.
+template <int CPW, bool AU, bool BU, bool MMI, bool FA, bool ACC = false>
 __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm, uint32_t (&sums)[CPW],
                                          const TileCoord tc, int warp, int q, int h, int lane, int c_vec) {
   const int row = tc.m0 + q * 32 + lane;
@@ -157,7 +159,7 @@ __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm,
     for (int g = 0; g < CPW / 16; ++g) {
       const int nb = tc.n0 + h * CPW + g * 16;
       if (nb >= p.N) break;
-      const bool full = (nb + 16 <= p.N) && c_vec;
+      const bool full = (nb + 16 <= p.N) && (c_vec & 1);
       uint32_t* o = &sums[g * 16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -194,7 +196,7 @@ __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm,
     return;
   }
   if (!MMI) {
-    as = __ldg(p.act_scale + (p.act_count == 1 ? 0 : mz));
+    if (!ACC || p.C) as = __ldg(p.act_scale + (p.act_count == 1 ? 0 : mz));
   } else {
     if (p.a_zp_count > 0) {
       const int zi = p.a_zp_count == 1 ? 0 : mz;
@@ -207,8 +209,38 @@ __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm,
   for (int g = 0; g < CPW / 16; ++g) {
     const int nb = tc.n0 + h * CPW + g * 16;
     if (nb >= p.N) break;
-    const bool full = (nb + 16 <= p.N) && c_vec;
+    const bool full = (nb + 16 <= p.N) && (c_vec & 1);
     uint32_t* o = &sums[g * 16];
+    if (ACC) {
+      const bool full_acc = (nb + 16 <= p.N) && (c_vec & 2);
+      if (p.acc_in) {   // the caller's int32 accumulator, added with wrap-around
+        const int* src = p.acc_in + crow + nb;
+        if (full_acc) {
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) {
+            const uint4 x = ldg_nc_v4(src + i);
+            o[i] += x.x;
+            o[i + 1] += x.y;
+            o[i + 2] += x.z;
+            o[i + 3] += x.w;
+          }
+        } else {
+          for (int i = 0; i < 16; ++i)
+            if (nb + i < p.N) o[i] += (uint32_t)__ldg(src + i);
+        }
+      }
+      if (p.acc_out) {
+        int* dst = p.acc_out + crow + nb;
+        if (full_acc) {
+#pragma unroll
+          for (int i = 0; i < 16; i += 4) st_global_v4_hint(dst + i, o[i], o[i + 1], o[i + 2], o[i + 3], pol);
+        } else {
+          for (int i = 0; i < 16; ++i)
+            if (nb + i < p.N) dst[i] = (int)o[i];
+        }
+      }
+      if (!p.C) continue;
+    }
     if (!MMI) {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -260,7 +292,7 @@ __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm,
   }
 }
 
-template <int BN, bool AU, bool BU, bool MMI, bool FA>
+template <int BN, bool AU, bool BU, bool MMI, bool FA, bool ACC>
 __global__ void __launch_bounds__(NT, 1)
     gemm_f16pair_kernel(const GemmF16Args p, const int cs, const int c_vec, const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB) {
@@ -396,7 +428,7 @@ __global__ void __launch_bounds__(NT, 1)
     uint32_t sums[CPW];
     int tl = 0, c = 0;
     TileCoord tc = tile_coord<BN>(p, 0, cid, ncl, (int)rank);
-    if (my_tiles > 0) stage_columns<CPW, BU, MMI, FA>(p, sm, tc, warp, h, lane);
+    if (my_tiles > 0) stage_columns<CPW, BU, MMI, FA, ACC>(p, sm, tc, warp, h, lane);
     for (int d = 0; d < total_chunks; ++d) {
       const int ab = d & 1;
       if (!mbar_wait_cluster(&sm.acc_full[ab], (uint32_t)((d >> 1) & 1), &sm.abort_flag, p.err, SITE_ACC_FULL))
@@ -422,10 +454,11 @@ __global__ void __launch_bounds__(NT, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_remote_cta(acc_empty_leader0 + (uint32_t)ab * 8u);
       if (c == cpt - 1) {
-        epilogue<CPW, AU, BU, MMI, FA>(p, sm, sums, tc, warp, q, h, lane, c_vec);
+        epilogue<CPW, AU, BU, MMI, FA, ACC>(p, sm, sums, tc, warp, q, h, lane, c_vec);
         __syncwarp();   // the warp's staged operands are read: restage for the next tile
         if (tl + 1 < my_tiles)
-          stage_columns<CPW, BU, MMI, FA>(p, sm, tile_coord<BN>(p, tl + 1, cid, ncl, (int)rank), warp, h, lane);
+          stage_columns<CPW, BU, MMI, FA, ACC>(p, sm, tile_coord<BN>(p, tl + 1, cid, ncl, (int)rank), warp, h,
+                                               lane);
       }
       if (++c == cpt) {
         c = 0;
@@ -460,10 +493,10 @@ struct DeviceLaunchInfo {
   int max_clusters = 0;
 };
 
-template <int BN, bool AU, bool BU, bool MMI, bool FA = false>
+template <int BN, bool AU, bool BU, bool MMI, bool FA = false, bool ACC = false>
 cudaError_t launch_one(const GemmF16Args& a, int cs, int c_vec, const CUtensorMap& ta, const CUtensorMap& tb,
                        cudaStream_t s) {
-  auto kern = gemm_f16pair_kernel<BN, AU, BU, MMI, FA>;
+  auto kern = gemm_f16pair_kernel<BN, AU, BU, MMI, FA, ACC>;
   static std::mutex mu;
   static DeviceLaunchInfo info[64];
   int dev = 0;
@@ -505,15 +538,18 @@ cudaError_t launch_one(const GemmF16Args& a, int cs, int c_vec, const CUtensorMa
 }
 
 // fp16 operand maps: A as {K, M, batch} (box 64 x 128), B as {N, K, batch}
-// (box 64 x 64), both with 128-byte swizzle.
+// (box 64 x 64), both with 128-byte swizzle; rows a_pitch / b_pitch elements
+// apart (the columns past K or N are never read: the copies there are zeros).
 cudaError_t make_maps(const GemmF16Args& a, CUtensorMap* ta, CUtensorMap* tb) {
   const uint64_t ab = a.a_bstride ? (uint64_t)a.batch : 1, bb = a.b_bstride ? (uint64_t)a.batch : 1;
-  const uint64_t as = 2ull * (a.a_bstride ? (uint64_t)a.a_bstride : (uint64_t)a.M * a.K);
-  const uint64_t bs = 2ull * (a.b_bstride ? (uint64_t)a.b_bstride : (uint64_t)a.K * a.N);
-  cudaError_t e = make_tmap_3d(ta, a.A16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)a.K, (uint64_t)a.M, ab,
-                               2ull * a.K, as, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  const uint64_t ap = a.a_pitch ? (uint64_t)a.a_pitch : (uint64_t)a.K;
+  const uint64_t bp = a.b_pitch ? (uint64_t)a.b_pitch : (uint64_t)a.N;
+  const uint64_t as = 2ull * (a.a_bstride ? (uint64_t)a.a_bstride : (uint64_t)a.M * ap);
+  const uint64_t bs = 2ull * (a.b_bstride ? (uint64_t)a.b_bstride : (uint64_t)a.K * bp);
+  cudaError_t e = make_tmap_3d(ta, a.A16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)a.K, (uint64_t)a.M, ab, 2ull * ap,
+                               as, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
   if (e != cudaSuccess) return e;
-  return make_tmap_3d(tb, a.B16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)a.N, (uint64_t)a.K, bb, 2ull * a.N, bs,
+  return make_tmap_3d(tb, a.B16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)a.N, (uint64_t)a.K, bb, 2ull * bp, bs,
                       64, BK, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
@@ -542,7 +578,12 @@ int choose_tile_width(const GemmF16Args& a) {
 template <int BN>
 cudaError_t dispatch(const GemmF16Args& a, bool a_u8, bool b_u8, bool mmi, int cs, int c_vec, const CUtensorMap& ta,
                      const CUtensorMap& tb, cudaStream_t s) {
-  if (!mmi) return launch_one<BN, false, false, false>(a, cs, c_vec, ta, tb, s);
+  if (!mmi) {
+    // the accumulator epilogue's extra loads fit the register budget at the
+    // 224-column width only (the 256-column one spills)
+    if (a.acc_in || a.acc_out || !a.C) return launch_one<224, false, false, false, false, true>(a, cs, c_vec, ta, tb, s);
+    return launch_one<BN, false, false, false>(a, cs, c_vec, ta, tb, s);
+  }
   if (!a_u8 && !b_u8) return launch_one<BN, false, false, true>(a, cs, c_vec, ta, tb, s);
   if (a_u8 && !b_u8) return launch_one<BN, true, false, true>(a, cs, c_vec, ta, tb, s);
   if (!a_u8 && b_u8) return launch_one<BN, false, true, true>(a, cs, c_vec, ta, tb, s);
@@ -556,11 +597,14 @@ cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool
   using namespace gemmf;
   const int cs = chunk_k / BK;
   const int celem = (mmi || a.c_f32) ? 4 : 2;
-  const int c_vec = ((reinterpret_cast<uintptr_t>(a.C) % 16) == 0) && (((long long)a.N * celem) % 16 == 0);
+  const bool acc_al = ((reinterpret_cast<uintptr_t>(a.acc_in) | reinterpret_cast<uintptr_t>(a.acc_out)) % 16) == 0;
+  const int c_vec = (((reinterpret_cast<uintptr_t>(a.C) % 16) == 0) && (((long long)a.N * celem) % 16 == 0) ? 1 : 0) |
+                    ((acc_al && a.N % 4 == 0) ? 2 : 0);
   CUtensorMap ta{}, tb{};
   cudaError_t e = make_maps(a, &ta, &tb);
   if (e != cudaSuccess) return e;
-  *kernel_name = mmi ? "gemm_tc05_pair_f16ops_matmul_integer" : "gemm_tc05_pair_f16ops_a8w8";
+  *kernel_name = mmi ? "gemm_tc05_pair_f16ops_matmul_integer"
+                     : ((a.acc_in || a.acc_out || !a.C) ? "gemm_tc05_pair_f16ops_a8w8_acc" : "gemm_tc05_pair_f16ops_a8w8");
   if (choose_tile_width(a) == 224) return dispatch<224>(a, a_u8, b_u8, mmi, cs, c_vec, ta, tb, s);
   return dispatch<256>(a, a_u8, b_u8, mmi, cs, c_vec, ta, tb, s);
 }

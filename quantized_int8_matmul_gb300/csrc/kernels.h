@@ -60,6 +60,14 @@ struct GemmF16Args {
   // weight's K coordinate wraps at fa_kwrap when A holds [hi | lo] halves of
   // fp32 activations (0: no wrap); scale = w_scale/w_count, zp = b_zp (int32)
   int fa_kwrap;
+  // row pitches of the fp16 copies in elements (0: dense, K for A and N for B;
+  // otherwise a multiple of 8, the operand padded on the right)
+  int a_pitch, b_pitch;
+  // accumulating A8W8: int32 [M][N] added to the exact product before the
+  // scaling (wrapping), and/or written with the combined sums; with C null only
+  // acc_out is written (act_scale / w_scale unused)
+  const int* acc_in;
+  int* acc_out;
 };
 cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool mmi, int chunk_k, cudaStream_t s,
                                 const char** kernel_name);
@@ -75,6 +83,24 @@ cudaError_t launch_convert_s8_bf16(const void* src, void* dst, long long bytes, 
 cudaError_t launch_rowsum_bf16(const void* A, long long rows, int K, float* rowsum, cudaStream_t s);
 cudaError_t launch_split_f32(const float* A, long long rows, int K, int Kp, void* out, float* rowsum,
                              cudaStream_t s);
+
+// General pre-pass plane: an 8-bit [rows][cols] matrix at a byte pitch, copied
+// (trans = 0: dst[r][c] = src[r][c]) or transposed (trans = 1: dst[c][r] =
+// src[r][c]) into exact fp16 at an element pitch that is a multiple of 8.
+struct ConvPlane {
+  const void* src;
+  long long src_pitch;     // bytes between source rows
+  int rows, cols;          // source extent
+  int trans;
+  __half* dst;
+  long long dst_pitch;     // fp16 elements between destination rows
+};
+// Both planes in one launch (a plane with rows or cols 0 is skipped).
+cudaError_t launch_convert_planes(const ConvPlane& a, bool au, const ConvPlane& b, bool bu, cudaStream_t s);
+// The accumulating A8W8 with an empty K: acc = acc_in (or 0); acc_out = acc,
+// C = out(f32(acc) * act_scale[m] * w_scale[n]) where C is given.
+cudaError_t launch_acc_only(const int* acc_in, int* acc_out, int M, int N, const float* act_scale, int act_count,
+                            const float* w_scale, int w_count, void* C, int c_f32, cudaStream_t s);
 
 // Pre-pass: 8-bit rows -> exact fp16 (one warp per row; optional row sums), and
 // 8-bit [mats][rows][cols] -> fp16 with column sums (colsum zeroed here).

@@ -173,6 +173,25 @@ W8Plan w8_plan(int a_dtype, int64_t M, int64_t K, int64_t N) {
   pl.use = true;
   return pl;
 }
+// Accumulating A8W8 (PyPTO PR #1920's tensor.a8w8_matmul_dequant_acc, with
+// its a_trans / b_trans): both operands converted, and transposed where they
+// are stored transposed, into fp16 copies whose rows are padded to 16 bytes;
+// then the SM-pair GEMM with the accumulator epilogue. Workspace:
+// [A16: M x Kp fp16][B16: K x Np fp16], Kp and Np rounded up to multiples of 8.
+struct AccPlan {
+  int64_t Kp = 0, Np = 0;
+  size_t off_b = 0, bytes = 0;
+};
+
+AccPlan acc_plan(int64_t M, int64_t K, int64_t N) {
+  AccPlan pl;
+  if (M <= 0 || K <= 0 || N <= 0) return pl;
+  pl.Kp = (K + 7) / 8 * 8;
+  pl.Np = (N + 7) / 8 * 8;
+  pl.off_b = round256((size_t)M * pl.Kp * 2);
+  pl.bytes = pl.off_b + round256((size_t)K * pl.Np * 2);
+  return pl;
+}
 }  // namespace
 
 int num_sms() {
@@ -571,6 +590,76 @@ qmm_status qmm_a8w8_packed(int64_t M, int64_t K, int64_t N, const float* act_sca
   f.err = err;
   return finish_launch(run_packed_gemm(pl, workspace, f, false, false, false, chunk_k_for(false, false), s),
                        kPackedA8W8);
+}
+
+size_t qmm_a8w8_acc_workspace_bytes(int64_t M, int64_t K, int64_t N) {
+  if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return 0;
+  return acc_plan(M, K, N).bytes;
+}
+
+qmm_status qmm_a8w8_acc(const int8_t* A, int a_trans, const int8_t* B, int b_trans, int64_t M, int64_t K, int64_t N,
+                        const int32_t* acc_in, int32_t* acc_out, const float* act_scale, int64_t act_count,
+                        const float* weight_scale, int64_t w_count, void* C, int c_dtype, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return QMM_ERR_INVALID_ARG;
+  if ((a_trans != 0 && a_trans != 1) || (b_trans != 0 && b_trans != 1)) return QMM_ERR_INVALID_ARG;
+  if (!C && !acc_out) return QMM_ERR_INVALID_ARG;
+  if (C) {
+    if (c_dtype != QMM_F32 && c_dtype != QMM_BF16) return QMM_ERR_INVALID_ARG;
+    if (act_count != 1 && act_count != M) return QMM_ERR_INVALID_ARG;
+    if (w_count != 1 && w_count != N) return QMM_ERR_INVALID_ARG;
+  }
+  if (M == 0 || N == 0) {
+    t_last_kernel = "none";
+    return QMM_OK;
+  }
+  if (C && (!act_scale || !weight_scale)) return QMM_ERR_INVALID_ARG;
+  if (K > 0 && (!A || !B)) return QMM_ERR_INVALID_ARG;
+  if (((M + 255) / 256) * ((N + 223) / 224) > (int64_t)INT_MAX) return QMM_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  const int c_f32 = C ? (c_dtype == QMM_F32) : 0;
+  if (K == 0)   // empty product: the accumulator passes through
+    return finish_launch(launch_acc_only(acc_in, acc_out, (int)M, (int)N, act_scale, (int)act_count, weight_scale,
+                                         (int)w_count, C, c_f32, s),
+                         "acc_passthrough");
+  const AccPlan pl = acc_plan(M, K, N);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < pl.bytes) return QMM_ERR_INVALID_ARG;
+  unsigned* err = err_word();
+  if (!err) return QMM_ERR_CUDA;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  __half* a16 = reinterpret_cast<__half*>(base);
+  __half* b16 = reinterpret_cast<__half*>(base + pl.off_b);
+  cudaError_t e;
+  if (!a_trans && !b_trans && K % 16 == 0 && N % 16 == 0 && aligned16(A) && aligned16(B)) {
+    e = launch_convert_bulk(A, false, a16, M * K, B, false, b16, K * N, err, s);   // dense copies: Kp = K, Np = N
+  } else {
+    const ConvPlane pa{A, a_trans ? M : K, (int)(a_trans ? K : M), (int)(a_trans ? M : K), a_trans, a16, pl.Kp};
+    const ConvPlane pb{B, b_trans ? K : N, (int)(b_trans ? N : K), (int)(b_trans ? K : N), b_trans, b16, pl.Np};
+    e = launch_convert_planes(pa, false, pb, false, s);
+  }
+  GemmF16Args f{};
+  f.A16 = a16;
+  f.B16 = b16;
+  f.batch = 1;
+  f.M = (int)M;
+  f.K = (int)K;
+  f.N = (int)N;
+  f.a_pitch = (int)pl.Kp;
+  f.b_pitch = (int)pl.Np;
+  f.C = C;
+  f.c_f32 = c_f32;
+  f.act_scale = act_scale;
+  f.act_count = (int)act_count;
+  f.w_scale = weight_scale;
+  f.w_count = (int)w_count;
+  f.acc_in = acc_in;
+  f.acc_out = acc_out;
+  f.zp_row_mod = (int)M;
+  f.err = err;
+  const char* gname = "none";
+  if (e == cudaSuccess) e = launch_gemm_f16pair(f, false, false, false, chunk_k_for(false, false), s, &gname);
+  return finish_launch(e, "f16_prepass+gemm_tc05_pair_f16ops_a8w8_acc");
 }
 
 size_t dynamic_quantize_linear_workspace_bytes(int64_t n) {

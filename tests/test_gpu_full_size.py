@@ -45,6 +45,24 @@ def test_a8w8_4096(workspace, kernel):
     assert_equal(got[rows], want, "a8w8 4096^3 sampled rows")
 
 
+@pytest.mark.parametrize("a_trans,b_trans", [(False, False), (True, True)])
+def test_a8w8_acc_4096(a_trans, b_trans):
+    w = W.a8w8_acc(4096, 4096, 4096, seed=0, a_trans=a_trans, b_trans=b_trans)
+    acc = torch.empty((4096, 4096), dtype=torch.int32, device="cuda")
+    C = q.qmm_a8w8_acc(dev(w.A), dev(w.B), dev(w.act_scale), dev(w.weight_scale), acc_in=dev(w.acc_in), acc_out=acc,
+                       a_trans=a_trans, b_trans=b_trans, out_dtype=torch.bfloat16)
+    q.check_device_error()
+    assert q.last_kernel() == "f16_prepass+gemm_tc05_pair_f16ops_a8w8_acc"
+    A = w.A.T if a_trans else w.A
+    B = np.ascontiguousarray(w.B.T) if b_trans else w.B
+    rows = sample(4096, 32, 2)
+    A_r = np.ascontiguousarray(A[rows])
+    want = O.a8w8_dequant_acc(w.acc_in[rows], A_r, B, w.act_scale[rows], w.weight_scale, "bf16")
+    assert_equal(host(C)[rows], want, "a8w8_acc 4096^3 sampled rows")
+    want_acc = O.wrap_int32(w.acc_in[rows].astype(np.int64) + O.a8w8_acc(A_r, B).astype(np.int64))
+    assert_equal(host(acc)[rows], want_acc, "a8w8_acc 4096^3 accumulator, sampled rows")
+
+
 @pytest.mark.parametrize("workspace,kernel", [("auto", "f16_prepass+gemm_tc05_pair_f16ops_matmul_integer"),
                                               (None, "gemm_tc05_pair_exact_matmul_integer")])
 def test_dql_then_matmul_integer_8192x4096x11008(workspace, kernel):
