@@ -256,6 +256,75 @@ def matmul_integer(A: np.ndarray, B: np.ndarray, a_zero_point=0, b_zero_point=0)
 
 
 # ---------------------------------------------------------------------------
+# ConvInteger
+# ---------------------------------------------------------------------------
+
+def conv_output_size(size: int, k: int, pad_begin: int, pad_end: int, stride: int, dilation: int) -> int:
+    """Output extent of one spatial axis: floor((size + pads - dilation*(k-1) - 1) / stride) + 1."""
+    return (size + pad_begin + pad_end - dilation * (k - 1) - 1) // stride + 1
+
+
+def conv_integer(x: np.ndarray, w: np.ndarray, x_zero_point=0, w_zero_point=0, pads=None, strides=None,
+                 dilations=None, group: int = 1) -> np.ndarray:
+    """y[n,m,oh,ow] = sum over the group's channels c and the kernel taps (kh,kw) of
+    (xs[n,c,oh*sh+kh*dh-pt, ow*sw+kw*dw-pl]) * (w[m,c,kh,kw] - w_zp[m]),
+    xs = x - x_zp and 0 outside the input (the padding); int64, wrapped to int32.
+
+    [P5] "What", ConvInteger paragraph: rank-4 NCHW, and rank-3 NCL widened to
+    the rank-4 path with a unit spatial row (NC1L) whose result is collapsed;
+    the activation zero point is a scalar; the weight zero point is a scalar or
+    one value per output channel. The page does not state the value taken at
+    padded positions; this reads the operator as the convolution of the
+    zero-point-shifted tensors, so a padded position contributes nothing
+    (equivalently, the input is padded with x_zp). pads follow ONNX order
+    [top, left, bottom, right] ([begin, end] for rank 3); strides and
+    dilations are (h, w) (one value for rank 3). w is [M, C/group, kH, kW]."""
+    x = np.asarray(x)
+    w = np.asarray(w)
+    rank3 = x.ndim == 3
+    if rank3:                                   # NCL -> NC1L
+        x = x[:, :, None, :]
+        w = w[:, :, None, :]
+        pads = [0, 0, 0, 0] if pads is None else [0, pads[0], 0, pads[1]]
+        strides = [1, 1] if strides is None else [1, strides[0]]
+        dilations = [1, 1] if dilations is None else [1, dilations[0]]
+    pads = [0, 0, 0, 0] if pads is None else list(pads)
+    strides = [1, 1] if strides is None else list(strides)
+    dilations = [1, 1] if dilations is None else list(dilations)
+    Nb, C, H, W_ = x.shape
+    M, Cg, kH, kW = w.shape
+    if C != Cg * group or M % group != 0:
+        raise ValueError("channels do not divide into the groups")
+    Mg = M // group
+    pt, pl, pb, pr = pads
+    sh, sw = strides
+    dh, dw = dilations
+    oH = conv_output_size(H, kH, pt, pb, sh, dh)
+    oW = conv_output_size(W_, kW, pl, pr, sw, dw)
+    xzp = np.asarray(x_zero_point, dtype=np.int64).reshape(-1)
+    wzp = np.asarray(w_zero_point, dtype=np.int64).reshape(-1)
+    if xzp.size != 1:
+        raise ValueError("x_zero_point must be a scalar")
+    if wzp.size not in (1, M):
+        raise ValueError("w_zero_point must have 1 or M values")
+    xs = x.astype(np.int64) - xzp[0]
+    ws = w.astype(np.int64) - (wzp[0] if wzp.size == 1 else wzp[:, None, None, None])
+    xp = np.zeros((Nb, C, H + pt + pb, W_ + pl + pr), dtype=np.int64)
+    xp[:, :, pt:pt + H, pl:pl + W_] = xs
+    y = np.zeros((Nb, M, oH, oW), dtype=np.int64)
+    for g in range(group):
+        xg = xp[:, g * Cg:(g + 1) * Cg]
+        for kh in range(kH):
+            for kw in range(kW):
+                h0, w0 = kh * dh, kw * dw
+                patch = xg[:, :, h0:h0 + sh * (oH - 1) + 1:sh, w0:w0 + sw * (oW - 1) + 1:sw]   # [N, Cg, oH, oW]
+                tap = ws[g * Mg:(g + 1) * Mg, :, kh, kw]                                        # [Mg, Cg]
+                y[:, g * Mg:(g + 1) * Mg] += np.einsum("nchw,mc->nmhw", patch, tap)
+    y = wrap_int32(y)
+    return y[:, :, 0, :] if rank3 else y
+
+
+# ---------------------------------------------------------------------------
 # Form (d): DynamicQuantizeLinear (uint8)
 # ---------------------------------------------------------------------------
 

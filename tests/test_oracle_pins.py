@@ -423,3 +423,113 @@ def test_a8w8_dequant_acc_brute_force_with_wrap():
             s = (s + 2**31) % 2**32 - 2**31
             v = f32(f32(f32(float(s)) * float(a_s[m])) * float(w_s[n]))
             assert got[m, n] == np.float32(v), (m, n)
+
+
+# ---------------------------------------------------------------------------
+# ConvInteger
+# ---------------------------------------------------------------------------
+
+def _conv_brute(x, w, xzp, wzp, pads, strides, dils, group):
+    """Exact Python integers, one output at a time, straight from the definition."""
+    N, C, H, Wd = x.shape
+    M, Cg, kH, kW = w.shape
+    pt, pl, pb, pr = pads
+    oH = (H + pt + pb - dils[0] * (kH - 1) - 1) // strides[0] + 1
+    oW = (Wd + pl + pr - dils[1] * (kW - 1) - 1) // strides[1] + 1
+    Mg = M // group
+    wz = list(wzp) if len(wzp) == M else [wzp[0]] * M
+    out = np.zeros((N, M, oH, oW), dtype=np.int64)
+    for n in range(N):
+        for m in range(M):
+            g = m // Mg
+            for oh in range(oH):
+                for ow in range(oW):
+                    s = 0
+                    for c in range(Cg):
+                        for kh in range(kH):
+                            for kw in range(kW):
+                                ih = oh * strides[0] + kh * dils[0] - pt
+                                iw = ow * strides[1] + kw * dils[1] - pl
+                                if 0 <= ih < H and 0 <= iw < Wd:
+                                    xv = int(x[n, g * Cg + c, ih, iw]) - int(xzp)
+                                else:
+                                    xv = 0
+                                s += xv * (int(w[m, c, kh, kw]) - int(wz[m]))
+                    out[n, m, oh, ow] = (s + 2**31) % 2**32 - 2**31
+    return out
+
+
+@pytest.mark.parametrize("xdt,wdt", [(np.uint8, np.int8), (np.int8, np.int8), (np.uint8, np.uint8)])
+def test_conv_integer_brute_force(xdt, wdt):
+    rng = np.random.default_rng(51)
+    info = {np.uint8: (0, 256), np.int8: (-128, 128)}
+    x = rng.integers(*info[xdt], size=(2, 4, 6, 7)).astype(xdt)
+    w = rng.integers(*info[wdt], size=(6, 2, 3, 2)).astype(wdt)
+    xzp = np.array([rng.integers(*info[xdt])], xdt)
+    wzp = rng.integers(*info[wdt], size=6).astype(wdt)
+    for pads, strides, dils, group in [([1, 0, 2, 1], [2, 1], [1, 2], 2), ([0, 0, 0, 0], [1, 1], [1, 1], 1)]:
+        wg = w if group == 2 else rng.integers(*info[wdt], size=(6, 4, 3, 2)).astype(wdt)
+        got = O.conv_integer(x, wg, xzp, wzp, pads, strides, dils, group)
+        assert np.array_equal(got, _conv_brute(x, wg, xzp[0], wzp, pads, strides, dils, group)), (pads, group)
+
+
+def test_conv_integer_single_channel_is_scipy_correlate():
+    """One input and one output channel: the zero-point-shifted input, zero
+    padded, correlated with the shifted kernel (scipy), then subsampled by
+    the stride; a dilation spreads the kernel taps apart with zeros."""
+    scipy_signal = pytest.importorskip("scipy.signal")
+    rng = np.random.default_rng(52)
+    x = rng.integers(0, 256, size=(1, 1, 11, 9)).astype(np.uint8)
+    w = rng.integers(-128, 128, size=(1, 1, 3, 4)).astype(np.int8)
+    xzp, wzp = 131, -7
+    for pads, strides, dils in [([0, 0, 0, 0], [1, 1], [1, 1]), ([2, 1, 1, 3], [2, 3], [1, 1]),
+                                ([1, 2, 2, 1], [1, 2], [2, 3])]:
+        xs = np.pad(x[0, 0].astype(np.int64) - xzp, ((pads[0], pads[2]), (pads[1], pads[3])))
+        ks = w[0, 0].astype(np.int64) - wzp
+        kd = np.zeros(((ks.shape[0] - 1) * dils[0] + 1, (ks.shape[1] - 1) * dils[1] + 1), np.int64)
+        kd[::dils[0], ::dils[1]] = ks
+        full = scipy_signal.correlate2d(xs, kd, mode="valid")
+        want = full[::strides[0], ::strides[1]]
+        got = O.conv_integer(x, w, xzp, wzp, pads, strides, dils)
+        assert np.array_equal(got[0, 0], want), (pads, strides, dils)
+
+
+def test_conv_integer_rank3_is_a_sum_of_1d_correlations():
+    scipy_signal = pytest.importorskip("scipy.signal")
+    rng = np.random.default_rng(53)
+    x = rng.integers(-128, 128, size=(2, 3, 20)).astype(np.int8)
+    w = rng.integers(-128, 128, size=(4, 3, 5)).astype(np.int8)
+    wzp = rng.integers(-128, 128, size=4).astype(np.int8)
+    got = O.conv_integer(x, w, -3, wzp, pads=[2, 1], strides=[2], dilations=[1])
+    for n in range(2):
+        for m in range(4):
+            acc = sum(scipy_signal.correlate(np.pad(x[n, c].astype(np.int64) + 3, (2, 1)),
+                                             w[m, c].astype(np.int64) - int(wzp[m]), mode="valid")
+                      for c in range(3))
+            assert np.array_equal(got[n, m], acc[::2]), (n, m)
+
+
+def test_conv_integer_1x1_is_a_matmul_per_image():
+    rng = np.random.default_rng(54)
+    x = rng.integers(0, 256, size=(3, 17, 5, 6)).astype(np.uint8)
+    w = rng.integers(-128, 128, size=(9, 17, 1, 1)).astype(np.int8)
+    wzp = rng.integers(-128, 128, size=9).astype(np.int8)
+    got = O.conv_integer(x, w, 100, wzp)
+    Wm = w[:, :, 0, 0].astype(np.int64) - wzp[:, None].astype(np.int64)
+    for n in range(3):
+        want = Wm @ (x[n].reshape(17, 30).astype(np.int64) - 100)
+        assert np.array_equal(got[n].reshape(9, 30), want)
+
+
+def test_conv_integer_output_extent_and_wrap():
+    """Closed form: every tap 255 * 127 over C*kH*kW taps, past the int32 range."""
+    C = 8000
+    x = np.full((1, C, 3, 3), 255, np.uint8)
+    w = np.full((2, C, 3, 3), 127, np.int8)
+    got = O.conv_integer(x, w)
+    assert got.shape == (1, 2, 1, 1)
+    total = 255 * 127 * C * 9
+    assert total > 2**31
+    assert (got == (total + 2**31) % 2**32 - 2**31).all()
+    assert O.conv_output_size(56, 3, 1, 1, 1, 1) == 56 and O.conv_output_size(56, 3, 1, 1, 2, 1) == 28
+    assert O.conv_output_size(10, 3, 0, 0, 1, 4) == 2
