@@ -479,6 +479,50 @@ def case_setups(q, torch, peaks):
                     "note": "bf16 x int8 weight (weight pre-pass to bf16 + SM-pair GEMM), fp32 accumulation"}
         return (lambda: q.qmm_w8_dequant(Ad, Wd, sd, None, out=Cd, workspace=wsp)), False, report
 
+    def a8w8_acc(Ma, Ka, Na, b_trans):
+        def setup():
+            w = W.a8w8_acc(Ma, Ka, Na, seed=0, b_trans=b_trans)
+            A, B = torch.from_numpy(w.A).cuda(), torch.from_numpy(w.B).cuda()
+            acc = torch.from_numpy(w.acc_in).cuda()
+            a_s, w_s = torch.from_numpy(w.act_scale).cuda(), torch.from_numpy(w.weight_scale).cuda()
+            C = torch.empty((Ma, Na), dtype=torch.bfloat16, device="cuda")
+            wsa = torch.empty(q.qmm_a8w8_acc_workspace_bytes(Ma, Ka, Na), dtype=torch.uint8, device="cuda")
+            ops = 2.0 * Ma * Ka * Na
+            nbytes = Ma * Ka + Ka * Na + Ma * Na * 4 + Ma * 4 + Na * 4 + Ma * Na * 2
+
+            def report(ms):
+                tops = ops / (ms * 1e-3) / 1e12
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                return {"us": ms * 1e3, "value": tops, "unit": "TOPS", "frac_tensor": tops / tc, "gbs": gbs,
+                        "frac_hbm": gbs / hbm, "algorithmic_bytes": nbytes,
+                        "note": f"int32 acc_in + A @ B, {'B stored [N,K] (b_trans)' if b_trans else 'B [K,N]'}, "
+                                "bf16 out; pre-pass + SM-pair GEMM"}
+            call = lambda: q.qmm_a8w8_acc(A, B, a_s, w_s, acc_in=acc, b_trans=b_trans, out=C,  # noqa: E731
+                                          workspace=wsa)
+            return call, Ma * Ka + Ka * Na < 2 * FLUSH_BYTES // 3, report
+        return setup
+
+    def conv(make):
+        def setup():
+            c = make()
+            x, w = torch.from_numpy(c.x).cuda(), torch.from_numpy(c.w).cuda()
+            xz, wz = torch.from_numpy(c.x_zp).cuda(), torch.from_numpy(c.w_zp).cuda()
+            y = q.conv_integer(x, w, xz, wz, pads=c.pads, strides=c.strides, dilations=c.dilations, group=c.group)
+            wsc = torch.empty(q.conv_integer_workspace_bytes(tuple(c.x.shape), tuple(c.w.shape), c.pads, c.strides,
+                                                             c.dilations, c.group), dtype=torch.uint8, device="cuda")
+            taps = int(np.prod(c.w.shape[1:]))
+            ops = 2.0 * y.numel() * taps
+
+            def report(ms):
+                tops = ops / (ms * 1e-3) / 1e12
+                return {"us": ms * 1e3, "value": tops, "unit": "TOPS", "frac_tensor": tops / tc,
+                        "note": f"x {list(c.x.shape)} u8, w {list(c.w.shape)} s8, scalar x_zp, per-channel w_zp; "
+                                "im2col pre-pass + SM-pair MatMulInteger GEMM"}
+            call = lambda: q.conv_integer(x, w, xz, wz, pads=c.pads, strides=c.strides,  # noqa: E731
+                                          dilations=c.dilations, group=c.group, out=y, workspace=wsc)
+            return call, True, report
+        return setup
+
     def w8():
         sw = W.w8_dequant_f32_64x256x192()
         As, Bs = torch.from_numpy(sw.A).cuda(), torch.from_numpy(sw.B).cuda()
@@ -492,12 +536,19 @@ def case_setups(q, torch, peaks):
             "w8_prefill_bf16_4096x8192x28672": w8_prefill,
             "decode_gemv_M1": gemv(1), "decode_gemv_M4": gemv(4), "decode_gemv_M16": gemv(16),
             "dql_8192x4096": dql, "matmul_integer_8192x4096x11008": mmi,
-            "batched_matmul_integer_65536x1024x1024": batched, "w8_dequant_f32_64x256x192": w8}
+            "batched_matmul_integer_65536x1024x1024": batched, "w8_dequant_f32_64x256x192": w8,
+            "a8w8_acc_4096x4096x4096_bf16": a8w8_acc(4096, 4096, 4096, False),
+            "a8w8_acc_4096x4096x4096_bf16_b_trans": a8w8_acc(4096, 4096, 4096, True),
+            "a8w8_acc_decode_M1_8192x28672_b_trans": a8w8_acc(1, 8192, 28672, True),
+            "conv_integer_3x3_8x256x56x56": conv(W.conv2d_3x3_8x256x56x56),
+            "conv_integer_1d_k3_4x512x3000": conv(W.conv1d_k3_4x512x3000)}
 
 
 SECONDARY = ["a8w8_4096x4096x4096_bf16_single_pass", "decode_gemv_M1", "decode_gemv_M4", "decode_gemv_M16", "dql_8192x4096",
              "matmul_integer_8192x4096x11008", "batched_matmul_integer_65536x1024x1024",
-             "w8_prefill_bf16_4096x8192x28672", "w8_dequant_f32_64x256x192"]
+             "w8_prefill_bf16_4096x8192x28672", "w8_dequant_f32_64x256x192", "a8w8_acc_4096x4096x4096_bf16",
+             "a8w8_acc_4096x4096x4096_bf16_b_trans", "a8w8_acc_decode_M1_8192x28672_b_trans",
+             "conv_integer_3x3_8x256x56x56", "conv_integer_1d_k3_4x512x3000"]
 
 
 def secondary(q, torch, flush, clocks, peaks):

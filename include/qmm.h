@@ -250,6 +250,46 @@ qmm_status matmul_integer_ws(const void* A, int a_dtype, const void* B, int b_dt
                              void* stream);
 
 /*
+ * ConvInteger. ROCm hip-ep PR #1248, "What", ConvInteger paragraph: rank-4
+ * NCHW, and rank-3 NCL widened to a unit spatial row (the caller passes H = 1,
+ * kH = 1 and zero top/bottom pads; the result is then [N, M, 1, oW]); a
+ * scalar activation zero point; a scalar or per-output-channel weight zero
+ * point. With Cg = C / group, Mg = M / group and g = m / Mg:
+ *   y[n,m,oh,ow] = sum_{c<Cg, kh, kw} (xs[n, g*Cg + c, oh*sh + kh*dh - pt, ow*sw + kw*dw - pl])
+ *                                     * (w[m,c,kh,kw] - w_zp[m])           (exact, int32, wrapping)
+ * where xs = x - x_zp inside the input and 0 at padded positions (the page
+ * leaves the pad value open; this is the convolution of the shifted tensors).
+ *
+ *  x            [N,C,H,W] 8-bit (x_dtype QMM_U8 / QMM_S8), device
+ *  w            [M,C/group,kH,kW] 8-bit (w_dtype), device
+ *  pads         host int64[4] {top, left, bottom, right} (ONNX order), or NULL (all 0)
+ *  strides      host int64[2] {h, w}, or NULL (1, 1)
+ *  dilations    host int64[2] {h, w}, or NULL (1, 1)
+ *  group        >= 1, dividing C and M
+ *  x_zero_point device, one value of x's type, or NULL (0)
+ *  w_zero_point device, w_zp_count (0, 1 or M) values of w's type
+ *  y            device int32 [N,M,oH,oW], oH = (H + pt + pb - dh*(kH-1) - 1)/sh + 1 (same for W)
+ *  workspace    at least conv_integer_workspace_bytes(...) bytes, 16-byte aligned
+ * Kernels: the weight as exact fp16 with its row sums, an im2col pre-pass that
+ * writes each image's [C*kH*kW, oH*oW] matrix as exact fp16 (padded positions
+ * holding x_zp) with its column sums, then the SM-pair MatMulInteger GEMM with
+ * A = the weight (per-row zero point w_zp), B = the im2col matrix (zero point
+ * x_zp), one batch per (image, group), its rows written straight into NCHW.
+ * Errors: QMM_ERR_INVALID_ARG for a bad dtype, geometry (group not dividing C
+ * and M, non-positive extents, strides or dilations, negative pads), zero-point
+ * count, null pointer or too small a workspace; QMM_ERR_UNSUPPORTED above
+ * 65535 (image, group) pairs per call. An empty output (N = 0, or a kernel wider than the
+ * padded input) launches nothing.
+ */
+size_t conv_integer_workspace_bytes(int64_t N, int64_t C, int64_t H, int64_t W, int64_t M, int64_t kH, int64_t kW,
+                                    const int64_t* pads, const int64_t* strides, const int64_t* dilations,
+                                    int64_t group);
+qmm_status conv_integer(const void* x, int x_dtype, const void* w, int w_dtype, int64_t N, int64_t C, int64_t H,
+                        int64_t W, int64_t M, int64_t kH, int64_t kW, const int64_t* pads, const int64_t* strides,
+                        const int64_t* dilations, int64_t group, const void* x_zero_point, const void* w_zero_point,
+                        int64_t w_zp_count, int32_t* y, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Form (d): DynamicQuantizeLinear, uint8 only. ROCm hip-ep PR #1248, section
  * "What", DynamicQuantizeLinear paragraph (reduce to a scalar min and max,
  * scale (max-min)/255 with a zero range selecting scale 1, ties-to-even zero

@@ -126,6 +126,43 @@ def a8w8_acc(M: int, K: int, N: int, seed: int = 0, a_trans: bool = False, b_tra
 
 
 @dataclass
+class ConvIntegerCase:
+    x: np.ndarray        # u8 [N, C, H, W] or [N, C, L]
+    w: np.ndarray        # s8 [M, C/group, kH, kW] or [M, C/group, k]
+    x_zp: np.ndarray     # u8 [1]
+    w_zp: np.ndarray     # s8 [M]
+    pads: list
+    strides: list
+    dilations: list
+    group: int
+
+
+def conv_integer_case(x_shape, w_shape, pads=None, strides=None, dilations=None, group=1, seed=0,
+                      x_dtype=np.uint8, w_dtype=np.int8) -> ConvIntegerCase:
+    """Quantised-convolution inputs: activations and weights uniform over their
+    8-bit range, a scalar activation zero point and one weight zero point per
+    output channel, drawn from the same ranges."""
+    rng = rng_for(seed)
+    lo = {np.uint8: 0, np.int8: -128}
+    x = uniform_int(rng, lo[x_dtype], lo[x_dtype] + 255, x_shape, x_dtype)
+    w = uniform_int(rng, lo[w_dtype], lo[w_dtype] + 255, w_shape, w_dtype)
+    xzp = uniform_int(rng, lo[x_dtype], lo[x_dtype] + 255, (1,), x_dtype)
+    wzp = uniform_int(rng, lo[w_dtype], lo[w_dtype] + 255, (w_shape[0],), w_dtype)
+    return ConvIntegerCase(x=x, w=w, x_zp=xzp, w_zp=wzp, pads=pads, strides=strides, dilations=dilations,
+                           group=group)
+
+
+def conv2d_3x3_8x256x56x56(seed: int = 0) -> ConvIntegerCase:
+    """A 3x3 convolution layer, 256 -> 256 channels on 56 x 56 maps, batch 8, same padding."""
+    return conv_integer_case((8, 256, 56, 56), (256, 256, 3, 3), pads=[1, 1, 1, 1], seed=seed)
+
+
+def conv1d_k3_4x512x3000(seed: int = 0) -> ConvIntegerCase:
+    """A rank-3 (NCL) encoder convolution, 512 -> 512 channels, kernel 3, length 3000, batch 4."""
+    return conv_integer_case((4, 512, 3000), (512, 512, 3), pads=[1, 1], seed=seed)
+
+
+@dataclass
 class DqlMatMulInteger:
     x: np.ndarray      # f32 [M, K]
     B: np.ndarray      # i8 [K, N]

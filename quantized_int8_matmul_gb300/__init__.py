@@ -59,6 +59,10 @@ def _load() -> ctypes.CDLL:
     lib.qmm_a8w8_acc_workspace_bytes.argtypes = [i64, i64, i64]
     lib.qmm_a8w8_acc_workspace_bytes.restype = sz
     lib.qmm_a8w8_acc.argtypes = [vp, ci, vp, ci, i64, i64, i64, vp, vp, vp, i64, vp, i64, vp, ci, vp, sz, vp]
+    lib.conv_integer_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64, i64, vp, vp, vp, i64]
+    lib.conv_integer_workspace_bytes.restype = sz
+    lib.conv_integer.argtypes = [vp, ci, vp, ci, i64, i64, i64, i64, i64, i64, i64, vp, vp, vp, i64, vp, vp, i64,
+                                 vp, vp, sz, vp]
     lib.qmm_a8w8_pack.argtypes = [vp, vp, i64, i64, i64, vp, sz, vp]
     lib.qmm_a8w8_packed.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, ci, vp, sz, vp]
     lib.matmul_integer_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64]
@@ -281,6 +285,85 @@ def qmm_a8w8_acc(A, B, act_scale=None, weight_scale=None, acc_in=None, acc_out=N
     return out
 
 
+def _conv_geometry(x_shape, w_shape, pads, strides, dilations):
+    """(N, C, H, W), (M, Cg, kH, kW) and the ctypes int64 arrays of the 2-D
+    geometry; a rank-3 NCL problem becomes NC1L (unit spatial row)."""
+    if len(x_shape) == 3:
+        if len(w_shape) != 3:
+            raise ValueError("a rank-3 input takes a rank-3 weight")
+        pads = [0, 0] if pads is None else list(pads)
+        strides = [1] if strides is None else list(strides)
+        dilations = [1] if dilations is None else list(dilations)
+        if len(pads) != 2 or len(strides) != 1 or len(dilations) != 1:
+            raise ValueError("rank 3: pads [begin, end], one stride, one dilation")
+        x4 = (x_shape[0], x_shape[1], 1, x_shape[2])
+        w4 = (w_shape[0], w_shape[1], 1, w_shape[2])
+        pads, strides, dilations = [0, pads[0], 0, pads[1]], [1, strides[0]], [1, dilations[0]]
+    elif len(x_shape) == 4:
+        if len(w_shape) != 4:
+            raise ValueError("a rank-4 input takes a rank-4 weight")
+        x4, w4 = tuple(x_shape), tuple(w_shape)
+        pads = [0, 0, 0, 0] if pads is None else list(pads)
+        strides = [1, 1] if strides is None else list(strides)
+        dilations = [1, 1] if dilations is None else list(dilations)
+        if len(pads) != 4 or len(strides) != 2 or len(dilations) != 2:
+            raise ValueError("rank 4: pads [top, left, bottom, right], strides and dilations (h, w)")
+    else:
+        raise ValueError("ConvInteger takes rank-3 (NCL) or rank-4 (NCHW) inputs")
+    arr = lambda v: (ctypes.c_int64 * len(v))(*[int(t) for t in v])  # noqa: E731
+    return x4, w4, (pads, strides, dilations), (arr(pads), arr(strides), arr(dilations))
+
+
+def conv_integer_workspace_bytes(x_shape, w_shape, pads=None, strides=None, dilations=None, group=1) -> int:
+    x4, w4, _, (p, st, dl) = _conv_geometry(x_shape, w_shape, pads, strides, dilations)
+    return int(_lib.conv_integer_workspace_bytes(*x4, w4[0], w4[2], w4[3], p, st, dl, group))
+
+
+def conv_integer(x, w, x_zero_point=None, w_zero_point=None, pads=None, strides=None, dilations=None, group=1,
+                 out=None, stream=None, workspace="auto"):
+    """ConvInteger: y = conv(x - x_zp, w - w_zp) in int32 (wrapping), x [N,C,H,W]
+    or [N,C,L], w [M,C/group,kH,kW] or [M,C/group,k], both uint8 or int8;
+    x_zero_point one value (x's dtype), w_zero_point one or M values (w's
+    dtype); pads in ONNX order ([top, left, bottom, right] / [begin, end])."""
+    _need(x, (torch.int8, torch.uint8), "x")
+    _need(w, (torch.int8, torch.uint8), "w")
+    x4, w4, (pads_, strides_, dils_), (p, st, dl) = _conv_geometry(tuple(x.shape), tuple(w.shape), pads, strides,
+                                                                   dilations)
+    N, C, H, Wd = x4
+    M, Cg, kH, kW = w4
+    if Cg * group != C or M % group != 0:
+        raise ValueError("channels do not divide into the groups")
+    xzp = wzp = None
+    if x_zero_point is not None:
+        _need(x_zero_point, (x.dtype,), "x_zero_point")
+        if x_zero_point.numel() != 1:
+            raise ValueError("x_zero_point must be a scalar")
+        xzp = x_zero_point
+    if w_zero_point is not None:
+        _need(w_zero_point, (w.dtype,), "w_zero_point")
+        if w_zero_point.numel() not in (1, M):
+            raise ValueError("w_zero_point must have 1 or M values")
+        wzp = w_zero_point
+    if min(strides_) >= 1 and min(dils_) >= 1:
+        oH = max((H + pads_[0] + pads_[2] - dils_[0] * (kH - 1) - 1) // strides_[0] + 1, 0)
+        oW = max((Wd + pads_[1] + pads_[3] - dils_[1] * (kW - 1) - 1) // strides_[1] + 1, 0)
+    else:
+        oH = oW = 0   # the library rejects the geometry
+    shape = (N, M, oW) if x.dim() == 3 else (N, M, oH, oW)
+    if out is None:
+        out = torch.empty(shape, dtype=torch.int32, device=x.device)
+    _need(out, (torch.int32,), "out")
+    if tuple(out.shape) != shape:
+        raise ValueError(f"out must be {shape}")
+    ws, wsb = _workspace(workspace, conv_integer_workspace_bytes(tuple(x.shape), tuple(w.shape), pads, strides,
+                                                                 dilations, group), x.device)
+    st_ = _lib.conv_integer(_ptr(x), _TORCH_TO_QMM[x.dtype], _ptr(w), _TORCH_TO_QMM[w.dtype], N, C, H, Wd, M, kH, kW,
+                            p, st, dl, group, _ptr(xzp), _ptr(wzp), 0 if wzp is None else wzp.numel(), _ptr(out),
+                            _ptr(ws), wsb, _stream(stream))
+    _check("conv_integer", st_)
+    return out
+
+
 def matmul_integer(A, B, a_zero_point=None, b_zero_point=None, out=None, stream=None, workspace="auto"):
     """Form (c): int32 C = (A - a_zp) @ (B - b_zp), A [...,M,K], B [K,N] (shared) or [...,K,N].
 
@@ -377,7 +460,7 @@ def num_sms() -> int:
 
 
 __all__ = [
-    "qmm_w8_dequant", "qmm_a8w8", "qmm_a8w8_acc", "matmul_integer", "dynamic_quantize_linear",
+    "qmm_w8_dequant", "qmm_a8w8", "qmm_a8w8_acc", "matmul_integer", "conv_integer", "dynamic_quantize_linear",
     "dynamic_quantize_linear_workspace_bytes", "last_kernel", "check_device_error", "QmmError", "lib",
     "num_sms", "LIB_PATH",
 ]

@@ -149,7 +149,8 @@ __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm,
   if (row >= p.M) return;
   const size_t crow = ((size_t)tc.b * p.M + (size_t)row) * (size_t)p.N;
   const uint64_t pol = l2_policy_evict_first();
-  const int mz = row % p.zp_row_mod;
+  const int ag = p.a_bmod ? tc.b % p.a_bmod : 0;   // weight slice of a grouped batch
+  const int mz = ag * p.M + row % p.zp_row_mod;
   float as = 0.f;
   uint32_t za = 0u, rs = 0u;
   if (FA) {
@@ -202,7 +203,8 @@ __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm,
       const int zi = p.a_zp_count == 1 ? 0 : mz;
       za = AU ? (uint32_t)__ldg((const uint8_t*)p.a_zp + zi) : (uint32_t)(int)__ldg((const int8_t*)p.a_zp + zi);
     }
-    if (p.b_zp_count > 0) rs = (uint32_t)__ldg(p.rowsum + (size_t)(p.a_bstride ? tc.b : 0) * p.M + row);
+    if (p.b_zp_count > 0)
+      rs = (uint32_t)__ldg(p.rowsum + (size_t)(p.a_bstride ? (p.a_bmod ? ag : tc.b) : 0) * p.M + row);
   }
   const uint32_t kzz = (uint32_t)p.K * za;
 #pragma unroll
@@ -211,24 +213,8 @@ __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm,
     if (nb >= p.N) break;
     const bool full = (nb + 16 <= p.N) && (c_vec & 1);
     uint32_t* o = &sums[g * 16];
-    if (ACC) {
+    if (ACC) {   // the sums already hold acc_in (loaded before the tile's first chunk)
       const bool full_acc = (nb + 16 <= p.N) && (c_vec & 2);
-      if (p.acc_in) {   // the caller's int32 accumulator, added with wrap-around
-        const int* src = p.acc_in + crow + nb;
-        if (full_acc) {
-#pragma unroll
-          for (int i = 0; i < 16; i += 4) {
-            const uint4 x = ldg_nc_v4(src + i);
-            o[i] += x.x;
-            o[i + 1] += x.y;
-            o[i + 2] += x.z;
-            o[i + 3] += x.w;
-          }
-        } else {
-          for (int i = 0; i < 16; ++i)
-            if (nb + i < p.N) o[i] += (uint32_t)__ldg(src + i);
-        }
-      }
       if (p.acc_out) {
         int* dst = p.acc_out + crow + nb;
         if (full_acc) {
@@ -288,6 +274,35 @@ __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm,
         for (int i = 0; i < 16; ++i)
           if (nb + i < p.N) out[i] = (int)o[i];
       }
+    }
+  }
+}
+
+// Accumulating A8W8: start this thread's running sums (one row, CPW columns)
+// from the caller's int32 accumulator (0 outside the problem). Issued before
+// the wait for the tile's first chunk, so the loads overlap the MMAs.
+template <int CPW>
+__device__ __forceinline__ void preload_acc(const GemmF16Args& p, const TileCoord tc, int q, int h, int lane,
+                                            uint32_t (&sums)[CPW], int c_vec) {
+  const int row = tc.m0 + q * 32 + lane;
+  const bool rv = p.acc_in && row < p.M;
+  const int* src = rv ? p.acc_in + ((size_t)tc.b * p.M + (size_t)row) * (size_t)p.N : nullptr;
+  const uint64_t pol = l2_policy_evict_first();   // read once: keep the operand tiles in L2
+#pragma unroll
+  for (int g = 0; g < CPW / 16; ++g) {
+    const int nb = tc.n0 + h * CPW + g * 16;
+    if (rv && nb + 16 <= p.N && (c_vec & 2)) {
+#pragma unroll
+      for (int i = 0; i < 16; i += 4) {
+        const uint4 x = ldg_nc_v4_hint(src + nb + i, pol);
+        sums[g * 16 + i] = x.x;
+        sums[g * 16 + i + 1] = x.y;
+        sums[g * 16 + i + 2] = x.z;
+        sums[g * 16 + i + 3] = x.w;
+      }
+    } else {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) sums[g * 16 + i] = (rv && nb + i < p.N) ? (uint32_t)__ldg(src + nb + i) : 0u;
     }
   }
 }
@@ -401,7 +416,7 @@ __global__ void __launch_bounds__(NT, 1)
         const uint32_t bar = full_leader0 + (uint32_t)slot * 8u;
         if (rank == 0) mbar_arrive_expect_tx(&sm.full[slot], 2u * STAGE_BYTES);
         const uint32_t dst = sbase + (uint32_t)slot * STAGE_BYTES;
-        const int ab = p.a_bstride ? tc.b : 0, bb = p.b_bstride ? tc.b : 0;
+        const int ab = p.a_bstride ? (p.a_bmod ? tc.b % p.a_bmod : tc.b) : 0, bb = p.b_bstride ? tc.b : 0;
         const int nc = tc.n0 + (int)rank * BNH;
         tma_load_3d_pair(dst, &tmA, s * BK, tc.m0, ab, bar);
         const int kb = (FA && p.fa_kwrap) ? (s * BK) % p.fa_kwrap : s * BK;   // [hi | lo] halves reread W
@@ -431,6 +446,7 @@ __global__ void __launch_bounds__(NT, 1)
     if (my_tiles > 0) stage_columns<CPW, BU, MMI, FA, ACC>(p, sm, tc, warp, h, lane);
     for (int d = 0; d < total_chunks; ++d) {
       const int ab = d & 1;
+      if (ACC && c == 0) preload_acc<CPW>(p, tc, q, h, lane, sums, c_vec);
       if (!mbar_wait_cluster(&sm.acc_full[ab], (uint32_t)((d >> 1) & 1), &sm.abort_flag, p.err, SITE_ACC_FULL))
         break;
       tc_fence_after();
@@ -446,7 +462,7 @@ __global__ void __launch_bounds__(NT, 1)
             sums[g * 16 + i] = acc[i];
           } else {
             const uint32_t v = (uint32_t)__float2int_rn(__uint_as_float(acc[i]));
-            sums[g * 16 + i] = (c == 0) ? v : sums[g * 16 + i] + v;
+            sums[g * 16 + i] = (c == 0 && !ACC) ? v : sums[g * 16 + i] + v;
           }
         }
       }
@@ -541,7 +557,8 @@ cudaError_t launch_one(const GemmF16Args& a, int cs, int c_vec, const CUtensorMa
 // (box 64 x 64), both with 128-byte swizzle; rows a_pitch / b_pitch elements
 // apart (the columns past K or N are never read: the copies there are zeros).
 cudaError_t make_maps(const GemmF16Args& a, CUtensorMap* ta, CUtensorMap* tb) {
-  const uint64_t ab = a.a_bstride ? (uint64_t)a.batch : 1, bb = a.b_bstride ? (uint64_t)a.batch : 1;
+  const uint64_t ab = a.a_bstride ? (uint64_t)(a.a_bmod ? a.a_bmod : a.batch) : 1;
+  const uint64_t bb = a.b_bstride ? (uint64_t)a.batch : 1;
   const uint64_t ap = a.a_pitch ? (uint64_t)a.a_pitch : (uint64_t)a.K;
   const uint64_t bp = a.b_pitch ? (uint64_t)a.b_pitch : (uint64_t)a.N;
   const uint64_t as = 2ull * (a.a_bstride ? (uint64_t)a.a_bstride : (uint64_t)a.M * ap);

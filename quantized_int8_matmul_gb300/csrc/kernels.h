@@ -68,6 +68,10 @@ struct GemmF16Args {
   // acc_out is written (act_scale / w_scale unused)
   const int* acc_in;
   int* acc_out;
+  // A's batch index is b % a_bmod when a_bmod > 0 (a weight shared by every
+  // image, one slice per convolution group); per-row zero points and row sums
+  // are then indexed (b % a_bmod) * M + row
+  int a_bmod;
 };
 cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool mmi, int chunk_k, cudaStream_t s,
                                 const char** kernel_name);
@@ -101,6 +105,28 @@ cudaError_t launch_convert_planes(const ConvPlane& a, bool au, const ConvPlane& 
 // C = out(f32(acc) * act_scale[m] * w_scale[n]) where C is given.
 cudaError_t launch_acc_only(const int* acc_in, int* acc_out, int M, int N, const float* act_scale, int act_count,
                             const float* w_scale, int w_count, void* C, int c_f32, cudaStream_t s);
+
+// ConvInteger pre-pass (conv.cu). im2col of an 8-bit NCHW input into fp16
+// col[n][k][p] (k = (c*kH + kh)*kW + kw over all C input channels, p = oh*oW +
+// ow, rows `pitch` elements apart), padded positions holding the activation
+// zero point, and, when colsum is given, colsum[n*G + g][p] = the sum of group
+// g's k rows (from per-group channel sums of x held in sum_scratch, of
+// im2col_sum_scratch_bytes).
+struct Im2colArgs {
+  const void* x;           // [Nb][C][H][W]
+  int Nb, C, H, W;
+  int kH, kW, pt, pl, sh, sw, dh, dw, oH, oW;
+  int G;                   // groups
+  const void* xzp;         // device: the activation zero point (one byte of the x type), or null (0)
+  __half* col;
+  long long pitch;
+  int* colsum;             // or null
+};
+size_t im2col_sum_scratch_bytes(long long Nb, long long G, long long H, long long W);
+cudaError_t launch_im2col(const Im2colArgs& a, bool x_u8, int* sum_scratch, cudaStream_t s);
+// rows x cols 8-bit (dense) -> fp16 at `pitch`, with optional int32 row sums.
+cudaError_t launch_rows_pitched(const void* src, bool u8, int rows, int cols, __half* dst, long long pitch,
+                                int* rowsum, cudaStream_t s);
 
 // Pre-pass: 8-bit rows -> exact fp16 (one warp per row; optional row sums), and
 // 8-bit [mats][rows][cols] -> fp16 with column sums (colsum zeroed here).

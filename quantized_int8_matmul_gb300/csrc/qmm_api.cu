@@ -192,6 +192,62 @@ AccPlan acc_plan(int64_t M, int64_t K, int64_t N) {
   pl.bytes = pl.off_b + round256((size_t)K * pl.Np * 2);
   return pl;
 }
+// ConvInteger (ROCm hip-ep PR #1248, "What", ConvInteger paragraph) as the
+// exact MatMulInteger GEMM: A = the weight [M][C/G*kH*kW] (shared by every
+// image, one slice per group), B = each image's im2col matrix, C = y in NCHW.
+// Workspace: [W16: M x Kgp fp16][col: N x C*kH*kW x Pp fp16][rowsum(W): M
+// int32][colsum(col): N*G x P int32][channel sums of x: N*G x H*W int32], Kgp
+// and Pp rounded up to multiples of 8.
+struct ConvPlan {
+  bool ok = false;
+  int oH = 0, oW = 0;
+  int64_t P = 0, Pp = 0, Kg = 0, Kgp = 0;
+  int64_t pt = 0, pl = 0, pb = 0, pr = 0, sh = 1, sw = 1, dh = 1, dw = 1;
+  size_t off_col = 0, off_rs = 0, off_cs = 0, off_s = 0, bytes = 0;
+};
+
+ConvPlan conv_plan(int64_t N, int64_t C, int64_t H, int64_t W, int64_t M, int64_t kH, int64_t kW,
+                   const int64_t* pads, const int64_t* strides, const int64_t* dilations, int64_t G) {
+  ConvPlan pl;
+  if (!dim_ok(N) || !dim_ok(C) || !dim_ok(H) || !dim_ok(W) || !dim_ok(M) || !dim_ok(kH) || !dim_ok(kW)) return pl;
+  if (C < 1 || H < 1 || W < 1 || M < 1 || kH < 1 || kW < 1 || G < 1 || C % G != 0 || M % G != 0) return pl;
+  if (pads) {
+    pl.pt = pads[0];
+    pl.pl = pads[1];
+    pl.pb = pads[2];
+    pl.pr = pads[3];
+  }
+  if (strides) {
+    pl.sh = strides[0];
+    pl.sw = strides[1];
+  }
+  if (dilations) {
+    pl.dh = dilations[0];
+    pl.dw = dilations[1];
+  }
+  const int64_t lim = 1 << 20;
+  if (pl.pt < 0 || pl.pl < 0 || pl.pb < 0 || pl.pr < 0 || pl.pt > lim || pl.pl > lim || pl.pb > lim || pl.pr > lim)
+    return pl;
+  if (pl.sh < 1 || pl.sw < 1 || pl.dh < 1 || pl.dw < 1 || pl.sh > lim || pl.sw > lim || pl.dh > lim || pl.dw > lim)
+    return pl;
+  const int64_t oH = (H + pl.pt + pl.pb - pl.dh * (kH - 1) - 1) / pl.sh + 1;
+  const int64_t oW = (W + pl.pl + pl.pr - pl.dw * (kW - 1) - 1) / pl.sw + 1;
+  const int64_t eh = H + pl.pt + pl.pb - pl.dh * (kH - 1), ew = W + pl.pl + pl.pr - pl.dw * (kW - 1);
+  pl.oH = eh >= 1 ? (int)oH : 0;   // a kernel wider than the padded input: empty output
+  pl.oW = ew >= 1 ? (int)oW : 0;
+  pl.P = (int64_t)pl.oH * pl.oW;
+  pl.Kg = C / G * kH * kW;
+  if (C * kH * kW > (int64_t)INT_MAX || pl.P > (int64_t)INT_MAX || N * G > (int64_t)INT_MAX) return pl;
+  pl.Kgp = (pl.Kg + 7) / 8 * 8;
+  pl.Pp = (pl.P + 7) / 8 * 8;
+  pl.off_col = round256((size_t)M * pl.Kgp * 2);
+  pl.off_rs = pl.off_col + round256((size_t)N * C * kH * kW * pl.Pp * 2);
+  pl.off_cs = pl.off_rs + round256((size_t)M * 4);
+  pl.off_s = pl.off_cs + round256((size_t)N * G * pl.P * 4);
+  pl.bytes = pl.off_s + round256(im2col_sum_scratch_bytes(N, G, H, W));
+  pl.ok = true;
+  return pl;
+}
 }  // namespace
 
 int num_sms() {
@@ -660,6 +716,92 @@ qmm_status qmm_a8w8_acc(const int8_t* A, int a_trans, const int8_t* B, int b_tra
   const char* gname = "none";
   if (e == cudaSuccess) e = launch_gemm_f16pair(f, false, false, false, chunk_k_for(false, false), s, &gname);
   return finish_launch(e, "f16_prepass+gemm_tc05_pair_f16ops_a8w8_acc");
+}
+
+size_t conv_integer_workspace_bytes(int64_t N, int64_t C, int64_t H, int64_t W, int64_t M, int64_t kH, int64_t kW,
+                                    const int64_t* pads, const int64_t* strides, const int64_t* dilations,
+                                    int64_t group) {
+  const ConvPlan pl = conv_plan(N, C, H, W, M, kH, kW, pads, strides, dilations, group);
+  return (pl.ok && N > 0 && pl.P > 0) ? pl.bytes : 0;
+}
+
+qmm_status conv_integer(const void* x, int x_dtype, const void* w, int w_dtype, int64_t N, int64_t C, int64_t H,
+                        int64_t W, int64_t M, int64_t kH, int64_t kW, const int64_t* pads, const int64_t* strides,
+                        const int64_t* dilations, int64_t group, const void* x_zero_point, const void* w_zero_point,
+                        int64_t w_zp_count, int32_t* y, void* workspace, size_t workspace_bytes, void* stream) {
+  if ((x_dtype != QMM_S8 && x_dtype != QMM_U8) || (w_dtype != QMM_S8 && w_dtype != QMM_U8)) return QMM_ERR_INVALID_ARG;
+  const ConvPlan pl = conv_plan(N, C, H, W, M, kH, kW, pads, strides, dilations, group);
+  if (!pl.ok) return QMM_ERR_INVALID_ARG;
+  if (w_zp_count != 0 && w_zp_count != 1 && w_zp_count != M) return QMM_ERR_INVALID_ARG;
+  if (N == 0 || pl.P == 0) {
+    t_last_kernel = "none";
+    return QMM_OK;
+  }
+  if (!x || !w || !y || (w_zp_count > 0 && !w_zero_point)) return QMM_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < pl.bytes) return QMM_ERR_INVALID_ARG;
+  const int64_t Mg = M / group, batch = N * group;
+  if (N * group > 65535 || (C * kH * kW + 31) / 32 > 65535) return QMM_ERR_UNSUPPORTED;
+  if (batch * ((Mg + 255) / 256) * ((pl.P + 223) / 224) > (int64_t)INT_MAX) return QMM_ERR_UNSUPPORTED;
+  unsigned* err = err_word();
+  if (!err) return QMM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  const bool xu = x_dtype == QMM_U8, wu = w_dtype == QMM_U8;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  __half* w16 = reinterpret_cast<__half*>(base);
+  __half* col = reinterpret_cast<__half*>(base + pl.off_col);
+  int* rs = reinterpret_cast<int*>(base + pl.off_rs);
+  int* cs = reinterpret_cast<int*>(base + pl.off_cs);
+  // rowsum(W) serves the x_zp term, colsum(col) the w_zp term
+  cudaError_t e = launch_rows_pitched(w, wu, (int)M, (int)pl.Kg, w16, pl.Kgp, x_zero_point ? rs : nullptr, s);
+  if (e == cudaSuccess) {
+    Im2colArgs a{};
+    a.x = x;
+    a.Nb = (int)N;
+    a.C = (int)C;
+    a.H = (int)H;
+    a.W = (int)W;
+    a.kH = (int)kH;
+    a.kW = (int)kW;
+    a.pt = (int)pl.pt;
+    a.pl = (int)pl.pl;
+    a.sh = (int)pl.sh;
+    a.sw = (int)pl.sw;
+    a.dh = (int)pl.dh;
+    a.dw = (int)pl.dw;
+    a.oH = pl.oH;
+    a.oW = pl.oW;
+    a.G = (int)group;
+    a.xzp = x_zero_point;
+    a.col = col;
+    a.pitch = pl.Pp;
+    a.colsum = w_zp_count > 0 ? cs : nullptr;
+    e = launch_im2col(a, xu, reinterpret_cast<int*>(base + pl.off_s), s);
+  }
+  GemmF16Args f{};
+  f.A16 = w16;
+  f.B16 = col;
+  f.a_pitch = (int)pl.Kgp;
+  f.b_pitch = (int)pl.Pp;
+  f.a_bstride = group > 1 ? Mg * pl.Kgp : 0;
+  f.a_bmod = group > 1 ? (int)group : 0;
+  f.b_bstride = pl.Kg * pl.Pp;
+  f.batch = (int)batch;
+  f.M = (int)Mg;
+  f.K = (int)pl.Kg;
+  f.N = (int)pl.P;
+  f.C = y;
+  f.a_zp = w_zero_point;
+  f.a_zp_count = (int)w_zp_count;
+  f.b_zp = x_zero_point;
+  f.b_zp_count = x_zero_point ? 1 : 0;
+  f.rowsum = rs;
+  f.colsum = cs;
+  f.zp_row_mod = (int)Mg;
+  f.err = err;
+  const char* gname = "none";
+  if (e == cudaSuccess) e = launch_gemm_f16pair(f, wu, xu, true, chunk_k_for(wu, xu), s, &gname);
+  return finish_launch(e, "im2col_f16+gemm_tc05_pair_f16ops_matmul_integer");
 }
 
 size_t dynamic_quantize_linear_workspace_bytes(int64_t n) {

@@ -45,6 +45,21 @@ def test_a8w8_4096(workspace, kernel):
     assert_equal(got[rows], want, "a8w8 4096^3 sampled rows")
 
 
+@pytest.mark.parametrize("case", ["conv2d_3x3_8x256x56x56", "conv1d_k3_4x512x3000"])
+def test_conv_integer_full_size(case):
+    c = getattr(W, case)()
+    y = q.conv_integer(dev(c.x), dev(c.w), dev(c.x_zp), dev(c.w_zp), pads=c.pads, strides=c.strides,
+                       dilations=c.dilations, group=c.group)
+    q.check_device_error()
+    assert q.last_kernel() == "im2col_f16+gemm_tc05_pair_f16ops_matmul_integer"
+    got = host(y)
+    imgs = sample(c.x.shape[0], 2, 3)
+    chans = sample(c.w.shape[0], 12, 4)
+    chans[:2] = [0, c.w.shape[0] - 1]
+    want = O.conv_integer(c.x[imgs], c.w[chans], c.x_zp, c.w_zp[chans], c.pads, c.strides, c.dilations, c.group)
+    assert_equal(got[imgs][:, chans], want, f"{case}: sampled images and channels")
+
+
 @pytest.mark.parametrize("a_trans,b_trans", [(False, False), (True, True)])
 def test_a8w8_acc_4096(a_trans, b_trans):
     w = W.a8w8_acc(4096, 4096, 4096, seed=0, a_trans=a_trans, b_trans=b_trans)
