@@ -387,3 +387,30 @@ def row_sums(y: np.ndarray, row_len: int) -> np.ndarray:
 def col_sums(B: np.ndarray) -> np.ndarray:
     """sum_k B[k, n] as int32 (wrapped)."""
     return wrap_int32(np.asarray(B, dtype=np.int64).sum(axis=0))
+
+
+# ---------------------------------------------------------------------------
+# The chain DynamicQuantizeLinear -> MatMulInteger -> dequantise
+# ---------------------------------------------------------------------------
+
+def dynamic_quantize_matmul(x: np.ndarray, W: np.ndarray, w_scale, w_zero_point=0, bias=None):
+    """C = f32(f32(acc) * s[n]) (+ bias[n]), s[n] = f32(y_scale * w_scale[n]),
+    acc = MatMulInteger(y, W, y_zp, w_zp), (y, y_scale, y_zp) = DynamicQuantizeLinear(x).
+
+    [P5] "Why" and "What": a graph using MatMulInteger casts, scales and adds
+    the bias after it (the fused qlinear ops would scale twice). This is the
+    plainest reading of those graph steps, each an fp32 operation rounded to
+    nearest even: Cast(int32 -> fp32), Mul(y_scale, w_scale) into one fp32
+    multiplier per column, Mul(cast, multiplier), then Add(bias).
+    x is float32 [M, K]; W is int8 or uint8 [K, N]; w_scale and w_zero_point
+    have 1 or N values. Returns (C float32 [M, N], y_scale, y_zp)."""
+    x = np.asarray(x, dtype=np.float32)
+    N = np.asarray(W).shape[1]
+    y, ys, yzp = dynamic_quantize_linear(x)
+    acc = matmul_integer(y, W, int(yzp), w_zero_point)
+    ws = _as_vector(w_scale, N, "w_scale").astype(np.float32)
+    s = (np.float32(ys) * ws).astype(np.float32)
+    C = (acc.astype(np.float32) * s[None, :]).astype(np.float32)
+    if bias is not None:
+        C = (C + _as_vector(bias, N, "bias").astype(np.float32)[None, :]).astype(np.float32)
+    return C, ys, yzp

@@ -533,3 +533,51 @@ def test_conv_integer_output_extent_and_wrap():
     assert (got == (total + 2**31) % 2**32 - 2**31).all()
     assert O.conv_output_size(56, 3, 1, 1, 1, 1) == 56 and O.conv_output_size(56, 3, 1, 1, 2, 1) == 28
     assert O.conv_output_size(10, 3, 0, 0, 1, 4) == 2
+
+
+# ---------------------------------------------------------------------------
+# DynamicQuantizeLinear -> MatMulInteger -> dequantise
+# ---------------------------------------------------------------------------
+
+def test_dynamic_quantize_matmul_within_the_quantisation_bound():
+    """Against float64 x @ ((W - w_zp) * w_scale): quantising x moves each
+    element by at most y_scale / 2 (the range covers all of x, so nothing
+    saturates), so |C - exact| <= y_scale/2 * sum_k |W_deq[k, n]| plus the
+    fp32 rounding of the last steps."""
+    rng = np.random.default_rng(61)
+    M, K, N = 9, 70, 13
+    x = (rng.standard_normal((M, K)) * 2.0).astype(np.float32)
+    W = rng.integers(-128, 128, size=(K, N)).astype(np.int8)
+    w_scale = rng.uniform(0.001, 0.01, N).astype(np.float32)
+    w_zp = rng.integers(-20, 20, size=N).astype(np.int8)
+    bias = rng.standard_normal(N).astype(np.float32)
+    C, ys, _ = O.dynamic_quantize_matmul(x, W, w_scale, w_zp, bias)
+    Wd = (W.astype(np.float64) - w_zp.astype(np.float64)) * w_scale.astype(np.float64)
+    exact = x.astype(np.float64) @ Wd + bias.astype(np.float64)
+    bound = float(ys) / 2 * np.abs(Wd).sum(axis=0)[None, :] + 4 * 2.0**-23 * (np.abs(exact) + 1)
+    assert (np.abs(C.astype(np.float64) - exact) <= bound).all()
+    # the bound is tight enough to catch an activation zero point off by one:
+    # on a column whose dequantised weights are all positive that error is
+    # y_scale * sum_k W_deq[k, n], twice the bound's main term
+    y, _, yzp = O.dynamic_quantize_linear(x)
+    Wp = np.abs(Wd[:, :1]) + 1e-3
+    off = (float(ys) * (y.astype(np.float64) - (float(yzp) + 1))) @ Wp
+    bound_p = float(ys) / 2 * Wp.sum() + 4 * 2.0**-23 * (np.abs(x.astype(np.float64) @ Wp) + 1)
+    assert (np.abs(off - x.astype(np.float64) @ Wp) > bound_p).all()
+
+
+def test_dynamic_quantize_matmul_uint8_weight_and_no_bias():
+    rng = np.random.default_rng(62)
+    x = rng.uniform(-3, 5, (6, 40)).astype(np.float32)
+    W = rng.integers(0, 256, size=(40, 7)).astype(np.uint8)
+    C, ys, yzp = O.dynamic_quantize_matmul(x, W, np.float32(0.004), np.uint8(128))
+    Wd = (W.astype(np.float64) - 128) * 0.004
+    err = np.abs(C.astype(np.float64) - x.astype(np.float64) @ Wd)
+    assert (err <= float(ys) / 2 * np.abs(Wd).sum(axis=0)[None, :] + 1e-5).all()
+    # integer core: brute force in Python integers from the pinned quantiser's outputs
+    y, _, _ = O.dynamic_quantize_linear(x)
+    for m in range(6):
+        for n in range(7):
+            acc = sum((int(y[m, k]) - int(yzp)) * (int(W[k, n]) - 128) for k in range(40))
+            s = np.float32(np.float32(ys) * np.float32(0.004))
+            assert C[m, n] == np.float32(np.float32(acc) * s)
