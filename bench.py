@@ -502,6 +502,24 @@ def case_setups(q, torch, peaks):
             return call, Ma * Ka + Ka * Na < 2 * FLUSH_BYTES // 3, report
         return setup
 
+    def dq_chain():
+        d = W.dql_matmul_integer_8192x4096x11008()
+        rng = np.random.default_rng(9)
+        x, Bd, bz = torch.from_numpy(d.x).cuda(), torch.from_numpy(d.B).cuda(), torch.from_numpy(d.b_zp).cuda()
+        w_s = torch.from_numpy(rng.uniform(0.001, 0.01, 11008).astype(np.float32)).cuda()
+        bias = torch.from_numpy(rng.standard_normal(11008).astype(np.float32)).cuda()
+        Cf = torch.empty((8192, 11008), dtype=torch.float32, device="cuda")
+        wsd = torch.empty(q.dynamic_quantize_matmul_workspace_bytes(8192, 4096, 11008), dtype=torch.uint8,
+                          device="cuda")
+        ops = 2.0 * 8192 * 4096 * 11008
+
+        def report(ms):
+            tops = ops / (ms * 1e-3) / 1e12
+            return {"us": ms * 1e3, "value": tops, "unit": "TOPS", "frac_tensor": tops / tc,
+                    "note": "x fp32 -> DynamicQuantizeLinear -> MatMulInteger(per-column w_zp) -> fp32 "
+                            "* y_scale*w_scale[n] + bias[n], one call; weight converted every call"}
+        return (lambda: q.dynamic_quantize_matmul(x, Bd, w_s, bz, bias, out=Cf, workspace=wsd)), False, report
+
     def conv(make):
         def setup():
             c = make()
@@ -540,6 +558,7 @@ def case_setups(q, torch, peaks):
             "a8w8_acc_4096x4096x4096_bf16": a8w8_acc(4096, 4096, 4096, False),
             "a8w8_acc_4096x4096x4096_bf16_b_trans": a8w8_acc(4096, 4096, 4096, True),
             "a8w8_acc_decode_M1_8192x28672_b_trans": a8w8_acc(1, 8192, 28672, True),
+            "dql_matmul_dequant_fused_8192x4096x11008": dq_chain,
             "conv_integer_3x3_8x256x56x56": conv(W.conv2d_3x3_8x256x56x56),
             "conv_integer_1d_k3_4x512x3000": conv(W.conv1d_k3_4x512x3000)}
 
@@ -548,7 +567,8 @@ SECONDARY = ["a8w8_4096x4096x4096_bf16_single_pass", "decode_gemv_M1", "decode_g
              "matmul_integer_8192x4096x11008", "batched_matmul_integer_65536x1024x1024",
              "w8_prefill_bf16_4096x8192x28672", "w8_dequant_f32_64x256x192", "a8w8_acc_4096x4096x4096_bf16",
              "a8w8_acc_4096x4096x4096_bf16_b_trans", "a8w8_acc_decode_M1_8192x28672_b_trans",
-             "conv_integer_3x3_8x256x56x56", "conv_integer_1d_k3_4x512x3000"]
+             "conv_integer_3x3_8x256x56x56", "conv_integer_1d_k3_4x512x3000",
+             "dql_matmul_dequant_fused_8192x4096x11008"]
 
 
 def secondary(q, torch, flush, clocks, peaks):

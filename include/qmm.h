@@ -290,6 +290,38 @@ qmm_status conv_integer(const void* x, int x_dtype, const void* w, int w_dtype, 
                         int64_t w_zp_count, int32_t* y, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The chain DynamicQuantizeLinear -> MatMulInteger -> dequantise, in one call.
+ * ROCm hip-ep PR #1248, "Why" and "What": a graph using MatMulInteger casts,
+ * scales and adds the bias after it. Each step below is one fp32 operation
+ * rounded to nearest even:
+ *   (y, y_scale, y_zp) = DynamicQuantizeLinear(x)            (as dynamic_quantize_linear)
+ *   acc[m,n] = sum_k (y[m,k] - y_zp) * (W[k,n] - w_zp[n])    (exact, int32, wrapping)
+ *   C[m,n]   = f32(f32(acc) * f32(y_scale * w_scale[n]))  (+ bias[n], one more rounding)
+ *
+ *  x             device float [M,K]
+ *  W             device 8-bit [K,N] (w_dtype QMM_S8 or QMM_U8)
+ *  w_scale       device float[w_scale_count], 1 or N
+ *  w_zero_point  device, w_zp_count (0, 1 or N) values of W's type
+ *  bias          device float[N], or NULL
+ *  C             device float [M,N]
+ *  y_scale, y_zero_point  device float[1] / uint8[1] receiving the quantiser's
+ *                scale and zero point, or NULL (then kept in the workspace)
+ *  workspace     at least dynamic_quantize_matmul_workspace_bytes(M, K, N), 16-byte aligned
+ * Kernels: the quantiser's min/max pass; the weight as exact fp16 with its
+ * column sums; the quantize pass writing y straight into the GEMM's fp16 A
+ * operand with y's row sums (no uint8 tensor in between); the SM-pair
+ * MatMulInteger GEMM whose epilogue applies the zero points, the multiplier
+ * and the bias and stores fp32 (no int32 tensor in between).
+ * Errors: QMM_ERR_INVALID_ARG for a bad dtype, count, null pointer or too small
+ * a workspace; QMM_ERR_UNSUPPORTED for K = 0. M = 0 or N = 0 launches nothing.
+ */
+size_t dynamic_quantize_matmul_workspace_bytes(int64_t M, int64_t K, int64_t N);
+qmm_status dynamic_quantize_matmul(const float* x, int64_t M, int64_t K, const void* W, int w_dtype, int64_t N,
+                                   const float* w_scale, int64_t w_scale_count, const void* w_zero_point,
+                                   int64_t w_zp_count, const float* bias, float* C, float* y_scale,
+                                   uint8_t* y_zero_point, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Form (d): DynamicQuantizeLinear, uint8 only. ROCm hip-ep PR #1248, section
  * "What", DynamicQuantizeLinear paragraph (reduce to a scalar min and max,
  * scale (max-min)/255 with a zero range selecting scale 1, ties-to-even zero

@@ -393,7 +393,7 @@ def col_sums(B: np.ndarray) -> np.ndarray:
 # The chain DynamicQuantizeLinear -> MatMulInteger -> dequantise
 # ---------------------------------------------------------------------------
 
-def dynamic_quantize_matmul(x: np.ndarray, W: np.ndarray, w_scale, w_zero_point=0, bias=None):
+def dynamic_quantize_matmul(x: np.ndarray, W: np.ndarray, w_scale, w_zero_point=0, bias=None, rows=None):
     """C = f32(f32(acc) * s[n]) (+ bias[n]), s[n] = f32(y_scale * w_scale[n]),
     acc = MatMulInteger(y, W, y_zp, w_zp), (y, y_scale, y_zp) = DynamicQuantizeLinear(x).
 
@@ -403,10 +403,13 @@ def dynamic_quantize_matmul(x: np.ndarray, W: np.ndarray, w_scale, w_zero_point=
     nearest even: Cast(int32 -> fp32), Mul(y_scale, w_scale) into one fp32
     multiplier per column, Mul(cast, multiplier), then Add(bias).
     x is float32 [M, K]; W is int8 or uint8 [K, N]; w_scale and w_zero_point
-    have 1 or N values. Returns (C float32 [M, N], y_scale, y_zp)."""
+    have 1 or N values. Returns (C float32 [M, N], y_scale, y_zp); with rows
+    given, C holds only those rows (the quantiser still sees all of x)."""
     x = np.asarray(x, dtype=np.float32)
     N = np.asarray(W).shape[1]
     y, ys, yzp = dynamic_quantize_linear(x)
+    if rows is not None:
+        y = y[rows]
     acc = matmul_integer(y, W, int(yzp), w_zero_point)
     ws = _as_vector(w_scale, N, "w_scale").astype(np.float32)
     s = (np.float32(ys) * ws).astype(np.float32)

@@ -63,6 +63,9 @@ def _load() -> ctypes.CDLL:
     lib.conv_integer_workspace_bytes.restype = sz
     lib.conv_integer.argtypes = [vp, ci, vp, ci, i64, i64, i64, i64, i64, i64, i64, vp, vp, vp, i64, vp, vp, i64,
                                  vp, vp, sz, vp]
+    lib.dynamic_quantize_matmul_workspace_bytes.argtypes = [i64, i64, i64]
+    lib.dynamic_quantize_matmul_workspace_bytes.restype = sz
+    lib.dynamic_quantize_matmul.argtypes = [vp, i64, i64, vp, ci, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, sz, vp]
     lib.qmm_a8w8_pack.argtypes = [vp, vp, i64, i64, i64, vp, sz, vp]
     lib.qmm_a8w8_packed.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, ci, vp, sz, vp]
     lib.matmul_integer_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64]
@@ -364,6 +367,45 @@ def conv_integer(x, w, x_zero_point=None, w_zero_point=None, pads=None, strides=
     return out
 
 
+def dynamic_quantize_matmul_workspace_bytes(M: int, K: int, N: int) -> int:
+    return int(_lib.dynamic_quantize_matmul_workspace_bytes(M, K, N))
+
+
+def dynamic_quantize_matmul(x, W, w_scale, w_zero_point=None, bias=None, out=None, stream=None, workspace="auto"):
+    """DynamicQuantizeLinear(x) -> MatMulInteger(y, W, y_zp, w_zp) -> fp32 cast,
+    times y_scale * w_scale[n], plus bias[n]: C float32 [M, N] from x float32
+    [M, K] and W int8/uint8 [K, N]. Returns (C, y_scale [1], y_zero_point [1])."""
+    _need(x, (torch.float32,), "x")
+    _need(W, (torch.int8, torch.uint8), "W")
+    _need(w_scale, (torch.float32,), "w_scale")
+    if x.dim() != 2 or W.dim() != 2 or x.shape[1] != W.shape[0]:
+        raise ValueError("x [M, K] and W [K, N] expected")
+    M, K = x.shape
+    N = W.shape[1]
+    if w_scale.numel() not in (1, N):
+        raise ValueError("w_scale must have 1 or N values")
+    if w_zero_point is not None:
+        _need(w_zero_point, (W.dtype,), "w_zero_point")
+        if w_zero_point.numel() not in (1, N):
+            raise ValueError("w_zero_point must have 1 or N values")
+    if bias is not None:
+        _need(bias, (torch.float32,), "bias")
+        if bias.numel() != N:
+            raise ValueError("bias must have N values")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _need(out, (torch.float32,), "out")
+    ys = torch.empty(1, dtype=torch.float32, device=x.device)
+    yz = torch.empty(1, dtype=torch.uint8, device=x.device)
+    ws, wsb = _workspace(workspace, dynamic_quantize_matmul_workspace_bytes(M, K, N), x.device)
+    st = _lib.dynamic_quantize_matmul(_ptr(x), M, K, _ptr(W), _TORCH_TO_QMM[W.dtype], N, _ptr(w_scale),
+                                      w_scale.numel(), _ptr(w_zero_point),
+                                      0 if w_zero_point is None else w_zero_point.numel(), _ptr(bias), _ptr(out),
+                                      _ptr(ys), _ptr(yz), _ptr(ws), wsb, _stream(stream))
+    _check("dynamic_quantize_matmul", st)
+    return out, ys, yz
+
+
 def matmul_integer(A, B, a_zero_point=None, b_zero_point=None, out=None, stream=None, workspace="auto"):
     """Form (c): int32 C = (A - a_zp) @ (B - b_zp), A [...,M,K], B [K,N] (shared) or [...,K,N].
 
@@ -460,7 +502,8 @@ def num_sms() -> int:
 
 
 __all__ = [
-    "qmm_w8_dequant", "qmm_a8w8", "qmm_a8w8_acc", "matmul_integer", "conv_integer", "dynamic_quantize_linear",
+    "qmm_w8_dequant", "qmm_a8w8", "qmm_a8w8_acc", "matmul_integer", "conv_integer", "dynamic_quantize_matmul",
+    "dynamic_quantize_linear",
     "dynamic_quantize_linear_workspace_bytes", "last_kernel", "check_device_error", "QmmError", "lib",
     "num_sms", "LIB_PATH",
 ]

@@ -447,7 +447,36 @@ __global__ void __launch_bounds__(256) acc_only_kernel(const int* __restrict__ a
   }
 }
 
+// colsum[c] += the sum of rows [r0, r0 + 64) of column c (one thread per column).
+template <bool U>
+__global__ void __launch_bounds__(256) colsum_kernel(const uint8_t* __restrict__ src, int rows, int cols,
+                                                     int* __restrict__ colsum) {
+  const int c = blockIdx.x * 256 + threadIdx.x;
+  if (c >= cols) return;
+  const int r0 = blockIdx.y * 64, r1 = min(rows, r0 + 64);
+  int acc = 0;
+#pragma unroll 8
+  for (int r = r0; r < r1; ++r) {
+    const uint32_t v = __ldg(src + (long long)r * cols + c);
+    acc += U ? (int)v : (int)(int8_t)(uint8_t)v;
+  }
+  atomicAdd(colsum + c, acc);
+}
+
 }  // namespace conv
+
+cudaError_t launch_colsum(const void* src, bool u8, int rows, int cols, int* colsum, cudaStream_t s) {
+  using namespace conv;
+  if (cols <= 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(colsum, 0, sizeof(int) * (size_t)cols, s);
+  if (e != cudaSuccess || rows <= 0) return e;
+  if ((rows + 63) / 64 > 65535) return cudaErrorInvalidValue;
+  const dim3 grid((unsigned)((cols + 255) / 256), (unsigned)((rows + 63) / 64));
+  const uint8_t* p = static_cast<const uint8_t*>(src);
+  if (u8) colsum_kernel<true><<<grid, 256, 0, s>>>(p, rows, cols, colsum);
+  else colsum_kernel<false><<<grid, 256, 0, s>>>(p, rows, cols, colsum);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_convert_planes(const ConvPlane& a, bool au, const ConvPlane& b, bool bu, cudaStream_t s) {
   using namespace conv;

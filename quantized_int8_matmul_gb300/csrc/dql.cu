@@ -271,6 +271,69 @@ __global__ void __launch_bounds__(THREADS) dql_quantize_rows_kernel(const float*
   }
 }
 
+// The same row quantization written as exact fp16 values (0..255) into an
+// operand copy whose rows are `pitch` elements apart, with each row's sum of
+// y: the A operand of a following MatMulInteger GEMM, without the uint8 tensor
+// in between.
+__global__ void __launch_bounds__(THREADS) dql_quantize_rows_f16_kernel(const float* __restrict__ x, long long rows,
+                                                                        long long row_len, int vec,
+                                                                        const float* __restrict__ partials,
+                                                                        int num_partials, __half* __restrict__ y16,
+                                                                        long long pitch, float* y_scale,
+                                                                        uint8_t* y_zp,
+                                                                        int32_t* __restrict__ row_sums) {
+  const ScaleZp sz = reduce_partials(partials, num_partials);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    *y_scale = sz.scale;
+    *y_zp = (uint8_t)(int)sz.zp;
+  }
+  const int zp = (int)sz.zp;
+  const float rcp = safe_recip(sz.scale);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long total_warps = (long long)gridDim.x * (THREADS / 32);
+  for (long long wr = (long long)(gridDim.x - 1 - blockIdx.x) * (THREADS / 32) + warp; wr < rows;
+       wr += total_warps) {
+    const float* xr = x + wr * row_len;
+    __half* yr = y16 + wr * pitch;
+    int s = 0;
+    if (vec) {   // x rows 16-byte aligned, row_len % 4 == 0: 4 values -> one 8-byte store
+      const float4* x4 = reinterpret_cast<const float4*>(xr);
+      uint2* y4 = reinterpret_cast<uint2*>(yr);
+      const long long r4 = row_len / 4;
+      long long i = lane;
+      for (; i + (UNROLL - 1) * 32 < r4; i += UNROLL * 32) {
+        float4 v[UNROLL];
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) v[u] = __ldg(x4 + i + u * 32);
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+          const uint32_t w = quant4(v[u], sz.scale, rcp, zp);
+          uint2 h;
+          bytes_to_half4<true>(w, h.x, h.y);
+          y4[i + u * 32] = h;
+          s += (int)__dp4a(w, 0x01010101u, 0u);
+        }
+      }
+      for (; i < r4; i += 32) {
+        const uint32_t w = quant4(__ldg(x4 + i), sz.scale, rcp, zp);
+        uint2 h;
+        bytes_to_half4<true>(w, h.x, h.y);
+        y4[i] = h;
+        s += (int)__dp4a(w, 0x01010101u, 0u);
+      }
+    } else {
+      for (long long i = lane; i < row_len; i += 32) {
+        const uint32_t q = quant1(__ldg(xr + i), sz.scale, zp);
+        yr[i] = __int2half_rn((int)q);   // 0..255: exact
+        s += (int)q;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    if (lane == 0) row_sums[wr] = s;
+  }
+}
+
 }  // namespace dql
 
 int dql_num_partials(long long n) {
@@ -301,6 +364,28 @@ cudaError_t launch_dql(const float* x, long long n, uint8_t* y, float* y_scale, 
     dql_quantize_kernel<<<num_partials, THREADS, 0, s>>>(x, n, vec, partials, num_partials, num_partials, y,
                                                           y_scale, y_zp);
   }
+  return cudaGetLastError();
+}
+
+}  // namespace qmm
+
+namespace qmm {
+
+cudaError_t launch_dql_rows_f16(const float* x, long long rows, long long row_len, __half* y16, long long pitch,
+                                float* y_scale, uint8_t* y_zp, int32_t* row_sums, float* partials,
+                                int num_partials, cudaStream_t s) {
+  using namespace dql;
+  if (rows <= 0 || row_len <= 0) return cudaSuccess;
+  dql_minmax_kernel<<<num_partials, THREADS, 0, s>>>(x, rows * row_len, reinterpret_cast<uintptr_t>(x) % 16 == 0,
+                                                     partials);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int vec = (reinterpret_cast<uintptr_t>(x) % 16 == 0) && (row_len % 4 == 0) && (pitch % 4 == 0) &&
+                  (reinterpret_cast<uintptr_t>(y16) % 8 == 0);
+  const long long want = (rows + (THREADS / 32) - 1) / (THREADS / 32);
+  const int grid = (int)std::max<long long>(1, std::min<long long>(want, 8LL * num_sms()));
+  dql_quantize_rows_f16_kernel<<<grid, THREADS, 0, s>>>(x, rows, row_len, vec, partials, num_partials, y16, pitch,
+                                                         y_scale, y_zp, row_sums);
   return cudaGetLastError();
 }
 

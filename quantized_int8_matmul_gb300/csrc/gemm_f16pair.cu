@@ -69,6 +69,9 @@ struct Shared {
   // A8W8 weight_scale (float bits) / MatMulInteger b_zp, and colsum(B)
   uint32_t col_op[NEW][CPW_MAX];
   int col_sum[NEW][CPW_MAX];
+  // MatMulInteger with dequantisation: the per-column multiplier and bias
+  float col_scale[NEW][CPW_MAX];
+  float col_bias[NEW][CPW_MAX];
 };
 
 constexpr size_t SMEM_BYTES = (size_t)NS * STAGE_BYTES + sizeof(Shared) + 1024;
@@ -109,10 +112,11 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
 
 // Per-tile operands of this warp's CPW columns, staged in shared memory by
 // the warp itself.
-template <int CPW, bool BU, bool MMI, bool FA, bool ACC = false>
+template <int CPW, bool BU, bool MMI, bool FA, bool ACC = false, bool DQ = false>
 __device__ __forceinline__ void stage_columns(const GemmF16Args& p, Shared& sm, const TileCoord tc, int warp, int h,
                                               int lane) {
   const int* colsum = (MMI && p.a_zp_count > 0) ? p.colsum + (p.b_bstride ? (size_t)tc.b * p.N : 0) : nullptr;
+  const float ys = DQ ? __ldg(p.act_scale) : 0.f;
   for (int col = lane; col < CPW; col += 32) {
     const int n = tc.n0 + h * CPW + col;
     uint32_t op = 0u;
@@ -133,6 +137,10 @@ __device__ __forceinline__ void stage_columns(const GemmF16Args& p, Shared& sm, 
     }
     sm.col_op[warp][col] = op;
     sm.col_sum[warp][col] = cs;
+    if (DQ) {
+      sm.col_scale[warp][col] = n < p.N ? __fmul_rn(ys, __ldg(p.w_scale + (p.w_count == 1 ? 0 : n))) : 0.f;
+      sm.col_bias[warp][col] = (n < p.N && p.bias) ? __ldg(p.bias + n) : 0.f;
+    }
   }
   __syncwarp();
 }
@@ -142,7 +150,7 @@ __device__ __forceinline__ void stage_columns(const GemmF16Args& p, Shared& sm, 
 // store the combined int32 sums to acc_out) or apply the zero-point expansion
 // (MatMulInteger), store C. c_vec bit 0: C rows take 16-byte vectors; bit 1:
 // so do acc_in / acc_out rows.
-template <int CPW, bool AU, bool BU, bool MMI, bool FA, bool ACC = false>
+template <int CPW, bool AU, bool BU, bool MMI, bool FA, bool ACC = false, bool DQ = false>
 __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm, uint32_t (&sums)[CPW],
                                          const TileCoord tc, int warp, int q, int h, int lane, int c_vec) {
   const int row = tc.m0 + q * 32 + lane;
@@ -265,6 +273,11 @@ __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm,
         const uint32_t zb = sm.col_op[warp][g * 16 + i];
         const uint32_t cs = (uint32_t)sm.col_sum[warp][g * 16 + i];
         o[i] = o[i] - za * cs - zb * rs + kzz * zb;
+        if (DQ) {   // cast, one multiply by y_scale * w_scale[n], then the bias
+          float v = __fmul_rn(__int2float_rn((int)o[i]), sm.col_scale[warp][g * 16 + i]);
+          if (p.bias) v = __fadd_rn(v, sm.col_bias[warp][g * 16 + i]);
+          o[i] = __float_as_uint(v);
+        }
       }
       int32_t* out = reinterpret_cast<int32_t*>(p.C) + crow + nb;
       if (full) {
@@ -307,7 +320,7 @@ __device__ __forceinline__ void preload_acc(const GemmF16Args& p, const TileCoor
   }
 }
 
-template <int BN, bool AU, bool BU, bool MMI, bool FA, bool ACC>
+template <int BN, bool AU, bool BU, bool MMI, bool FA, bool ACC, bool DQ>
 __global__ void __launch_bounds__(NT, 1)
     gemm_f16pair_kernel(const GemmF16Args p, const int cs, const int c_vec, const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB) {
@@ -443,7 +456,7 @@ __global__ void __launch_bounds__(NT, 1)
     uint32_t sums[CPW];
     int tl = 0, c = 0;
     TileCoord tc = tile_coord<BN>(p, 0, cid, ncl, (int)rank);
-    if (my_tiles > 0) stage_columns<CPW, BU, MMI, FA, ACC>(p, sm, tc, warp, h, lane);
+    if (my_tiles > 0) stage_columns<CPW, BU, MMI, FA, ACC, DQ>(p, sm, tc, warp, h, lane);
     for (int d = 0; d < total_chunks; ++d) {
       const int ab = d & 1;
       if (ACC && c == 0) preload_acc<CPW>(p, tc, q, h, lane, sums, c_vec);
@@ -470,11 +483,11 @@ __global__ void __launch_bounds__(NT, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_remote_cta(acc_empty_leader0 + (uint32_t)ab * 8u);
       if (c == cpt - 1) {
-        epilogue<CPW, AU, BU, MMI, FA, ACC>(p, sm, sums, tc, warp, q, h, lane, c_vec);
+        epilogue<CPW, AU, BU, MMI, FA, ACC, DQ>(p, sm, sums, tc, warp, q, h, lane, c_vec);
         __syncwarp();   // the warp's staged operands are read: restage for the next tile
         if (tl + 1 < my_tiles)
-          stage_columns<CPW, BU, MMI, FA, ACC>(p, sm, tile_coord<BN>(p, tl + 1, cid, ncl, (int)rank), warp, h,
-                                               lane);
+          stage_columns<CPW, BU, MMI, FA, ACC, DQ>(p, sm, tile_coord<BN>(p, tl + 1, cid, ncl, (int)rank), warp,
+                                                   h, lane);
       }
       if (++c == cpt) {
         c = 0;
@@ -509,10 +522,10 @@ struct DeviceLaunchInfo {
   int max_clusters = 0;
 };
 
-template <int BN, bool AU, bool BU, bool MMI, bool FA = false, bool ACC = false>
+template <int BN, bool AU, bool BU, bool MMI, bool FA = false, bool ACC = false, bool DQ = false>
 cudaError_t launch_one(const GemmF16Args& a, int cs, int c_vec, const CUtensorMap& ta, const CUtensorMap& tb,
                        cudaStream_t s) {
-  auto kern = gemm_f16pair_kernel<BN, AU, BU, MMI, FA, ACC>;
+  auto kern = gemm_f16pair_kernel<BN, AU, BU, MMI, FA, ACC, DQ>;
   static std::mutex mu;
   static DeviceLaunchInfo info[64];
   int dev = 0;
@@ -601,6 +614,11 @@ cudaError_t dispatch(const GemmF16Args& a, bool a_u8, bool b_u8, bool mmi, int c
     if (a.acc_in || a.acc_out || !a.C) return launch_one<224, false, false, false, false, true>(a, cs, c_vec, ta, tb, s);
     return launch_one<BN, false, false, false>(a, cs, c_vec, ta, tb, s);
   }
+  if (a.act_scale) {   // dequantising MatMulInteger: A is the quantised activation (uint8); 224 columns
+    if (!a_u8) return cudaErrorInvalidValue;   // fit the extra epilogue operands without spilling
+    if (b_u8) return launch_one<224, true, true, true, false, false, true>(a, cs, c_vec, ta, tb, s);
+    return launch_one<224, true, false, true, false, false, true>(a, cs, c_vec, ta, tb, s);
+  }
   if (!a_u8 && !b_u8) return launch_one<BN, false, false, true>(a, cs, c_vec, ta, tb, s);
   if (a_u8 && !b_u8) return launch_one<BN, true, false, true>(a, cs, c_vec, ta, tb, s);
   if (!a_u8 && b_u8) return launch_one<BN, false, true, true>(a, cs, c_vec, ta, tb, s);
@@ -620,7 +638,8 @@ cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool
   CUtensorMap ta{}, tb{};
   cudaError_t e = make_maps(a, &ta, &tb);
   if (e != cudaSuccess) return e;
-  *kernel_name = mmi ? "gemm_tc05_pair_f16ops_matmul_integer"
+  *kernel_name = mmi ? (a.act_scale ? "gemm_tc05_pair_f16ops_matmul_integer_dequant"
+                           : "gemm_tc05_pair_f16ops_matmul_integer")
                      : ((a.acc_in || a.acc_out || !a.C) ? "gemm_tc05_pair_f16ops_a8w8_acc" : "gemm_tc05_pair_f16ops_a8w8");
   if (choose_tile_width(a) == 224) return dispatch<224>(a, a_u8, b_u8, mmi, cs, c_vec, ta, tb, s);
   return dispatch<256>(a, a_u8, b_u8, mmi, cs, c_vec, ta, tb, s);

@@ -68,6 +68,9 @@ struct GemmF16Args {
   // acc_out is written (act_scale / w_scale unused)
   const int* acc_in;
   int* acc_out;
+  // MatMulInteger followed by the dequantisation of a DynamicQuantizeLinear
+  // chain (f32 out): C = f32(f32(acc) * f32(act_scale[0] * w_scale[n])) (+ bias[n])
+  const float* bias;
   // A's batch index is b % a_bmod when a_bmod > 0 (a weight shared by every
   // image, one slice per convolution group); per-row zero points and row sums
   // are then indexed (b % a_bmod) * M + row
@@ -105,6 +108,14 @@ cudaError_t launch_convert_planes(const ConvPlane& a, bool au, const ConvPlane& 
 // C = out(f32(acc) * act_scale[m] * w_scale[n]) where C is given.
 cudaError_t launch_acc_only(const int* acc_in, int* acc_out, int M, int N, const float* act_scale, int act_count,
                             const float* w_scale, int w_count, void* C, int c_f32, cudaStream_t s);
+
+// DynamicQuantizeLinear of `rows` rows of `row_len` floats into exact fp16 rows
+// at `pitch` (the A operand of the following GEMM) with the rows' sums of y.
+cudaError_t launch_dql_rows_f16(const float* x, long long rows, long long row_len, __half* y16, long long pitch,
+                                float* y_scale, uint8_t* y_zp, int32_t* row_sums, float* partials,
+                                int num_partials, cudaStream_t s);
+// colsum[c] = sum over the rows of an 8-bit [rows][cols] matrix (dense; zeroed here).
+cudaError_t launch_colsum(const void* src, bool u8, int rows, int cols, int* colsum, cudaStream_t s);
 
 // ConvInteger pre-pass (conv.cu). im2col of an 8-bit NCHW input into fp16
 // col[n][k][p] (k = (c*kH + kh)*kW + kw over all C input channels, p = oh*oW +

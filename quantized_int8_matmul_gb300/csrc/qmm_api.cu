@@ -248,6 +248,26 @@ ConvPlan conv_plan(int64_t N, int64_t C, int64_t H, int64_t W, int64_t M, int64_
   pl.ok = true;
   return pl;
 }
+// The DynamicQuantizeLinear -> MatMulInteger -> dequantise chain. Workspace:
+// [DQL partials][A16: M x Kp fp16][B16: K x Np fp16][rowsum(y): M int32]
+// [colsum(W): N int32][y_scale: f32, y_zp: u8], Kp and Np rounded up to 8.
+struct DqmPlan {
+  int64_t Kp = 0, Np = 0;
+  size_t off_a = 0, off_b = 0, off_rs = 0, off_cs = 0, off_sz = 0, bytes = 0;
+};
+
+DqmPlan dqm_plan(int64_t M, int64_t K, int64_t N) {
+  DqmPlan pl;
+  pl.Kp = (K + 7) / 8 * 8;
+  pl.Np = (N + 7) / 8 * 8;
+  pl.off_a = round256(dynamic_quantize_linear_workspace_bytes(M * K));
+  pl.off_b = pl.off_a + round256((size_t)M * pl.Kp * 2);
+  pl.off_rs = pl.off_b + round256((size_t)K * pl.Np * 2);
+  pl.off_cs = pl.off_rs + round256((size_t)M * 4);
+  pl.off_sz = pl.off_cs + round256((size_t)N * 4);
+  pl.bytes = pl.off_sz + 256;
+  return pl;
+}
 }  // namespace
 
 int num_sms() {
@@ -802,6 +822,83 @@ qmm_status conv_integer(const void* x, int x_dtype, const void* w, int w_dtype, 
   const char* gname = "none";
   if (e == cudaSuccess) e = launch_gemm_f16pair(f, wu, xu, true, chunk_k_for(wu, xu), s, &gname);
   return finish_launch(e, "im2col_f16+gemm_tc05_pair_f16ops_matmul_integer");
+}
+
+size_t dynamic_quantize_matmul_workspace_bytes(int64_t M, int64_t K, int64_t N) {
+  if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N) || M == 0 || K == 0 || N == 0) return 0;
+  return dqm_plan(M, K, N).bytes;
+}
+
+qmm_status dynamic_quantize_matmul(const float* x, int64_t M, int64_t K, const void* W, int w_dtype, int64_t N,
+                                   const float* w_scale, int64_t w_scale_count, const void* w_zero_point,
+                                   int64_t w_zp_count, const float* bias, float* C, float* y_scale,
+                                   uint8_t* y_zero_point, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return QMM_ERR_INVALID_ARG;
+  if (w_dtype != QMM_S8 && w_dtype != QMM_U8) return QMM_ERR_INVALID_ARG;
+  if (w_scale_count != 1 && w_scale_count != N) return QMM_ERR_INVALID_ARG;
+  if (w_zp_count != 0 && w_zp_count != 1 && w_zp_count != N) return QMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) {
+    t_last_kernel = "none";
+    return QMM_OK;
+  }
+  if (K == 0) return QMM_ERR_UNSUPPORTED;
+  if (!x || !W || !w_scale || !C || (w_zp_count > 0 && !w_zero_point)) return QMM_ERR_INVALID_ARG;
+  const DqmPlan pl = dqm_plan(M, K, N);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < pl.bytes) return QMM_ERR_INVALID_ARG;
+  if (((M + 255) / 256) * ((N + 223) / 224) > (int64_t)INT_MAX || M * K / 32768 > (int64_t)INT_MAX)
+    return QMM_ERR_UNSUPPORTED;
+  unsigned* err = err_word();
+  if (!err) return QMM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  const bool wu = w_dtype == QMM_U8;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  __half* a16 = reinterpret_cast<__half*>(base + pl.off_a);
+  __half* b16 = reinterpret_cast<__half*>(base + pl.off_b);
+  int* rs = reinterpret_cast<int*>(base + pl.off_rs);
+  int* cs = reinterpret_cast<int*>(base + pl.off_cs);
+  float* ys = y_scale ? y_scale : reinterpret_cast<float*>(base + pl.off_sz);
+  uint8_t* yz = y_zero_point ? y_zero_point : base + pl.off_sz + 16;
+  // the weight: exact fp16 copy and column sums (the y_zp term)
+  cudaError_t e;
+  if (N % 16 == 0 && aligned16(W)) {
+    e = launch_convert_cols(W, wu, b16, 1, (int)K, (int)N, cs, s);
+  } else {
+    const ConvPlane none{nullptr, 0, 0, 0, 0, nullptr, 0};
+    const ConvPlane pb{W, N, (int)K, (int)N, 0, b16, pl.Np};
+    e = launch_convert_planes(none, false, pb, wu, s);
+    if (e == cudaSuccess) e = launch_colsum(W, wu, (int)K, (int)N, cs, s);
+  }
+  // the activations: DynamicQuantizeLinear straight into the fp16 operand, with rowsum(y)
+  if (e == cudaSuccess)
+    e = launch_dql_rows_f16(x, M, K, a16, pl.Kp, ys, yz, rs, reinterpret_cast<float*>(base),
+                            dql_num_partials(M * K), s);
+  GemmF16Args f{};
+  f.A16 = a16;
+  f.B16 = b16;
+  f.a_pitch = (int)pl.Kp;
+  f.b_pitch = (int)pl.Np;
+  f.batch = 1;
+  f.M = (int)M;
+  f.K = (int)K;
+  f.N = (int)N;
+  f.C = C;
+  f.a_zp = yz;
+  f.a_zp_count = 1;
+  f.b_zp = w_zero_point;
+  f.b_zp_count = (int)w_zp_count;
+  f.rowsum = rs;
+  f.colsum = cs;
+  f.act_scale = ys;
+  f.act_count = 1;
+  f.w_scale = w_scale;
+  f.w_count = (int)w_scale_count;
+  f.bias = bias;
+  f.zp_row_mod = (int)M;
+  f.err = err;
+  const char* gname = "none";
+  if (e == cudaSuccess) e = launch_gemm_f16pair(f, true, wu, true, chunk_k_for(true, wu), s, &gname);
+  return finish_launch(e, "dql_f16+gemm_tc05_pair_f16ops_matmul_integer_dequant");
 }
 
 size_t dynamic_quantize_linear_workspace_bytes(int64_t n) {

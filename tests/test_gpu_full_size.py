@@ -45,6 +45,21 @@ def test_a8w8_4096(workspace, kernel):
     assert_equal(got[rows], want, "a8w8 4096^3 sampled rows")
 
 
+def test_dynamic_quantize_matmul_8192x4096x11008():
+    w = W.dql_matmul_integer_8192x4096x11008()
+    rng = np.random.default_rng(9)
+    w_scale = rng.uniform(0.001, 0.01, 11008).astype(np.float32)
+    bias = rng.standard_normal(11008).astype(np.float32)
+    C, ys, yz = q.dynamic_quantize_matmul(dev(w.x), dev(w.B), dev(w_scale), dev(w.b_zp), dev(bias))
+    q.check_device_error()
+    assert q.last_kernel() == "dql_f16+gemm_tc05_pair_f16ops_matmul_integer_dequant"
+    rows = sample(8192, 24, 5)
+    rows[:2] = [0, 8191]
+    want, wys, wyz = O.dynamic_quantize_matmul(w.x, w.B, w_scale, w.b_zp, bias, rows=rows)
+    assert float(ys.item()) == float(wys) and int(yz.item()) == int(wyz)
+    assert_equal(host(C)[rows], want, "fused chain 8192x4096x11008, sampled rows")
+
+
 @pytest.mark.parametrize("case", ["conv2d_3x3_8x256x56x56", "conv1d_k3_4x512x3000"])
 def test_conv_integer_full_size(case):
     c = getattr(W, case)()
