@@ -496,7 +496,7 @@ def case_setups(q, torch, peaks):
                 return {"us": ms * 1e3, "value": tops, "unit": "TOPS", "frac_tensor": tops / tc, "gbs": gbs,
                         "frac_hbm": gbs / hbm, "algorithmic_bytes": nbytes,
                         "note": f"int32 acc_in + A @ B, {'B stored [N,K] (b_trans)' if b_trans else 'B [K,N]'}, "
-                                "bf16 out; pre-pass + SM-pair GEMM"}
+                                "bf16 out"}
             call = lambda: q.qmm_a8w8_acc(A, B, a_s, w_s, acc_in=acc, b_trans=b_trans, out=C,  # noqa: E731
                                           workspace=wsa)
             return call, Ma * Ka + Ka * Na < 2 * FLUSH_BYTES // 3, report
@@ -558,6 +558,8 @@ def case_setups(q, torch, peaks):
             "a8w8_acc_4096x4096x4096_bf16": a8w8_acc(4096, 4096, 4096, False),
             "a8w8_acc_4096x4096x4096_bf16_b_trans": a8w8_acc(4096, 4096, 4096, True),
             "a8w8_acc_decode_M1_8192x28672_b_trans": a8w8_acc(1, 8192, 28672, True),
+            "a8w8_acc_decode_M1_8192x28672": a8w8_acc(1, 8192, 28672, False),
+            "a8w8_acc_decode_M16_8192x28672_b_trans": a8w8_acc(16, 8192, 28672, True),
             "dql_matmul_dequant_fused_8192x4096x11008": dq_chain,
             "conv_integer_3x3_8x256x56x56": conv(W.conv2d_3x3_8x256x56x56),
             "conv_integer_1d_k3_4x512x3000": conv(W.conv1d_k3_4x512x3000)}
@@ -567,6 +569,7 @@ SECONDARY = ["a8w8_4096x4096x4096_bf16_single_pass", "decode_gemv_M1", "decode_g
              "matmul_integer_8192x4096x11008", "batched_matmul_integer_65536x1024x1024",
              "w8_prefill_bf16_4096x8192x28672", "w8_dequant_f32_64x256x192", "a8w8_acc_4096x4096x4096_bf16",
              "a8w8_acc_4096x4096x4096_bf16_b_trans", "a8w8_acc_decode_M1_8192x28672_b_trans",
+             "a8w8_acc_decode_M1_8192x28672", "a8w8_acc_decode_M16_8192x28672_b_trans",
              "conv_integer_3x3_8x256x56x56", "conv_integer_1d_k3_4x512x3000",
              "dql_matmul_dequant_fused_8192x4096x11008"]
 

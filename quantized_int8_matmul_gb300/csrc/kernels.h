@@ -172,6 +172,24 @@ bool gemv_supported(long long M, long long K, long long N, const void* A, const 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, const char** kernel_name);
 
 // ---------------------------------------------------------------------------
+// Decode-shaped accumulating A8W8 (M <= 16), dp4a on the CUDA cores.
+// ---------------------------------------------------------------------------
+struct GemvAccArgs {
+  const int8_t* A;             // [M][K] (after the a_trans copy)
+  const int8_t* B;             // [N][K] (b_trans) or [K][N]
+  int M, K, N;
+  const int* acc_in;           // [M][N] or null
+  int* acc_out;                // [M][N] or null
+  const float* act_scale; int act_count;
+  const float* w_scale; int w_count;
+  void* C; int c_f32;          // [M][N] or null
+};
+bool gemv_acc_supported(long long M, long long K, long long N, int b_trans, const void* A, const void* B);
+size_t gemv_acc_workspace_bytes(long long M, long long K, long long N);
+cudaError_t launch_gemv_acc(GemvAccArgs p, int a_trans, int b_trans, void* ws, cudaStream_t s,
+                            const char** kernel_name);
+
+// ---------------------------------------------------------------------------
 // Generic CUDA-core form (a): float A (f32 or bf16) x int8 B, any shape.
 // ---------------------------------------------------------------------------
 struct W8SimtArgs {

@@ -8,6 +8,7 @@
 #include "kernels.h"
 #include "../../include/qmm.h"
 
+#include <algorithm>
 #include <climits>
 #include <cstdlib>
 #include <cstring>
@@ -670,7 +671,9 @@ qmm_status qmm_a8w8_packed(int64_t M, int64_t K, int64_t N, const float* act_sca
 
 size_t qmm_a8w8_acc_workspace_bytes(int64_t M, int64_t K, int64_t N) {
   if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return 0;
-  return acc_plan(M, K, N).bytes;
+  const size_t general = acc_plan(M, K, N).bytes;
+  if (M < 1 || M > 16 || K < 1 || N < 1) return general;
+  return std::max(general, gemv_acc_workspace_bytes(M, K, N));   // the decode path's needs
 }
 
 qmm_status qmm_a8w8_acc(const int8_t* A, int a_trans, const int8_t* B, int b_trans, int64_t M, int64_t K, int64_t N,
@@ -700,7 +703,27 @@ qmm_status qmm_a8w8_acc(const int8_t* A, int a_trans, const int8_t* B, int b_tra
                                          (int)w_count, C, c_f32, s),
                          "acc_passthrough");
   const AccPlan pl = acc_plan(M, K, N);
-  if (!workspace || !aligned16(workspace) || workspace_bytes < pl.bytes) return QMM_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < qmm_a8w8_acc_workspace_bytes(M, K, N))
+    return QMM_ERR_INVALID_ARG;
+  // decode shapes (PyPTO PR #1920's gemv_acc for a logical M of 1): a weight-streaming dp4a kernel
+  if (gemv_acc_supported(M, K, N, b_trans, A, B)) {
+    GemvAccArgs g{};
+    g.A = A;
+    g.B = B;
+    g.M = (int)M;
+    g.K = (int)K;
+    g.N = (int)N;
+    g.acc_in = acc_in;
+    g.acc_out = acc_out;
+    g.act_scale = act_scale;
+    g.act_count = (int)act_count;
+    g.w_scale = weight_scale;
+    g.w_count = (int)w_count;
+    g.C = C;
+    g.c_f32 = c_f32;
+    const char* name = "none";
+    return finish_launch(launch_gemv_acc(g, a_trans, b_trans, workspace, s, &name), name);
+  }
   unsigned* err = err_word();
   if (!err) return QMM_ERR_CUDA;
   uint8_t* base = static_cast<uint8_t*>(workspace);

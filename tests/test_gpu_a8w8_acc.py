@@ -18,6 +18,13 @@ q = pytest.importorskip("quantized_int8_matmul_gb300")
 KERNEL = "f16_prepass+gemm_tc05_pair_f16ops_a8w8_acc"
 
 
+def expected_kernel(M, K, N, b_trans):
+    """Decode shapes (M <= 16) whose rows suit the weight-streaming kernels take them."""
+    if 1 <= M <= 16 and (K % 16 == 0 if b_trans else (K % 4 == 0 and N % 4 == 0)):
+        return "gemv_acc_a8w8_kmajor" if b_trans else "gemv_acc_a8w8_nmajor"
+    return KERNEL
+
+
 def logical(w):
     A = w.A.T if w.a_trans else w.A
     B = w.B.T if w.b_trans else w.B
@@ -50,7 +57,7 @@ def test_acc_matches_oracle(M, K, N, a_trans, b_trans):
     A, B = logical(w)
     for out in ("f32", "bf16"):
         C, acc = run(w, out)
-        assert q.last_kernel() == KERNEL
+        assert q.last_kernel() == expected_kernel(M, K, N, b_trans)
         tag = f"{M}x{K}x{N} a_trans={a_trans} b_trans={b_trans} {out}"
         assert_equal(C, O.a8w8_dequant_acc(w.acc_in, A, B, w.act_scale, w.weight_scale, out), tag)
         assert_equal(acc, want_acc(w.acc_in, A, B), "acc_out " + tag)
@@ -148,3 +155,42 @@ def test_argument_errors():
     small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
     with pytest.raises(q.QmmError):
         q.qmm_a8w8_acc(A, B, torch.ones(1, device="cuda"), torch.ones(1, device="cuda"), workspace=small)
+
+
+DECODE = [(1, 64, 256), (1, 4096, 1000), (2, 1040, 132), (5, 2048, 4), (8, 512, 520), (16, 1024, 264),
+          (1, 8192, 4100)]
+
+
+@pytest.mark.parametrize("M,K,N", DECODE)
+@pytest.mark.parametrize("a_trans,b_trans", [(False, False), (True, False), (False, True), (True, True)])
+def test_decode_shapes_match_oracle(M, K, N, a_trans, b_trans):
+    w = W.a8w8_acc(M, K, N, seed=7 * M + K + N, a_trans=a_trans, b_trans=b_trans)
+    A, B = logical(w)
+    C, acc = run(w, "bf16")
+    assert q.last_kernel() == expected_kernel(M, K, N, b_trans)
+    tag = f"decode {M}x{K}x{N} a_trans={a_trans} b_trans={b_trans}"
+    assert_equal(acc, want_acc(w.acc_in, A, B), "acc_out " + tag)
+    assert_equal(C, O.a8w8_dequant_acc(w.acc_in, A, B, w.act_scale, w.weight_scale, "bf16"), tag)
+
+
+@pytest.mark.parametrize("b_trans", [False, True])
+def test_decode_wraps_and_optional_operands(b_trans):
+    """Extremes and int32-spanning accumulators (sums wrap); no acc_in; acc_out only."""
+    M, K, N = 3, 8192, 512
+    w = W.a8w8_acc(M, K, N, seed=4, b_trans=b_trans, acc_bound=2**31)
+    w.A[...] = -128
+    w.B[...] = -128
+    A, B = logical(w)
+    C, acc = run(w, "f32")
+    assert q.last_kernel() == expected_kernel(M, K, N, b_trans)
+    wide = w.acc_in.astype(np.int64) + O.a8w8_acc(A, B).astype(np.int64)
+    assert (wide != want_acc(w.acc_in, A, B)).any(), "the case must wrap"
+    assert_equal(acc, want_acc(w.acc_in, A, B), "wrapped decode accumulator")
+    assert_equal(C, O.a8w8_dequant_acc(w.acc_in, A, B, w.act_scale, w.weight_scale, "f32"), "wrapped decode")
+    C2, acc2 = run(w, "f32", with_acc_in=False)
+    assert_equal(acc2, O.a8w8_acc(A, B), "decode without acc_in")
+    acc3 = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    assert q.qmm_a8w8_acc(dev(w.A), dev(w.B), acc_in=dev(w.acc_in), acc_out=acc3, b_trans=b_trans,
+                          out_dtype=None) is None
+    q.check_device_error()
+    assert_equal(host(acc3), want_acc(w.acc_in, A, B), "decode, acc_out only")

@@ -45,6 +45,18 @@ def test_a8w8_4096(workspace, kernel):
     assert_equal(got[rows], want, "a8w8 4096^3 sampled rows")
 
 
+@pytest.mark.parametrize("b_trans", [False, True])
+def test_a8w8_acc_decode_M1_8192x28672(b_trans):
+    w = W.a8w8_acc(1, 8192, 28672, seed=0, b_trans=b_trans)
+    C = q.qmm_a8w8_acc(dev(w.A), dev(w.B), dev(w.act_scale), dev(w.weight_scale), acc_in=dev(w.acc_in),
+                       b_trans=b_trans, out_dtype=torch.bfloat16)
+    q.check_device_error()
+    assert q.last_kernel() == ("gemv_acc_a8w8_kmajor" if b_trans else "gemv_acc_a8w8_nmajor")
+    B = np.ascontiguousarray(w.B.T) if b_trans else w.B
+    want = O.a8w8_dequant_acc(w.acc_in, w.A, B, w.act_scale, w.weight_scale, "bf16")
+    assert_equal(host(C), want, "decode accumulating A8W8, M = 1")
+
+
 def test_dynamic_quantize_matmul_8192x4096x11008():
     w = W.dql_matmul_integer_8192x4096x11008()
     rng = np.random.default_rng(9)
