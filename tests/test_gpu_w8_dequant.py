@@ -13,9 +13,9 @@ pytestmark = pytest.mark.gpu
 q = pytest.importorskip("quantized_int8_matmul_gb300")
 
 
-def check(A_dev, A_vals, B, scale, zp, out, kernel):
+def check(A_dev, A_vals, B, scale, zp, out, kernel, workspace=None):
     zp_dev = None if zp is None else dev(zp.astype(np.int32))
-    C = q.qmm_w8_dequant(A_dev, dev(B), dev(scale), zp_dev, out_dtype=out, workspace=None)
+    C = q.qmm_w8_dequant(A_dev, dev(B), dev(scale), zp_dev, out_dtype=out, workspace=workspace)
     torch.cuda.synchronize()
     assert q.last_kernel() == kernel
     got = host(C)
@@ -62,3 +62,39 @@ def test_decode_shapes_outside_gemv_fall_back_to_cuda_cores(M, K, N):
 def test_gemv_ragged_k_and_scalar_scale():
     w = W.decode_gemv(3, K=1000, N=384, seed=9)
     check(bf16_dev(w.A_bits), w.A, w.W, w.scale[:1].copy(), None, torch.float32, "gemv_w8_bf16_tma")
+
+
+SIMT = "gemv_w8_simt_f32x2"
+
+
+@pytest.mark.parametrize("M", [1])
+@pytest.mark.parametrize("zp", [None, "tensor", "column"])
+@pytest.mark.parametrize("out", [torch.bfloat16, torch.float32])
+def test_decode_simt_bf16(M, zp, out):
+    """With a workspace, a single activation row takes the CUDA-core weight-streaming kernel."""
+    w = W.decode_gemv(M, K=1024, N=640, seed=M + 11)
+    rng = np.random.default_rng(M)
+    z = None if zp is None else (np.array([-4], np.int32) if zp == "tensor" else rng.integers(-9, 9, 640).astype(np.int32))
+    check(bf16_dev(w.A_bits), w.A, w.W, w.scale, z, out, SIMT, workspace="auto")
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 1, 16), (1, 100, 16), (1, 1000, 4096), (1, 4100, 528), (1, 8192, 1040)])
+def test_decode_simt_fp32_activations_and_ragged_k(M, K, N):
+    rng = np.random.default_rng(K + N)
+    A = rng.uniform(-1, 1, (M, K)).astype(np.float32)
+    B = rng.integers(-128, 128, (K, N)).astype(np.int8)
+    scale = rng.uniform(0.001, 0.05, N).astype(np.float32)
+    z = rng.integers(-9, 9, N).astype(np.int32)
+    check(dev(A), A, B, scale, z, torch.float32, SIMT, workspace="auto")
+    check(dev(A), A, B, scale[:1].copy(), None, torch.bfloat16, SIMT, workspace="auto")
+
+
+def test_decode_simt_is_deterministic():
+    w = W.decode_gemv(1, K=4096, N=2048, seed=5)
+    outs = []
+    for _ in range(3):
+        C = q.qmm_w8_dequant(bf16_dev(w.A_bits), dev(w.W), dev(w.scale), None, out_dtype=torch.float32)
+        q.check_device_error()
+        assert q.last_kernel() == SIMT
+        outs.append(host(C))
+    assert all(np.array_equal(outs[0], o) for o in outs[1:])
