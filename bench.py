@@ -394,7 +394,7 @@ def case_setups(q, torch, peaks):
             (lambda ms: {"us": ms * 1e3, "value": OPS / (ms * 1e-3) / 1e12, "unit": "TOPS",
                          "frac": OPS / (ms * 1e-3) / 1e12 / tc, "note": "single-pass fused kernel, no workspace"})
 
-    def gemv(Mg, workspace=True):
+    def gemv(Mg):
         def setup():
             g = W.decode_gemv(Mg)
             Ad = torch.from_numpy(g.A_bits.view(np.int16)).view(torch.bfloat16).cuda()
@@ -407,10 +407,8 @@ def case_setups(q, torch, peaks):
                 gbs = nbytes / (ms * 1e-3) / 1e9
                 return {"us": ms * 1e3, "value": gbs, "unit": "GB/s", "bound": "hbm", "frac": gbs / hbm,
                         "algorithmic_bytes": nbytes}
-            # the weight stream (235 MB) exceeds L2: no flush needed; a preallocated workspace
-            wsg = torch.empty(max(1, q.qmm_w8_dequant_workspace_bytes(torch.bfloat16, Mg, 8192, 28672)),
-                              dtype=torch.uint8, device="cuda") if workspace else None
-            return (lambda: q.qmm_w8_dequant(Ad, Wd, sd, None, out=Cd, workspace=wsg)), False, report
+            # the weight stream (235 MB) exceeds L2: no flush needed
+            return (lambda: q.qmm_w8_dequant(Ad, Wd, sd, None, out=Cd)), False, report
         return setup
 
     def dql():
@@ -555,7 +553,6 @@ def case_setups(q, torch, peaks):
             "a8w8_4096x4096x4096_bf16_single_pass": a8w8_single_pass,
             "w8_prefill_bf16_4096x8192x28672": w8_prefill,
             "decode_gemv_M1": gemv(1), "decode_gemv_M4": gemv(4), "decode_gemv_M16": gemv(16),
-            "decode_gemv_M1_tensor_core": gemv(1, workspace=False),
             "dql_8192x4096": dql, "matmul_integer_8192x4096x11008": mmi,
             "batched_matmul_integer_65536x1024x1024": batched, "w8_dequant_f32_64x256x192": w8,
             "a8w8_acc_4096x4096x4096_bf16": a8w8_acc(4096, 4096, 4096, False),
@@ -569,7 +566,7 @@ def case_setups(q, torch, peaks):
 
 
 SECONDARY = ["a8w8_4096x4096x4096_bf16_single_pass", "decode_gemv_M1", "decode_gemv_M4", "decode_gemv_M16",
-             "decode_gemv_M1_tensor_core", "dql_8192x4096",
+             "dql_8192x4096",
              "matmul_integer_8192x4096x11008", "batched_matmul_integer_65536x1024x1024",
              "w8_prefill_bf16_4096x8192x28672", "w8_dequant_f32_64x256x192", "a8w8_acc_4096x4096x4096_bf16",
              "a8w8_acc_4096x4096x4096_bf16_b_trans", "a8w8_acc_decode_M1_8192x28672_b_trans",

@@ -172,8 +172,9 @@ bool gemv_supported(long long M, long long K, long long N, const void* A, const 
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, const char** kernel_name);
 
 // ---------------------------------------------------------------------------
-// Decode-shaped form (a) for M <= 4 on the CUDA cores (packed fp32 FMAs),
-// split over K into fp32 partials in a workspace.
+// Decode-shaped form (a) for M <= 4 on the CUDA cores: TMA-staged weight,
+// packed fp32 FMAs, CTA pairs splitting K and reducing through distributed
+// shared memory (one launch, no workspace).
 // ---------------------------------------------------------------------------
 struct GemvSimtArgs {
   const void* A; int a_bf16;   // [M][K] bf16 (1) or f32 (0)
@@ -183,9 +184,8 @@ struct GemvSimtArgs {
   const int32_t* zp;  int zp_count;           // 0, 1 or N
   void* C; int c_f32;
 };
-bool gemv_simt_supported(long long M, long long K, long long N, const void* W);
-size_t gemv_simt_workspace_bytes(long long M, long long N);
-cudaError_t launch_gemv_simt(const GemvSimtArgs& p, void* ws, cudaStream_t s, const char** kernel_name);
+bool gemv_simt_supported(long long M, long long K, long long N, int a_bf16, const void* A, const void* W);
+cudaError_t launch_gemv_simt(const GemvSimtArgs& p, unsigned* err, cudaStream_t s, const char** kernel_name);
 
 // ---------------------------------------------------------------------------
 // Decode-shaped accumulating A8W8 (M <= 16), dp4a on the CUDA cores.

@@ -344,6 +344,24 @@ qmm_status qmm_w8_dequant(const void* A, int a_dtype, const int8_t* B, int64_t M
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaGetLastError();
   const char* name = "none";
+  if (gemv_simt_supported(M, K, N, a_dtype == QMM_BF16, A, B)) {   // one to four rows: CUDA cores, CTA pairs
+    GemvSimtArgs g{};
+    g.A = A;
+    g.a_bf16 = a_dtype == QMM_BF16;
+    g.W = B;
+    g.M = (int)M;
+    g.K = (int)K;
+    g.N = (int)N;
+    g.scale = scale;
+    g.scale_count = (int)scale_count;
+    g.zp = zero_point;
+    g.zp_count = (int)zp_count;
+    g.C = C;
+    g.c_f32 = c_dtype == QMM_F32;
+    unsigned* err = err_word();
+    if (!err) return QMM_ERR_CUDA;
+    return finish_launch(launch_gemv_simt(g, err, s, &name), name);
+  }
   if (a_dtype == QMM_BF16 && gemv_supported(M, K, N, A, B)) {
     GemvArgs g{};
     g.A = static_cast<const uint16_t*>(A);
@@ -381,7 +399,6 @@ qmm_status qmm_w8_dequant(const void* A, int a_dtype, const int8_t* B, int64_t M
 size_t qmm_w8_dequant_workspace_bytes(int a_dtype, int64_t M, int64_t K, int64_t N) {
   if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return 0;
   if (a_dtype != QMM_F32 && a_dtype != QMM_BF16) return 0;
-  if (M <= 4 && gemv_simt_supported(M, K, N, nullptr)) return gemv_simt_workspace_bytes(M, N);
   const W8Plan pl = w8_plan(a_dtype, M, K, N);
   return pl.use ? pl.bytes : 0;
 }
@@ -389,32 +406,6 @@ size_t qmm_w8_dequant_workspace_bytes(int a_dtype, int64_t M, int64_t K, int64_t
 qmm_status qmm_w8_dequant_ws(const void* A, int a_dtype, const int8_t* B, int64_t M, int64_t K, int64_t N,
                              const float* scale, int64_t scale_count, const int32_t* zero_point, int64_t zp_count,
                              void* C, int c_dtype, void* workspace, size_t workspace_bytes, void* stream) {
-  // one to four activation rows: the CUDA-core weight-streaming kernel, K split into partials
-  if (dim_ok(M) && dim_ok(K) && dim_ok(N) && (a_dtype == QMM_F32 || a_dtype == QMM_BF16) &&
-      gemv_simt_supported(M, K, N, B) && workspace && aligned16(workspace) &&
-      workspace_bytes >= gemv_simt_workspace_bytes(M, N)) {
-    if (c_dtype != QMM_F32 && c_dtype != QMM_BF16) return QMM_ERR_INVALID_ARG;
-    if (scale_count != 1 && scale_count != N) return QMM_ERR_INVALID_ARG;
-    if (zp_count != 0 && zp_count != 1 && zp_count != N) return QMM_ERR_INVALID_ARG;
-    if (!scale || !C || !A || (zp_count > 0 && !zero_point)) return QMM_ERR_INVALID_ARG;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaGetLastError();
-    GemvSimtArgs g{};
-    g.A = A;
-    g.a_bf16 = a_dtype == QMM_BF16;
-    g.W = B;
-    g.M = (int)M;
-    g.K = (int)K;
-    g.N = (int)N;
-    g.scale = scale;
-    g.scale_count = (int)scale_count;
-    g.zp = zero_point;
-    g.zp_count = (int)zp_count;
-    g.C = C;
-    g.c_f32 = c_dtype == QMM_F32;
-    const char* name = "none";
-    return finish_launch(launch_gemv_simt(g, workspace, s, &name), name);
-  }
   const W8Plan pl = (dim_ok(M) && dim_ok(K) && dim_ok(N)) ? w8_plan(a_dtype, M, K, N) : W8Plan{};
   const bool a_ok = a_dtype == QMM_F32 ? (reinterpret_cast<uintptr_t>(A) % 4) == 0 : aligned16(A);
   if (!pl.use || N == 0 || !a_ok || !aligned16(B))

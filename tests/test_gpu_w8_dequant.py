@@ -49,7 +49,10 @@ def test_decode_gemv(M, zp, out):
     w = W.decode_gemv(M, K=1024, N=640, seed=M)
     rng = np.random.default_rng(M)
     z = None if zp is None else (np.array([-4], np.int32) if zp == "tensor" else rng.integers(-9, 9, 640).astype(np.int32))
-    kernel = "gemv_w8_bf16_tma" if zp is None else "gemv_w8_bf16_tma_zp"
+    if M <= 2:
+        kernel = "gemv_w8_pair_simt_f32x2"
+    else:
+        kernel = "gemv_w8_bf16_tma" if zp is None else "gemv_w8_bf16_tma_zp"
     check(bf16_dev(w.A_bits), w.A, w.W, w.scale, z, out, kernel)
 
 
@@ -62,23 +65,26 @@ def test_decode_shapes_outside_gemv_fall_back_to_cuda_cores(M, K, N):
 def test_gemv_ragged_k_and_scalar_scale():
     w = W.decode_gemv(3, K=1000, N=384, seed=9)
     check(bf16_dev(w.A_bits), w.A, w.W, w.scale[:1].copy(), None, torch.float32, "gemv_w8_bf16_tma")
+    w = W.decode_gemv(2, K=1000, N=384, seed=9)
+    check(bf16_dev(w.A_bits), w.A, w.W, w.scale[:1].copy(), None, torch.float32, "gemv_w8_pair_simt_f32x2")
 
 
-SIMT = "gemv_w8_simt_f32x2"
+SIMT = "gemv_w8_pair_simt_f32x2"
 
 
-@pytest.mark.parametrize("M", [1])
+@pytest.mark.parametrize("M", [1, 2])
 @pytest.mark.parametrize("zp", [None, "tensor", "column"])
 @pytest.mark.parametrize("out", [torch.bfloat16, torch.float32])
 def test_decode_simt_bf16(M, zp, out):
-    """With a workspace, a single activation row takes the CUDA-core weight-streaming kernel."""
+    """One or two activation rows take the CUDA-core weight-streaming kernel (CTA pairs)."""
     w = W.decode_gemv(M, K=1024, N=640, seed=M + 11)
     rng = np.random.default_rng(M)
     z = None if zp is None else (np.array([-4], np.int32) if zp == "tensor" else rng.integers(-9, 9, 640).astype(np.int32))
     check(bf16_dev(w.A_bits), w.A, w.W, w.scale, z, out, SIMT, workspace="auto")
 
 
-@pytest.mark.parametrize("M,K,N", [(1, 1, 16), (1, 100, 16), (1, 1000, 4096), (1, 4100, 528), (1, 8192, 1040)])
+@pytest.mark.parametrize("M,K,N", [(1, 4, 16), (2, 100, 16), (2, 1000, 4096), (1, 4100, 528), (1, 8192, 1040),
+                                   (2, 64, 512), (1, 196, 28672)])
 def test_decode_simt_fp32_activations_and_ragged_k(M, K, N):
     rng = np.random.default_rng(K + N)
     A = rng.uniform(-1, 1, (M, K)).astype(np.float32)
@@ -90,7 +96,7 @@ def test_decode_simt_fp32_activations_and_ragged_k(M, K, N):
 
 
 def test_decode_simt_is_deterministic():
-    w = W.decode_gemv(1, K=4096, N=2048, seed=5)
+    w = W.decode_gemv(2, K=4096, N=2048, seed=5)
     outs = []
     for _ in range(3):
         C = q.qmm_w8_dequant(bf16_dev(w.A_bits), dev(w.W), dev(w.scale), None, out_dtype=torch.float32)
