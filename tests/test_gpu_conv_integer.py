@@ -42,6 +42,9 @@ GEOMETRIES = [
     ((2, 32, 10, 10), (32, 1, 3, 3), [1, 1, 1, 1], [1, 1], [1, 1], 32),     # depthwise
     ((2, 20, 7, 30), (300, 20, 1, 1), [0, 0, 0, 0], [1, 1], [1, 1], 1),    # 1x1, M > 256
     ((1, 3, 33, 35), (16, 3, 7, 7), [3, 3, 3, 3], [2, 2], [1, 1], 1),      # stem-like, K = 147
+    ((2, 16, 16, 16), (32, 16, 3, 3), [1, 1, 1, 1], [1, 1], [1, 1], 1),    # pixel rows of 16-byte multiples
+    ((1, 32, 8, 8), (272, 32, 1, 1), [0, 0, 0, 0], [1, 1], [1, 1], 1),     # 1x1, 272 output channels
+    ((3, 48, 12, 20), (300, 48, 3, 3), [1, 1, 1, 1], [1, 1], [1, 1], 1),   # ragged pair row tile
 ]
 
 
