@@ -295,15 +295,26 @@ def main():
     def gemm():
         q.qmm_a8w8_packed(M, K, N, a_s, w_s, ws, out=C)
 
+    def step():
+        pack()
+        gemm()
+
     clocks.start()
     barrier()
     torch.cuda.synchronize()
     t0 = time.time()
-    times, gemm_times = time_gpu_split(pack, gemm, args.steps, args.warmup, flush=flush)
+    # the whole step, with nothing between the two calls (the GEMM is launched as
+    # a programmatic dependent of the pre-pass and overlaps its tail)
+    times = time_gpu(step, args.steps, args.warmup, flush=flush)
     t1 = time.time()
     barrier()
     clocks.mark(t0, t1)
     gemm_kernel = q.last_kernel()
+    # the GEMM kernel alone (operands packed once), for the roofline
+    pack()
+    t0g = time.time()
+    gemm_times = time_gpu(gemm, max(20, min(args.steps, 200)), args.warmup, flush=flush)
+    clocks.mark(t0g, time.time())
     kernel_name = "f16_prepass+" + gemm_kernel
     q.check_device_error()
     mean_ms = statistics.mean(times)
@@ -354,7 +365,7 @@ def main():
                    "contraction": "int8 operands copied once to exact fp16 (pre-pass), then exact products on "
                                   "tcgen05 kind::f16 in 2-SM pairs, K-chunked fp32 TMEM accumulators "
                                   "(double-buffered) drained to int32",
-                   "prepass_ms": mean_ms - gemm_ms},
+                   "prepass_exposed_ms": mean_ms - gemm_ms},
         "roofline": {"bound": "tensor", "kernel": gemm_kernel, "achieved": achieved, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                      "traffic": kernel_traffic(gemm_kernel), "kernel_ms": gemm_ms,

@@ -38,6 +38,7 @@ __device__ __forceinline__ int byte_value(uint32_t v) {
 // input rows a band of output rows needs do not fit in shared memory.
 template <bool U>
 __global__ void __launch_bounds__(kThreads) im2col_gather_kernel(const Im2colArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
   const int P = a.oH * a.oW;
   const int p0 = (blockIdx.x * kThreads + threadIdx.x) * kPix;
   if (p0 >= P) return;
@@ -91,6 +92,7 @@ __global__ void __launch_bounds__(kThreads) im2col_gather_kernel(const Im2colArg
 // fp16 values.
 template <bool U>
 __global__ void __launch_bounds__(kThreads) im2col_staged_kernel(const Im2colArgs a, int R, int ws, int cpb) {
+  asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
   extern __shared__ uint8_t sx[];
   const int n = blockIdx.z;
   const int oh0 = blockIdx.x * R;
@@ -205,6 +207,7 @@ __global__ void __launch_bounds__(kThreads) chansum_kernel(const uint8_t* __rest
 template <bool U>
 __global__ void __launch_bounds__(kThreads) window_colsum_kernel(const int* __restrict__ S, const Im2colArgs a,
                                                                  int* __restrict__ colsum) {
+  asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
   const int P = a.oH * a.oW;
   const int p = blockIdx.x * kThreads + threadIdx.x;
   if (p >= P) return;

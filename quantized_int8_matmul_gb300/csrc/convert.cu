@@ -72,6 +72,7 @@ template <bool UA, bool UB>
 __global__ void __launch_bounds__(kBulkThreads, 1)
     convert_bulk_kernel(const uint8_t* __restrict__ A, __half* __restrict__ A16, long long a_bytes,
                         const uint8_t* __restrict__ B, __half* __restrict__ B16, long long b_bytes, unsigned* err) {
+  asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
   extern __shared__ uint8_t smem_raw[];
   __shared__ uint64_t full[kBulkStages];
   __shared__ int abort_flag;
@@ -143,6 +144,7 @@ template <bool UA, bool UB>
 __global__ void __launch_bounds__(256) convert_flat_kernel(const uint8_t* __restrict__ A, __half* __restrict__ A16,
                                                            long long nA, const uint8_t* __restrict__ B,
                                                            __half* __restrict__ B16, long long nB) {
+  asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
   const long long total = nA + nB;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += 4 * stride) {
@@ -177,6 +179,7 @@ __global__ void __launch_bounds__(256) convert_flat_kernel(const uint8_t* __rest
 template <bool U, bool ROWSUM>
 __global__ void __launch_bounds__(256) convert_rows_kernel(const uint8_t* __restrict__ src, __half* __restrict__ dst,
                                                            long long rows, int row_bytes, int* __restrict__ rowsum) {
+  asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
   const int lane = threadIdx.x & 31;
   const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -223,6 +226,7 @@ constexpr int kColRows = 32;
 template <bool U>
 __global__ void __launch_bounds__(256) convert_cols_kernel(const uint8_t* __restrict__ src, __half* __restrict__ dst,
                                                            int mats, int rows, int cols, int* __restrict__ colsum) {
+  asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
   const int cchunks = cols >> 4;
   const int rblocks = (rows + kColRows - 1) / kColRows;
   const long long tasks = (long long)mats * rblocks * cchunks;
@@ -418,6 +422,7 @@ __device__ __forceinline__ void plane_tile(const ConvPlane& p, long long tile, u
 
 template <bool UA, bool UB>
 __global__ void __launch_bounds__(256) convert_planes_kernel(const ConvPlane a, const ConvPlane b, long long tiles_a) {
+  asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
   __shared__ uint8_t st[kPT][kPT + 4];
   if ((long long)blockIdx.x < tiles_a) plane_tile<UA>(a, (long long)blockIdx.x, st);
   else plane_tile<UB>(b, (long long)blockIdx.x - tiles_a, st);
@@ -451,6 +456,7 @@ __global__ void __launch_bounds__(256) acc_only_kernel(const int* __restrict__ a
 template <bool U>
 __global__ void __launch_bounds__(256) colsum_kernel(const uint8_t* __restrict__ src, int rows, int cols,
                                                      int* __restrict__ colsum) {
+  asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
   const int c = blockIdx.x * 256 + threadIdx.x;
   if (c >= cols) return;
   const int r0 = blockIdx.y * 64, r1 = min(rows, r0 + 64);
@@ -524,6 +530,7 @@ __device__ __forceinline__ void s8_to_bf16x4(uint32_t w, uint32_t& lo, uint32_t&
 
 __global__ void __launch_bounds__(256) convert_s8_bf16_kernel(const uint8_t* __restrict__ src,
                                                               uint32_t* __restrict__ dst, long long n16) {
+  asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += 4 * stride) {
     uint4 v[4];
@@ -548,6 +555,7 @@ __global__ void __launch_bounds__(256) convert_s8_bf16_kernel(const uint8_t* __r
 // fp32 row sums of bf16 rows (one warp per row).
 __global__ void __launch_bounds__(256) rowsum_bf16_kernel(const uint16_t* __restrict__ A, long long rows, int K,
                                                           float* __restrict__ rowsum) {
+  asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
   const int lane = threadIdx.x & 31;
   const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -572,6 +580,7 @@ __global__ void __launch_bounds__(256) rowsum_bf16_kernel(const uint16_t* __rest
 // row sums of a (one warp per row).
 __global__ void __launch_bounds__(256) split_f32_kernel(const float* __restrict__ A, long long rows, int K, int Kp,
                                                         uint16_t* __restrict__ out, float* __restrict__ rowsum) {
+  asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
   const int lane = threadIdx.x & 31;
   const long long warp0 = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;

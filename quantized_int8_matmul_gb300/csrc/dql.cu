@@ -282,6 +282,7 @@ __global__ void __launch_bounds__(THREADS) dql_quantize_rows_f16_kernel(const fl
                                                                         long long pitch, float* y_scale,
                                                                         uint8_t* y_zp,
                                                                         int32_t* __restrict__ row_sums) {
+  asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
   const ScaleZp sz = reduce_partials(partials, num_partials);
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     *y_scale = sz.scale;

@@ -370,6 +370,9 @@ __global__ void __launch_bounds__(NT, 1)
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
+  // launched as a programmatic dependent of the pre-pass: everything above ran
+  // while it finished; nothing below reads its output before it completes
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 
   if (warp == NEW) {
     // ---------------- pair MMA issuer (even CTA) ----------------
@@ -531,17 +534,19 @@ cudaError_t launch_one(const GemmF16Args& a, int cs, int c_vec, const CUtensorMa
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;   // overlap the pre-pass's tail
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.blockDim = dim3(NT, 1, 1);
   cfg.dynamicSmemBytes = SMEM_BYTES;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   int max_clusters = 0;
   {
     std::lock_guard<std::mutex> lock(mu);
