@@ -470,6 +470,13 @@ __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t byt
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// TMA store of a 3-D box from shared memory (bulk group completion); elements
+// outside the tensor are not written.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int x, int y, int z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(tmap),
+               "r"(src), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
 // Wait until at most N of this thread's bulk groups still read shared memory.
 template <int N>
 __device__ __forceinline__ void bulk_wait_read() {

@@ -45,7 +45,9 @@ constexpr int BM = 128;
 constexpr int BMP = 2 * BM;
 constexpr int BN_MAX = 256;
 constexpr int BK = 64;
-constexpr int NS = 6;                   // stages in the ring
+constexpr int NS = 6;                   // stages in the ring (5 with the TMA-store epilogue)
+constexpr int STG_BYTES = 2 * 32 * 64;  // per drain warp: two 32-row x 64-byte C staging buffers
+constexpr int STG_TOTAL = 8 * STG_BYTES;
 constexpr int NEW = 8;                  // drain / epilogue warps
 constexpr int NT = NEW * 32 + 64;       // + MMA warp + producer warp
 constexpr int CPW_MAX = BN_MAX / 2;     // accumulator columns per drain warp (two warps per TMEM lane quarter)
@@ -74,8 +76,15 @@ struct Shared {
   float col_bias[NEW][CPW_MAX];
 };
 
-constexpr size_t SMEM_BYTES = (size_t)NS * STAGE_BYTES + sizeof(Shared) + 1024;
-static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+// Ring stages of an instantiation: the 4-byte-output (MatMulInteger) ones give
+// one stage to the C staging buffers of their TMA-store epilogue.
+template <bool TS>
+__host__ __device__ constexpr int ring_stages() { return TS ? NS - 1 : NS; }
+template <bool TS>
+constexpr size_t smem_bytes() {
+  return (size_t)ring_stages<TS>() * STAGE_BYTES + (TS ? STG_TOTAL : 0) + sizeof(Shared) + 1024;
+}
+static_assert(smem_bytes<false>() <= 232448 && smem_bytes<true>() <= 232448, "shared memory per CTA");
 
 enum : unsigned {
   SITE_EMPTY = 0x400, SITE_FULL = 0x401, SITE_ACC_FULL = 0x402, SITE_ACC_EMPTY = 0x403, SITE_TEARDOWN = 0x404,
@@ -291,6 +300,65 @@ __device__ __forceinline__ void epilogue(const GemmF16Args& p, const Shared& sm,
   }
 }
 
+// MatMulInteger epilogue (int32 out, or fp32 with the dequantising step)
+// through TMA stores: per 16-column group the warp's 32 rows x 64 bytes go to
+// one of its two staging buffers (64-byte swizzle: chunk j of row r at chunk
+// j ^ ((r >> 1) & 3), conflict-free), and one lane stores the box; rows and
+// columns outside C are not written. nst counts this warp's stores.
+template <int CPW, bool AU, bool BU, bool DQ>
+__device__ __forceinline__ void epilogue_tma(const GemmF16Args& p, const Shared& sm, uint32_t (&sums)[CPW],
+                                             const TileCoord tc, int warp, int q, int h, int lane, uint32_t stg,
+                                             const CUtensorMap* tmC, int& nst) {
+  const int row0 = tc.m0 + q * 32;
+  if (row0 >= p.M) return;
+  const int row = row0 + lane;
+  const bool rv = row < p.M;
+  const int ag = p.a_bmod ? tc.b % p.a_bmod : 0;
+  uint32_t za = 0u, rs = 0u;
+  if (rv && p.a_zp_count > 0) {
+    const int zi = p.a_zp_count == 1 ? 0 : ag * p.M + row % p.zp_row_mod;
+    za = AU ? (uint32_t)__ldg((const uint8_t*)p.a_zp + zi) : (uint32_t)(int)__ldg((const int8_t*)p.a_zp + zi);
+  }
+  if (rv && p.b_zp_count > 0)
+    rs = (uint32_t)__ldg(p.rowsum + (size_t)(p.a_bstride ? (p.a_bmod ? ag : tc.b) : 0) * p.M + row);
+  const uint32_t kzz = (uint32_t)p.K * za;
+  const uint32_t swz = (uint32_t)((lane >> 1) & 3);
+#pragma unroll
+  for (int g = 0; g < CPW / 16; ++g) {
+    const int nb = tc.n0 + h * CPW + g * 16;
+    if (nb >= p.N) break;
+    uint32_t* o = &sums[g * 16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const uint32_t zb = sm.col_op[warp][g * 16 + i];
+      const uint32_t cs = (uint32_t)sm.col_sum[warp][g * 16 + i];
+      o[i] = o[i] - za * cs - zb * rs + kzz * zb;
+      if (DQ) {   // cast, one multiply by y_scale * w_scale[n], then the bias
+        float v = __fmul_rn(__int2float_rn((int)o[i]), sm.col_scale[warp][g * 16 + i]);
+        if (p.bias) v = __fadd_rn(v, sm.col_bias[warp][g * 16 + i]);
+        o[i] = __float_as_uint(v);
+      }
+    }
+    const int buf = nst & 1;
+    if (nst >= 2) {   // the store that used this buffer has read it
+      if (lane == 0) bulk_wait_read<1>();
+      __syncwarp();
+    }
+    const uint32_t b = stg + (uint32_t)buf * (32 * 64);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      st_shared_v4(b + (uint32_t)lane * 64u + ((uint32_t)j ^ swz) * 16u, o[4 * j], o[4 * j + 1], o[4 * j + 2],
+                   o[4 * j + 3]);
+    fence_proxy_async_smem();   // the generic-proxy writes, visible to the copy engine
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_3d(tmC, b, nb, row0, tc.b);
+      bulk_commit();
+    }
+    ++nst;
+  }
+}
+
 // Accumulating A8W8: start this thread's running sums (one row, CPW columns)
 // from the caller's int32 accumulator (0 outside the problem). Issued before
 // the wait for the tile's first chunk, so the loads overlap the MMAs.
@@ -323,7 +391,9 @@ __device__ __forceinline__ void preload_acc(const GemmF16Args& p, const TileCoor
 template <int BN, bool AU, bool BU, bool MMI, bool FA, bool ACC, bool DQ>
 __global__ void __launch_bounds__(NT, 1)
     gemm_f16pair_kernel(const GemmF16Args p, const int cs, const int c_vec, const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB) {
+                        const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC) {
+  constexpr bool TS = MMI;                 // 4-byte outputs leave through the TMA-store epilogue
+  constexpr int kNS = ring_stages<TS>();
   constexpr int BNH = BN / 2;   // B columns of each CTA
   constexpr int CPW = BN / 2;   // accumulator columns per drain warp
   static_assert(BN % 32 == 0 && BN <= BN_MAX && BNH <= 128, "pair tile width");
@@ -331,7 +401,8 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* sbase_ptr = smem_raw + (sbase - raw);
-  Shared& sm = *reinterpret_cast<Shared*>(sbase_ptr + NS * STAGE_BYTES);
+  const uint32_t stg_base = sbase + (uint32_t)(kNS * STAGE_BYTES);   // C staging (TS), 1024-byte aligned
+  Shared& sm = *reinterpret_cast<Shared*>(sbase_ptr + kNS * STAGE_BYTES + (TS ? STG_TOTAL : 0));
 
   const int t = threadIdx.x;
   const int warp = t >> 5;
@@ -350,7 +421,7 @@ __global__ void __launch_bounds__(NT, 1)
   const int total_chunks = my_tiles * cpt;
 
   if (t == 0) {
-    for (int i = 0; i < NS; ++i) {
+    for (int i = 0; i < kNS; ++i) {
       mbar_init(&sm.full[i], 1);
       mbar_init(&sm.empty[i], 1);
     }
@@ -393,8 +464,8 @@ __global__ void __launch_bounds__(NT, 1)
           const int s_beg = c * cs;
           const int s_end = min(spt, s_beg + cs);
           for (int s = s_beg; s < s_end; ++s, ++g) {
-            const int slot = g % NS;
-            ok = mbar_wait_cluster(&sm.full[slot], (uint32_t)((g / NS) & 1), &sm.abort_flag, p.err, SITE_FULL);
+            const int slot = g % kNS;
+            ok = mbar_wait_cluster(&sm.full[slot], (uint32_t)((g / kNS) & 1), &sm.abort_flag, p.err, SITE_FULL);
             if (!ok) break;
             tc_fence_after();
             const uint32_t a_addr = sbase + (uint32_t)slot * STAGE_BYTES;
@@ -425,9 +496,9 @@ __global__ void __launch_bounds__(NT, 1)
       TileCoord tc = tile_coord<BN>(p, 0, cid, ncl, (int)rank);
       int g = 0;
       for (; g < total_stages; ++g) {
-        const int slot = g % NS;
-        if (g >= NS &&
-            !mbar_wait(&sm.empty[slot], (uint32_t)(((g / NS) - 1) & 1), &sm.abort_flag, p.err, SITE_EMPTY))
+        const int slot = g % kNS;
+        if (g >= kNS &&
+            !mbar_wait(&sm.empty[slot], (uint32_t)(((g / kNS) - 1) & 1), &sm.abort_flag, p.err, SITE_EMPTY))
           break;
         const uint32_t bar = full_leader0 + (uint32_t)slot * 8u;
         if (rank == 0) mbar_arrive_expect_tx(&sm.full[slot], 2u * STAGE_BYTES);
@@ -446,8 +517,8 @@ __global__ void __launch_bounds__(NT, 1)
       // The even CTA's `full` barriers count both CTAs' bytes: once the phases
       // of the last stages complete, no copy of either CTA is in flight.
       if (rank == 0)
-        for (int j = (g > NS ? g - NS : 0); j < g; ++j)
-          mbar_wait_cluster(&sm.full[j % NS], (uint32_t)((j / NS) & 1), nullptr, p.err, SITE_FINAL);
+        for (int j = (g > kNS ? g - kNS : 0); j < g; ++j)
+          mbar_wait_cluster(&sm.full[j % kNS], (uint32_t)((j / kNS) & 1), nullptr, p.err, SITE_FINAL);
     }
     __syncwarp();
   } else {
@@ -457,6 +528,7 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&sm.acc_empty[0]), 0);
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     uint32_t sums[CPW];
+    int nst = 0;   // TMA stores this warp has issued
     int tl = 0, c = 0;
     TileCoord tc = tile_coord<BN>(p, 0, cid, ncl, (int)rank);
     if (my_tiles > 0) stage_columns<CPW, BU, MMI, FA, ACC, DQ>(p, sm, tc, warp, h, lane);
@@ -486,7 +558,11 @@ __global__ void __launch_bounds__(NT, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_remote_cta(acc_empty_leader0 + (uint32_t)ab * 8u);
       if (c == cpt - 1) {
-        epilogue<CPW, AU, BU, MMI, FA, ACC, DQ>(p, sm, sums, tc, warp, q, h, lane, c_vec);
+        if (TS && (c_vec & 1))
+          epilogue_tma<CPW, AU, BU, DQ>(p, sm, sums, tc, warp, q, h, lane, stg_base + (uint32_t)warp * STG_BYTES,
+                                        &tmC, nst);
+        else
+          epilogue<CPW, AU, BU, MMI, FA, ACC, DQ>(p, sm, sums, tc, warp, q, h, lane, c_vec);
         __syncwarp();   // the warp's staged operands are read: restage for the next tile
         if (tl + 1 < my_tiles)
           stage_columns<CPW, BU, MMI, FA, ACC, DQ>(p, sm, tile_coord<BN>(p, tl + 1, cid, ncl, (int)rank), warp,
@@ -498,6 +574,7 @@ __global__ void __launch_bounds__(NT, 1)
         tc = tile_coord<BN>(p, tl, cid, ncl, (int)rank);
       }
     }
+    if (TS && lane == 0 && nst > 0) bulk_wait_all();   // this warp's stores are complete
     tc_fence_before();
   }
 
@@ -527,7 +604,8 @@ struct DeviceLaunchInfo {
 
 template <int BN, bool AU, bool BU, bool MMI, bool FA = false, bool ACC = false, bool DQ = false>
 cudaError_t launch_one(const GemmF16Args& a, int cs, int c_vec, const CUtensorMap& ta, const CUtensorMap& tb,
-                       cudaStream_t s) {
+                       const CUtensorMap& tc, cudaStream_t s) {
+  constexpr size_t SMEM_BYTES = smem_bytes<MMI>();
   auto kern = gemm_f16pair_kernel<BN, AU, BU, MMI, FA, ACC, DQ>;
   static std::mutex mu;
   static DeviceLaunchInfo info[64];
@@ -566,7 +644,7 @@ cudaError_t launch_one(const GemmF16Args& a, int cs, int c_vec, const CUtensorMa
   const long long tiles = (long long)a.batch * m_tiles * n_tiles;
   const int ncl = (int)std::min<long long>(tiles, (long long)max_clusters);
   cfg.gridDim = dim3(2 * ncl, 1, 1);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, cs, c_vec, ta, tb);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a, cs, c_vec, ta, tb, tc);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -612,22 +690,22 @@ int choose_tile_width(const GemmF16Args& a) {
 
 template <int BN>
 cudaError_t dispatch(const GemmF16Args& a, bool a_u8, bool b_u8, bool mmi, int cs, int c_vec, const CUtensorMap& ta,
-                     const CUtensorMap& tb, cudaStream_t s) {
+                     const CUtensorMap& tb, const CUtensorMap& tc, cudaStream_t s) {
   if (!mmi) {
     // the accumulator epilogue's extra loads fit the register budget at the
     // 224-column width only (the 256-column one spills)
-    if (a.acc_in || a.acc_out || !a.C) return launch_one<224, false, false, false, false, true>(a, cs, c_vec, ta, tb, s);
-    return launch_one<BN, false, false, false>(a, cs, c_vec, ta, tb, s);
+    if (a.acc_in || a.acc_out || !a.C) return launch_one<224, false, false, false, false, true>(a, cs, c_vec, ta, tb, tc, s);
+    return launch_one<BN, false, false, false>(a, cs, c_vec, ta, tb, tc, s);
   }
   if (a.act_scale) {   // dequantising MatMulInteger: A is the quantised activation (uint8); 224 columns
     if (!a_u8) return cudaErrorInvalidValue;   // fit the extra epilogue operands without spilling
-    if (b_u8) return launch_one<224, true, true, true, false, false, true>(a, cs, c_vec, ta, tb, s);
-    return launch_one<224, true, false, true, false, false, true>(a, cs, c_vec, ta, tb, s);
+    if (b_u8) return launch_one<224, true, true, true, false, false, true>(a, cs, c_vec, ta, tb, tc, s);
+    return launch_one<224, true, false, true, false, false, true>(a, cs, c_vec, ta, tb, tc, s);
   }
-  if (!a_u8 && !b_u8) return launch_one<BN, false, false, true>(a, cs, c_vec, ta, tb, s);
-  if (a_u8 && !b_u8) return launch_one<BN, true, false, true>(a, cs, c_vec, ta, tb, s);
-  if (!a_u8 && b_u8) return launch_one<BN, false, true, true>(a, cs, c_vec, ta, tb, s);
-  return launch_one<BN, true, true, true>(a, cs, c_vec, ta, tb, s);
+  if (!a_u8 && !b_u8) return launch_one<BN, false, false, true>(a, cs, c_vec, ta, tb, tc, s);
+  if (a_u8 && !b_u8) return launch_one<BN, true, false, true>(a, cs, c_vec, ta, tb, tc, s);
+  if (!a_u8 && b_u8) return launch_one<BN, false, true, true>(a, cs, c_vec, ta, tb, tc, s);
+  return launch_one<BN, true, true, true>(a, cs, c_vec, ta, tb, tc, s);
 }
 
 }  // namespace gemmf
@@ -640,14 +718,19 @@ cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool
   const bool acc_al = ((reinterpret_cast<uintptr_t>(a.acc_in) | reinterpret_cast<uintptr_t>(a.acc_out)) % 16) == 0;
   const int c_vec = (((reinterpret_cast<uintptr_t>(a.C) % 16) == 0) && (((long long)a.N * celem) % 16 == 0) ? 1 : 0) |
                     ((acc_al && a.N % 4 == 0) ? 2 : 0);
-  CUtensorMap ta{}, tb{};
+  CUtensorMap ta{}, tb{}, tc{};
   cudaError_t e = make_maps(a, &ta, &tb);
   if (e != cudaSuccess) return e;
+  if (mmi && (c_vec & 1)) {   // C as {N, M, batch} int32 / fp32, box 16 x 32, for the TMA-store epilogue
+    e = make_tmap_3d(&tc, a.C, CU_TENSOR_MAP_DATA_TYPE_INT32, (uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.batch,
+                     4ull * (uint64_t)a.N, 4ull * (uint64_t)a.M * (uint64_t)a.N, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (e != cudaSuccess) return e;
+  }
   *kernel_name = mmi ? (a.act_scale ? "gemm_tc05_pair_f16ops_matmul_integer_dequant"
                            : "gemm_tc05_pair_f16ops_matmul_integer")
                      : ((a.acc_in || a.acc_out || !a.C) ? "gemm_tc05_pair_f16ops_a8w8_acc" : "gemm_tc05_pair_f16ops_a8w8");
-  if (choose_tile_width(a) == 224) return dispatch<224>(a, a_u8, b_u8, mmi, cs, c_vec, ta, tb, s);
-  return dispatch<256>(a, a_u8, b_u8, mmi, cs, c_vec, ta, tb, s);
+  if (choose_tile_width(a) == 224) return dispatch<224>(a, a_u8, b_u8, mmi, cs, c_vec, ta, tb, tc, s);
+  return dispatch<256>(a, a_u8, b_u8, mmi, cs, c_vec, ta, tb, tc, s);
 }
 
 cudaError_t launch_gemm_w8_bf16pair(const GemmF16Args& a, int w_k, cudaStream_t s, const char** kernel_name) {
@@ -661,12 +744,12 @@ cudaError_t launch_gemm_w8_bf16pair(const GemmF16Args& a, int w_k, cudaStream_t 
   GemmF16Args wa = a;
   wa.K = w_k;
   cudaError_t e = make_maps(a, &ta, &tb);
-  CUtensorMap unused{};
+  CUtensorMap unused{}, tc{};
   if (e == cudaSuccess) e = make_maps(wa, &unused, &tb);
   if (e != cudaSuccess) return e;
   *kernel_name = "gemm_tc05_pair_w8_bf16";
-  if (choose_tile_width(a) == 224) return launch_one<224, false, false, false, true>(a, cs, c_vec, ta, tb, s);
-  return launch_one<256, false, false, false, true>(a, cs, c_vec, ta, tb, s);
+  if (choose_tile_width(a) == 224) return launch_one<224, false, false, false, true>(a, cs, c_vec, ta, tb, tc, s);
+  return launch_one<256, false, false, false, true>(a, cs, c_vec, ta, tb, tc, s);
 }
 
 }  // namespace qmm
