@@ -167,9 +167,27 @@ struct GemvArgs {
   const int32_t* zp;  int zp_count;           // 0, 1 or N
   void* C; int c_f32;                         // [M][N] bf16 (0) or f32 (1)
   unsigned* err;                              // device error word
+  // fp16 route (A16 non-null): the activations as fp16 [M][Kp] (Kp = K rounded
+  // up to 16), row m scaled by 2^s_m and its K order permuted inside every
+  // 16-element group, as launch_gemv_prep writes them; inv[m] = 2^-s_m
+  const uint16_t* A16;
+  const float* inv;
+  int Kp;
 };
 bool gemv_supported(long long M, long long K, long long N, const void* A, const void* W);
 cudaError_t launch_gemv(const GemvArgs& a, cudaStream_t s, const char** kernel_name);
+// The fp16 route's pre-pass (one CTA per row; bf16 A [M][K], K % 8 == 0): a
+// power-of-two row scale 2^s_m that puts the row's largest magnitude in
+// [2^14, 2^15) (exact, and inside fp16's range), then fp16 copies of the
+// scaled values (exact for every bf16 value down to 2^-17 of the row maximum)
+// in the K order the GEMV's fragments read: inside each group of 16, element
+// q holds k = q with bits 0 and 1 swapped. Workspace: gemv_f16_workspace_bytes.
+size_t gemv_f16_workspace_bytes(long long M, long long K);
+cudaError_t launch_gemv_prep(const uint16_t* A, int M, int K, void* workspace, cudaStream_t s);
+// The fp16 route: the GEMV launched as a programmatic dependent of the prep
+// (its weight stream starts before the prep ends); A16 / inv / Kp point into
+// the prep's workspace.
+cudaError_t launch_gemv_f16(GemvArgs a, void* workspace, cudaStream_t s, const char** kernel_name);
 
 // ---------------------------------------------------------------------------
 // Decode-shaped form (a) for M <= 4 on the CUDA cores: TMA-staged weight,

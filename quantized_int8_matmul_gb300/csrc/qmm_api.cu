@@ -396,9 +396,17 @@ qmm_status qmm_w8_dequant(const void* A, int a_dtype, const int8_t* B, int64_t M
   return finish_launch(launch_w8_simt(w, s, &name), name);
 }
 
+// Decode shapes of 3 to 16 bf16 rows take the GEMV's fp16 route when a
+// workspace is given (the activations pre-scaled to fp16 there); one or two
+// rows keep the CUDA-core pair kernel, which is faster for them.
+bool gemv_f16_shape(int a_dtype, int64_t M, int64_t K, int64_t N) {
+  return a_dtype == QMM_BF16 && M >= 3 && M <= 16 && K >= 8 && K % 8 == 0 && N >= 16 && N % 16 == 0;
+}
+
 size_t qmm_w8_dequant_workspace_bytes(int a_dtype, int64_t M, int64_t K, int64_t N) {
   if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return 0;
   if (a_dtype != QMM_F32 && a_dtype != QMM_BF16) return 0;
+  if (gemv_f16_shape(a_dtype, M, K, N)) return gemv_f16_workspace_bytes(M, K);
   const W8Plan pl = w8_plan(a_dtype, M, K, N);
   return pl.use ? pl.bytes : 0;
 }
@@ -406,6 +414,34 @@ size_t qmm_w8_dequant_workspace_bytes(int a_dtype, int64_t M, int64_t K, int64_t
 qmm_status qmm_w8_dequant_ws(const void* A, int a_dtype, const int8_t* B, int64_t M, int64_t K, int64_t N,
                              const float* scale, int64_t scale_count, const int32_t* zero_point, int64_t zp_count,
                              void* C, int c_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  if (dim_ok(M) && dim_ok(K) && dim_ok(N) && gemv_f16_shape(a_dtype, M, K, N) && gemv_supported(M, K, N, A, B) &&
+      workspace && aligned16(workspace) && workspace_bytes >= gemv_f16_workspace_bytes(M, K)) {
+    if (c_dtype != QMM_F32 && c_dtype != QMM_BF16) return QMM_ERR_INVALID_ARG;
+    if (scale_count != 1 && scale_count != N) return QMM_ERR_INVALID_ARG;
+    if (zp_count != 0 && zp_count != 1 && zp_count != N) return QMM_ERR_INVALID_ARG;
+    if (!scale || !C || (zp_count > 0 && !zero_point)) return QMM_ERR_INVALID_ARG;
+    unsigned* err = err_word();
+    if (!err) return QMM_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaGetLastError();
+    GemvArgs g{};
+    g.A = static_cast<const uint16_t*>(A);
+    g.W = B;
+    g.M = (int)M;
+    g.K = (int)K;
+    g.N = (int)N;
+    g.scale = scale;
+    g.scale_count = (int)scale_count;
+    g.zp = zero_point;
+    g.zp_count = (int)zp_count;
+    g.C = C;
+    g.c_f32 = c_dtype == QMM_F32;
+    g.err = err;
+    const char* name = "none";
+    cudaError_t e = launch_gemv_prep(g.A, g.M, g.K, workspace, s);
+    if (e == cudaSuccess) e = launch_gemv_f16(g, workspace, s, &name);
+    return finish_launch(e, zp_count > 0 ? "gemv_f16_prep+gemv_w8_f16_tma_zp" : "gemv_f16_prep+gemv_w8_f16_tma");
+  }
   const W8Plan pl = (dim_ok(M) && dim_ok(K) && dim_ok(N)) ? w8_plan(a_dtype, M, K, N) : W8Plan{};
   const bool a_ok = a_dtype == QMM_F32 ? (reinterpret_cast<uintptr_t>(A) % 4) == 0 : aligned16(A);
   if (!pl.use || N == 0 || !a_ok || !aligned16(B))

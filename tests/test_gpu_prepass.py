@@ -63,6 +63,49 @@ def test_two_pass_a8w8_scalar_scales_and_chunk_edge():
     assert (a8w8(A, B, one, one) == np.float32(16384 * K)).all()
 
 
+def test_one_workspace_serves_calls_of_several_shapes():
+    """A workspace of arbitrary bytes, reused by calls of other shapes."""
+    shapes = [(1000, 1040, 1008), (1536, 192, 2000), (1000, 1040, 1008), (257, 128, 272)]
+    need = max(q.qmm_a8w8_workspace_bytes(*s) for s in shapes)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    for i, (M, K, N) in enumerate(shapes):
+        w = W.a8w8(M, K, N, seed=40 + i)
+        got = a8w8(w.A, w.B, w.act_scale, w.weight_scale, "bf16", workspace=ws)
+        assert q.last_kernel() == TWO_PASS_A8W8
+        assert_equal(got, O.a8w8(w.A, w.B, w.act_scale, w.weight_scale, "bf16"), f"reused workspace {M}x{K}x{N}")
+
+
+def test_captured_call_replays_exactly():
+    """The two-pass call captured into a CUDA graph (the GEMM a programmatic
+    dependent of the pre-pass inside the graph) replays exactly with new
+    inputs."""
+    M, K, N = 1000, 1040, 1008
+    w1, w2 = W.a8w8(M, K, N, seed=50), W.a8w8(M, K, N, seed=51)
+    A, B, a_s, w_s = dev(w1.A), dev(w1.B), dev(w1.act_scale), dev(w1.weight_scale)
+    ws = torch.empty(q.qmm_a8w8_workspace_bytes(M, K, N), dtype=torch.uint8, device="cuda")
+    out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        q.qmm_a8w8(A, B, a_s, w_s, out=out, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    assert q.last_kernel() == TWO_PASS_A8W8
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        q.qmm_a8w8(A, B, a_s, w_s, out=out, workspace=ws)
+    assert q.last_kernel() == TWO_PASS_A8W8
+    for w in (w2, w1, w2):
+        A.copy_(dev(w.A))
+        B.copy_(dev(w.B))
+        a_s.copy_(dev(w.act_scale))
+        w_s.copy_(dev(w.weight_scale))
+        g.replay()
+        torch.cuda.synchronize()
+        q.check_device_error()
+        assert_equal(host(out), O.a8w8(w.A, w.B, w.act_scale, w.weight_scale, "bf16"), "graph replay")
+
+
 @pytest.mark.parametrize("adt,bdt", [("s8", "s8"), ("u8", "s8"), ("s8", "u8"), ("u8", "u8")])
 @pytest.mark.parametrize("zp", ["none", "scalar", "vector", "a_only", "b_only"])
 @pytest.mark.parametrize("M,K,N", [(260, 1040, 272), (513, 272, 400)])

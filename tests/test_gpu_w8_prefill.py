@@ -63,7 +63,7 @@ def test_scalar_scale_and_wide_dynamic_range():
 
 
 @pytest.mark.parametrize("M,K,N,kernel", [(63, 256, 256, "w8_dequant_simt"), (128, 40, 256, "w8_dequant_simt"),
-                                          (16, 1024, 640, "gemv_w8_bf16_tma")])
+                                          (16, 1024, 640, "gemv_f16_prep+gemv_w8_f16_tma")])
 def test_shapes_outside_the_prefill_path(M, K, N, kernel):
     w = W.decode_gemv(M, K=K, N=N, seed=3)
     assert q.qmm_w8_dequant_workspace_bytes(torch.bfloat16, M, K, N) == 0 or M <= 16
