@@ -221,14 +221,26 @@ __global__ void __launch_bounds__(256) convert_rows_kernel(const uint8_t* __rest
 // converts rows [rb*R, rb*R + R) of 16 columns and adds its 16 partial column
 // sums into colsum (zeroed beforehand) with atomics. `mats` matrices of
 // `rows` x `cols` bytes each (batch of B), colsum is [mats][cols].
-constexpr int kColRows = 32;
+constexpr int kColRows = 32;   // rows per task at most (fewer when the matrix is small)
+
+// Rows per task: as many as keep every SM busy with a few waves of tasks, a
+// multiple of 4 in [4, kColRows] (a 1024 x 1024 weight gets 4: 64 CTAs instead of 8
+// with 32).
+int col_rows_per_task(long long mats, int rows, int cols) {
+  const long long target = (long long)num_sms() * 1024;
+  const long long work = mats * (long long)rows * (cols / 16);
+  long long r = (work + target - 1) / target;
+  r = (r + 3) / 4 * 4;
+  return (int)std::max<long long>(4, std::min<long long>(kColRows, r));
+}
 
 template <bool U>
 __global__ void __launch_bounds__(256) convert_cols_kernel(const uint8_t* __restrict__ src, __half* __restrict__ dst,
-                                                           int mats, int rows, int cols, int* __restrict__ colsum) {
+                                                           int mats, int rows, int cols, int* __restrict__ colsum,
+                                                           int rpt) {
   asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
   const int cchunks = cols >> 4;
-  const int rblocks = (rows + kColRows - 1) / kColRows;
+  const int rblocks = (rows + rpt - 1) / rpt;
   const long long tasks = (long long)mats * rblocks * cchunks;
   for (long long task = (long long)blockIdx.x * blockDim.x + threadIdx.x; task < tasks;
        task += (long long)gridDim.x * blockDim.x) {
@@ -240,9 +252,9 @@ __global__ void __launch_bounds__(256) convert_cols_kernel(const uint8_t* __rest
     int sum[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) sum[i] = 0;
-    const int r_end = min(rows, (rb + 1) * kColRows);
+    const int r_end = min(rows, (rb + 1) * rpt);
 #pragma unroll 4
-    for (int r = rb * kColRows; r < r_end; ++r) {
+    for (int r = rb * rpt; r < r_end; ++r) {
       const size_t off = base + (size_t)r * cols + 16 * (size_t)cc;
       const uint4 v = ldg_nc_v4(src + off);
       uint32_t h[8];
@@ -340,11 +352,12 @@ cudaError_t launch_convert_cols(const void* src, bool u8, __half* dst, int mats,
   if (mats <= 0 || rows <= 0 || cols <= 0) return cudaSuccess;
   cudaError_t e = cudaMemsetAsync(colsum, 0, sizeof(int) * (size_t)mats * cols, s);
   if (e != cudaSuccess) return e;
-  const long long tasks = (long long)mats * ((rows + kColRows - 1) / kColRows) * (cols / 16);
+  const int rpt = col_rows_per_task(mats, rows, cols);
+  const long long tasks = (long long)mats * ((rows + rpt - 1) / rpt) * (cols / 16);
   const int grid = grid_for(tasks, 256);
   const uint8_t* p = static_cast<const uint8_t*>(src);
-  if (u8) convert_cols_kernel<true><<<grid, 256, 0, s>>>(p, dst, mats, rows, cols, colsum);
-  else convert_cols_kernel<false><<<grid, 256, 0, s>>>(p, dst, mats, rows, cols, colsum);
+  if (u8) convert_cols_kernel<true><<<grid, 256, 0, s>>>(p, dst, mats, rows, cols, colsum, rpt);
+  else convert_cols_kernel<false><<<grid, 256, 0, s>>>(p, dst, mats, rows, cols, colsum, rpt);
   return cudaGetLastError();
 }
 
