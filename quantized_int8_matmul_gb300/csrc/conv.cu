@@ -302,6 +302,101 @@ cudaError_t im2col_one(const Im2colArgs& a, int* S, cudaStream_t s) {
 }
 }  // namespace convk
 
+// ---------------------------------------------------------------------------
+// Implicit-GEMM route: the operands with their zero points already taken out,
+// as fp16 (every difference of two 8-bit values lies in [-255, 255]). The
+// input becomes channels-innermost (NHWC) so that an im2col tensor copy can
+// gather a 64-channel slice of 128 output pixels' windows per stage; padding
+// then reads as 0, i.e. as x_zp before the shift.
+// ---------------------------------------------------------------------------
+namespace convk {
+
+template <bool U>
+__device__ __forceinline__ int zp_value(const void* zp, int i) {
+  return U ? (int)static_cast<const uint8_t*>(zp)[i] : (int)static_cast<const int8_t*>(zp)[i];
+}
+
+// One CTA per 64 pixels x 64 channels of one image, transposed through shared
+// memory: reads 64 channel rows of 64 bytes, writes 64 pixel rows of 64 fp16.
+template <bool U>
+__global__ void __launch_bounds__(kThreads) conv_x16_kernel(const uint8_t* __restrict__ x, int C, int HW,
+                                                            const void* xzp, __half* __restrict__ x16, bool vec) {
+  asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
+  __shared__ uint8_t tile[64][64 + 16];
+  const int p0 = blockIdx.x * 64, c0 = blockIdx.y * 64, n = blockIdx.z;
+  const int zp = xzp ? zp_value<U>(xzp, 0) : 0;
+  {
+    const int lc = threadIdx.x >> 2, lp = (threadIdx.x & 3) * 16;
+    const uint8_t* src = x + ((size_t)n * C + c0 + lc) * HW + p0 + lp;
+    if (vec && p0 + lp + 16 <= HW) {
+      const uint4 v = ldg_nc_v4(src);
+      *reinterpret_cast<uint4*>(&tile[lc][lp]) = v;
+    } else {
+      for (int i = 0; i < 16; ++i) tile[lc][lp + i] = (p0 + lp + i < HW) ? src[i] : (uint8_t)0;
+    }
+  }
+  __syncthreads();
+  const int pp = threadIdx.x >> 2, cc = (threadIdx.x & 3) * 16;
+  if (p0 + pp < HW) {
+    uint32_t h[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const __half2 v = __halves2half2(__int2half_rn(byte_value<U>(tile[cc + 2 * i][pp]) - zp),
+                                       __int2half_rn(byte_value<U>(tile[cc + 2 * i + 1][pp]) - zp));
+      h[i] = *reinterpret_cast<const uint32_t*>(&v);
+    }
+    __half* d = x16 + ((size_t)n * HW + p0 + pp) * C + c0 + cc;
+    st_v4(d, h[0], h[1], h[2], h[3]);
+    st_v4(d + 8, h[4], h[5], h[6], h[7]);
+  }
+}
+
+// One thread per element of w16 [M][(r*kW + s)*Cg + c].
+template <bool U>
+__global__ void __launch_bounds__(kThreads) conv_w16_kernel(const uint8_t* __restrict__ w, int M, int Cg, int kH,
+                                                            int kW, const void* wzp, int wzp_count,
+                                                            __half* __restrict__ w16) {
+  asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
+  const long long Kg = (long long)kH * kW * Cg;
+  const long long idx = (long long)blockIdx.x * kThreads + threadIdx.x;
+  if (idx >= (long long)M * Kg) return;
+  const int m = (int)(idx / Kg);
+  const int k = (int)(idx - (long long)m * Kg);
+  const int tap = k / Cg, c = k - tap * Cg;
+  const int r = tap / kW, sx = tap - r * kW;
+  const int zp = wzp_count == 0 ? 0 : zp_value<U>(wzp, wzp_count == 1 ? 0 : m);
+  const int v = byte_value<U>(w[(((size_t)m * Cg + c) * kH + r) * kW + sx]);
+  w16[idx] = __int2half_rn(v - zp);
+}
+
+}  // namespace convk
+
+cudaError_t launch_conv_x16(const void* x, bool u8, int Nb, int C, int HW, const void* xzp, __half* x16,
+                            cudaStream_t s) {
+  using namespace convk;
+  if (Nb <= 0 || C <= 0 || HW <= 0) return cudaSuccess;
+  if (C % 64 != 0 || Nb > 65535 || C / 64 > 65535) return cudaErrorInvalidValue;
+  const bool vec = HW % 16 == 0 && (reinterpret_cast<uintptr_t>(x) % 16) == 0;
+  const dim3 grid((HW + 63) / 64, C / 64, Nb);
+  const uint8_t* p = static_cast<const uint8_t*>(x);
+  if (u8) conv_x16_kernel<true><<<grid, kThreads, 0, s>>>(p, C, HW, xzp, x16, vec);
+  else conv_x16_kernel<false><<<grid, kThreads, 0, s>>>(p, C, HW, xzp, x16, vec);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_conv_w16(const void* w, bool u8, int M, int Cg, int kH, int kW, const void* wzp, int wzp_count,
+                            __half* w16, cudaStream_t s) {
+  using namespace convk;
+  const long long total = (long long)M * kH * kW * Cg;
+  if (total <= 0) return cudaSuccess;
+  const long long blocks = (total + kThreads - 1) / kThreads;
+  if (blocks > INT_MAX) return cudaErrorInvalidValue;
+  const uint8_t* p = static_cast<const uint8_t*>(w);
+  if (u8) conv_w16_kernel<true><<<(unsigned)blocks, kThreads, 0, s>>>(p, M, Cg, kH, kW, wzp, wzp_count, w16);
+  else conv_w16_kernel<false><<<(unsigned)blocks, kThreads, 0, s>>>(p, M, Cg, kH, kW, wzp, wzp_count, w16);
+  return cudaGetLastError();
+}
+
 size_t im2col_sum_scratch_bytes(long long Nb, long long G, long long H, long long W) {
   return (size_t)Nb * G * H * W * sizeof(int);
 }

@@ -119,6 +119,18 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
       : "memory");
 }
 
+// Im2col tensor copy (rank 4, {C, W, H, N}) completing on an mbarrier of
+// either CTA of the pair: the pixels from base (w, h) of image n onwards, each
+// shifted by the tap offsets (ow, oh), channels [c, c + box).
+__device__ __forceinline__ void tma_im2col_4d_pair(uint32_t dst, const void* tmap, int c, int w, int h, int n,
+                                                   uint16_t ow, uint16_t oh, uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.cta_group::2.shared::cluster.global.im2col.mbarrier::complete_tx::bytes [%0], [%1, "
+      "{%2, %3, %4, %5}], [%6], {%7, %8};" ::"r"(dst),
+      "l"(tmap), "r"(c), "r"(w), "r"(h), "r"(n), "r"(bar_cluster), "h"(ow), "h"(oh)
+      : "memory");
+}
+
 // Per-tile operands of this warp's CPW columns, staged in shared memory by
 // the warp itself.
 template <int CPW, bool BU, bool MMI, bool FA, bool ACC = false, bool DQ = false>
@@ -388,7 +400,7 @@ __device__ __forceinline__ void preload_acc(const GemmF16Args& p, const TileCoor
   }
 }
 
-template <int BN, bool AU, bool BU, bool MMI, bool FA, bool ACC, bool DQ>
+template <int BN, bool AU, bool BU, bool MMI, bool FA, bool ACC, bool DQ, bool CV>
 __global__ void __launch_bounds__(NT, 1)
     gemm_f16pair_kernel(const GemmF16Args p, const int cs, const int c_vec, const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC) {
@@ -448,7 +460,9 @@ __global__ void __launch_bounds__(NT, 1)
   if (warp == NEW) {
     // ---------------- pair MMA issuer (even CTA) ----------------
     if (rank == 0 && lane == 0) {
-      const uint32_t idesc = FA ? idesc_bf16_f32(BMP, BN, false, true) : idesc_f16_f32(BMP, BN, false, true);
+      // B is MN-major (64-column boxes of [K][N] rows) except for the implicit
+      // convolution, whose im2col copies deliver pixel rows of 64 channels (K-major)
+      const uint32_t idesc = FA ? idesc_bf16_f32(BMP, BN, false, true) : idesc_f16_f32(BMP, BN, false, !CV);
       int g = 0, d = 0;
       bool ok = true;
       for (int tl = 0; tl < my_tiles && ok; ++tl) {
@@ -474,7 +488,8 @@ __global__ void __launch_bounds__(NT, 1)
             for (int j = 0; j < BK / 16; ++j) {
               const uint64_t ad = sdesc_sw128(a_addr + (uint32_t)j * 32u, 16u, 1024u);
               // B: 64-column boxes 8 KB apart (LBO), 8-row k groups 1 KB apart (SBO)
-              const uint64_t bd = sdesc_sw128(b_addr + (uint32_t)j * 2048u, (uint32_t)B_BOX, 1024u);
+              const uint64_t bd = CV ? sdesc_sw128(b_addr + (uint32_t)j * 32u, 16u, 1024u)
+                                     : sdesc_sw128(b_addr + (uint32_t)j * 2048u, (uint32_t)B_BOX, 1024u);
               tc_mma_f16_pair(tacc, ad, bd, idesc, (s > s_beg || j > 0) ? 1u : 0u);
             }
             tc_commit_pair_mc(&sm.empty[slot], 0x3);
@@ -506,9 +521,22 @@ __global__ void __launch_bounds__(NT, 1)
         const int ab = p.a_bstride ? (p.a_bmod ? tc.b % p.a_bmod : tc.b) : 0, bb = p.b_bstride ? tc.b : 0;
         const int nc = tc.n0 + (int)rank * BNH;
         tma_load_3d_pair(dst, &tmA, s * BK, tc.m0, ab, bar);
-        const int kb = (FA && p.fa_kwrap) ? (s * BK) % p.fa_kwrap : s * BK;   // [hi | lo] halves reread W
-        tma_load_3d_pair(dst + A_BYTES, &tmB, nc, kb, bb, bar);
-        tma_load_3d_pair(dst + A_BYTES + B_BOX, &tmB, nc + 64, kb, bb, bar);
+        if (CV) {
+          // K stage s: tap (r, sx) and 64-channel block cb of the group; the
+          // CTA's 128 pixels start at output pixel nc of image b / G (a start
+          // past the image's last pixel loads pixels that are never stored)
+          const int tap = s / p.cv_cb, cb = s - tap * p.cv_cb;
+          const int r = tap / p.cv_kW, sx = tap - r * p.cv_kW;
+          const int img = tc.b / p.cv_G, grp = tc.b - img * p.cv_G;
+          const int px = nc < p.N ? nc : 0;
+          const int oh = px / p.cv_oW, ow = px - oh * p.cv_oW;
+          tma_im2col_4d_pair(dst + A_BYTES, &tmB, grp * p.cv_Cg + cb * 64, ow * p.cv_sw - p.cv_pl,
+                             oh * p.cv_sh - p.cv_pt, img, (uint16_t)(sx * p.cv_dw), (uint16_t)(r * p.cv_dh), bar);
+        } else {
+          const int kb = (FA && p.fa_kwrap) ? (s * BK) % p.fa_kwrap : s * BK;   // [hi | lo] halves reread W
+          tma_load_3d_pair(dst + A_BYTES, &tmB, nc, kb, bb, bar);
+          tma_load_3d_pair(dst + A_BYTES + B_BOX, &tmB, nc + 64, kb, bb, bar);
+        }
         if (++s == spt) {
           s = 0;
           tc = tile_coord<BN>(p, ++tl, cid, ncl, (int)rank);
@@ -602,11 +630,11 @@ struct DeviceLaunchInfo {
   int max_clusters = 0;
 };
 
-template <int BN, bool AU, bool BU, bool MMI, bool FA = false, bool ACC = false, bool DQ = false>
+template <int BN, bool AU, bool BU, bool MMI, bool FA = false, bool ACC = false, bool DQ = false, bool CV = false>
 cudaError_t launch_one(const GemmF16Args& a, int cs, int c_vec, const CUtensorMap& ta, const CUtensorMap& tb,
                        const CUtensorMap& tc, cudaStream_t s) {
   constexpr size_t SMEM_BYTES = smem_bytes<MMI>();
-  auto kern = gemm_f16pair_kernel<BN, AU, BU, MMI, FA, ACC, DQ>;
+  auto kern = gemm_f16pair_kernel<BN, AU, BU, MMI, FA, ACC, DQ, CV>;
   static std::mutex mu;
   static DeviceLaunchInfo info[64];
   int dev = 0;
@@ -731,6 +759,28 @@ cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool
                      : ((a.acc_in || a.acc_out || !a.C) ? "gemm_tc05_pair_f16ops_a8w8_acc" : "gemm_tc05_pair_f16ops_a8w8");
   if (choose_tile_width(a) == 224) return dispatch<224>(a, a_u8, b_u8, mmi, cs, c_vec, ta, tb, tc, s);
   return dispatch<256>(a, a_u8, b_u8, mmi, cs, c_vec, ta, tb, tc, s);
+}
+
+cudaError_t launch_gemm_f16pair_conv(const GemmF16Args& a, const CUtensorMap& tx, cudaStream_t s,
+                                     const char** kernel_name) {
+  using namespace gemmf;
+  // |(x - x_zp)(w - w_zp)| <= 255^2: the u8 x u8 chunk keeps every fp32 sum exact
+  const int cs = gemm_default_chunk_k(true, true) / BK;
+  const int c_vec = (((reinterpret_cast<uintptr_t>(a.C) % 16) == 0) && (((long long)a.N * 4) % 16 == 0)) ? 1 : 0;
+  if (!c_vec) return cudaErrorInvalidValue;   // the TMA-store epilogue needs 16-byte rows
+  // A: the fp16 weight {K, Mg, groups} (box 64 x 128, 128-byte swizzle)
+  const uint64_t ab = a.a_bstride ? (uint64_t)(a.a_bmod ? a.a_bmod : a.batch) : 1;
+  const uint64_t ap = a.a_pitch ? (uint64_t)a.a_pitch : (uint64_t)a.K;
+  const uint64_t as = 2ull * (a.a_bstride ? (uint64_t)a.a_bstride : (uint64_t)a.M * ap);
+  CUtensorMap ta{}, tc{};
+  cudaError_t e = make_tmap_3d(&ta, a.A16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, (uint64_t)a.K, (uint64_t)a.M, ab,
+                               2ull * ap, as, BK, BM, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_3d(&tc, a.C, CU_TENSOR_MAP_DATA_TYPE_INT32, (uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.batch,
+                   4ull * (uint64_t)a.N, 4ull * (uint64_t)a.M * (uint64_t)a.N, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+  if (e != cudaSuccess) return e;
+  *kernel_name = "gemm_tc05_pair_f16ops_conv_im2col";
+  return launch_one<256, false, false, true, false, false, false, true>(a, cs, c_vec, ta, tx, tc, s);
 }
 
 cudaError_t launch_gemm_w8_bf16pair(const GemmF16Args& a, int w_k, cudaStream_t s, const char** kernel_name) {

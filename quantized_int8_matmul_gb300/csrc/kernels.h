@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 
@@ -75,9 +76,25 @@ struct GemmF16Args {
   // image, one slice per convolution group); per-row zero points and row sums
   // are then indexed (b % a_bmod) * M + row
   int a_bmod;
+  // implicit-GEMM convolution (launch_gemm_f16pair_conv): B is gathered per
+  // stage from an fp16 NHWC input by im2col tensor copies instead of read from
+  // B16. K runs over (tap row r, tap column s, 64-channel block) with the
+  // channel block fastest, N over the output pixels of one image (oh * oW +
+  // ow), and batch b is image b / cv_G, group b % cv_G.
+  int cv_oW, cv_sh, cv_sw, cv_pt, cv_pl, cv_dh, cv_dw, cv_kW;
+  int cv_cb;   // 64-channel blocks per group
+  int cv_G, cv_Cg;
 };
 cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool mmi, int chunk_k, cudaStream_t s,
                                 const char** kernel_name);
+// ConvInteger as an implicit GEMM on the same engine: A = the fp16 weight
+// [G][Mg][K] in (r, s, c) order, B = im2col copies of the fp16 NHWC input
+// described by tx (rank 4, {C, W, H, N}, 64 channels x 128 pixels, 128-byte
+// swizzle), C int32 [N * G][Mg][P]; the operands already hold x - x_zp and
+// w - w_zp, so the epilogue stores the exact sums unchanged.
+cudaError_t launch_gemm_f16pair_conv(const GemmF16Args& a, const CUtensorMap& tx, cudaStream_t s,
+                                     const char** kernel_name);
+
 // Form (a) on the same engine: C = scale[n] * (A @ W - zp[n] * rowsum(A)[m]),
 // A bf16 [M][K_eff] (K_eff = a.K: the weight's w_k, or 2*Kp for split fp32
 // activations), W the bf16 copy [w_k][N]; one fp32 accumulation over K_eff.
@@ -135,6 +152,15 @@ struct Im2colArgs {
 };
 size_t im2col_sum_scratch_bytes(long long Nb, long long G, long long H, long long W);
 cudaError_t launch_im2col(const Im2colArgs& a, bool x_u8, int* sum_scratch, cudaStream_t s);
+// Implicit-GEMM ConvInteger pre-passes (conv.cu): x [Nb][C][HW] (8-bit) ->
+// x16 [Nb][HW][C] fp16 holding x - x_zp (xzp: a device byte of the x type, or
+// null for 0); w [M][Cg][kH][kW] -> w16 [M][(r*kW + s)*Cg + c] fp16 holding
+// w - w_zp[m] (wzp: device bytes of the w type, wzp_count 0, 1 or M). Every
+// difference lies in [-255, 255], exact in fp16.
+cudaError_t launch_conv_x16(const void* x, bool u8, int Nb, int C, int HW, const void* xzp, __half* x16,
+                            cudaStream_t s);
+cudaError_t launch_conv_w16(const void* w, bool u8, int M, int Cg, int kH, int kW, const void* wzp, int wzp_count,
+                            __half* w16, cudaStream_t s);
 // rows x cols 8-bit (dense) -> fp16 at `pitch`, with optional int32 row sums.
 cudaError_t launch_rows_pitched(const void* src, bool u8, int rows, int cols, __half* dst, long long pitch,
                                 int* rowsum, cudaStream_t s);

@@ -6,6 +6,7 @@
 // ("What", last paragraph): the CUDA last-error state is cleared before a
 // launch and read back after it.
 #include "kernels.h"
+#include "tma.h"
 #include "../../include/qmm.h"
 
 #include <algorithm>
@@ -205,6 +206,10 @@ struct ConvPlan {
   int64_t P = 0, Pp = 0, Kg = 0, Kgp = 0;
   int64_t pt = 0, pl = 0, pb = 0, pr = 0, sh = 1, sw = 1, dh = 1, dw = 1;
   size_t off_col = 0, off_rs = 0, off_cs = 0, off_s = 0, bytes = 0;
+  // implicit-GEMM route: [w16: M x Kg fp16][x16: N x H x W x C fp16]
+  bool im2col_tma = false;
+  int lower[2] = {0, 0}, upper[2] = {0, 0};   // bounding-box corners, W then H
+  size_t off_x16 = 0;
 };
 
 ConvPlan conv_plan(int64_t N, int64_t C, int64_t H, int64_t W, int64_t M, int64_t kH, int64_t kW,
@@ -247,6 +252,26 @@ ConvPlan conv_plan(int64_t N, int64_t C, int64_t H, int64_t W, int64_t M, int64_
   pl.off_s = pl.off_cs + round256((size_t)N * G * pl.P * 4);
   pl.bytes = pl.off_s + round256(im2col_sum_scratch_bytes(N, G, H, W));
   pl.ok = true;
+  // The implicit GEMM (im2col tensor copies of an fp16 NHWC input) applies when
+  // a group's channels come in whole 64-channel boxes, the traversal strides
+  // and the window's bounding-box corners fit the copy's fields, and output
+  // rows are 16-byte multiples (the TMA-store epilogue). Otherwise the
+  // materialised im2col matrix above is used.
+  const int64_t Cg = C / G;
+  const int64_t lw = -pl.pl, lh = -pl.pt;
+  const int64_t uw = (int64_t)(pl.oW - 1) * pl.sw - pl.pl - (W - 1);
+  const int64_t uh = (int64_t)(pl.oH - 1) * pl.sh - pl.pt - (H - 1);
+  if (pl.P > 0 && Cg % 64 == 0 && pl.P % 4 == 0 && pl.sh <= 8 && pl.sw <= 8 && lw >= -128 && lh >= -128 &&
+      uw >= -128 && uw <= 127 && uh >= -128 && uh <= 127 && (kW - 1) * pl.dw <= 32767 && (kH - 1) * pl.dh <= 32767 &&
+      N * H * W * C <= ((int64_t)1 << 40)) {
+    pl.im2col_tma = true;
+    pl.lower[0] = (int)lw;
+    pl.lower[1] = (int)lh;
+    pl.upper[0] = (int)uw;
+    pl.upper[1] = (int)uh;
+    pl.off_x16 = round256((size_t)M * pl.Kg * 2);
+    pl.bytes = pl.off_x16 + round256((size_t)N * H * W * C * 2);
+  }
   return pl;
 }
 // The DynamicQuantizeLinear -> MatMulInteger -> dequantise chain. Workspace:
@@ -847,6 +872,47 @@ qmm_status conv_integer(const void* x, int x_dtype, const void* w, int w_dtype, 
   const bool xu = x_dtype == QMM_U8, wu = w_dtype == QMM_U8;
   uint8_t* base = static_cast<uint8_t*>(workspace);
   __half* w16 = reinterpret_cast<__half*>(base);
+  if (pl.im2col_tma) {
+    // implicit GEMM: the shifted operands in fp16, the input channels-innermost,
+    // then the pair GEMM gathering each stage's windows with im2col copies
+    __half* x16 = reinterpret_cast<__half*>(base + pl.off_x16);
+    const int Cg = (int)(C / group);
+    cudaError_t e = launch_conv_w16(w, wu, (int)M, Cg, (int)kH, (int)kW, w_zero_point, (int)w_zp_count, w16, s);
+    if (e == cudaSuccess) e = launch_conv_x16(x, xu, (int)N, (int)C, (int)(H * W), x_zero_point, x16, s);
+    CUtensorMap tx{};
+    if (e == cudaSuccess) {
+      const uint64_t dims[4] = {(uint64_t)C, (uint64_t)W, (uint64_t)H, (uint64_t)N};
+      const uint64_t strides[3] = {(uint64_t)C * 2, (uint64_t)W * C * 2, (uint64_t)H * W * C * 2};
+      const uint32_t es[4] = {1u, (uint32_t)pl.sw, (uint32_t)pl.sh, 1u};
+      e = make_tmap_im2col(&tx, x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, dims, strides, pl.lower, pl.upper, 64, 128,
+                           es, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
+    GemmF16Args f{};
+    f.A16 = w16;
+    f.a_bstride = group > 1 ? Mg * pl.Kg : 0;
+    f.a_bmod = group > 1 ? (int)group : 0;
+    f.batch = (int)batch;
+    f.M = (int)Mg;
+    f.K = (int)pl.Kg;
+    f.N = (int)pl.P;
+    f.C = y;
+    f.zp_row_mod = (int)Mg;
+    f.err = err;
+    f.cv_oW = pl.oW;
+    f.cv_sh = (int)pl.sh;
+    f.cv_sw = (int)pl.sw;
+    f.cv_pt = (int)pl.pt;
+    f.cv_pl = (int)pl.pl;
+    f.cv_dh = (int)pl.dh;
+    f.cv_dw = (int)pl.dw;
+    f.cv_kW = (int)kW;
+    f.cv_cb = Cg / 64;
+    f.cv_G = (int)group;
+    f.cv_Cg = Cg;
+    const char* gname = "none";
+    if (e == cudaSuccess) e = launch_gemm_f16pair_conv(f, tx, s, &gname);
+    return finish_launch(e, "conv_f16_nhwc+gemm_tc05_pair_f16ops_conv_im2col");
+  }
   __half* col = reinterpret_cast<__half*>(base + pl.off_col);
   int* rs = reinterpret_cast<int*>(base + pl.off_rs);
   int* cs = reinterpret_cast<int*>(base + pl.off_cs);

@@ -10,6 +10,25 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
+using EncodeIm2colFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                    const cuuint64_t*, const int*, const int*, cuuint32_t, cuuint32_t,
+                                    const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeIm2colFn encode_im2col_fn() {
+  static std::once_flag once;
+  static EncodeIm2colFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeIm2col", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeIm2colFn>(p);
+  });
+  return fn;
+}
+
 EncodeTiledFn encode_fn() {
   static std::once_flag once;
   static EncodeTiledFn fn = nullptr;
@@ -52,6 +71,25 @@ cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType
   const cuuint32_t elem_strides[3] = {1, 1, 1};
   const CUresult r = fn(map, dtype, 3, const_cast<void*>(base), dims, strides, box, elem_strides,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+cudaError_t make_tmap_im2col(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int rank,
+                             const uint64_t* dims, const uint64_t* strides_bytes, const int* lower, const int* upper,
+                             uint32_t channels, uint32_t pixels, const uint32_t* elem_strides,
+                             CUtensorMapSwizzle swizzle) {
+  EncodeIm2colFn fn = encode_im2col_fn();
+  if (!fn || rank < 3 || rank > 5) return cudaErrorInvalidValue;
+  cuuint64_t d[5], st[4];
+  cuuint32_t es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    es[i] = elem_strides[i];
+  }
+  for (int i = 0; i < rank - 1; ++i) st[i] = strides_bytes[i];
+  const CUresult r = fn(map, dtype, (cuuint32_t)rank, const_cast<void*>(base), d, st, lower, upper, channels, pixels,
+                        es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }

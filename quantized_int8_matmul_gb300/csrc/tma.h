@@ -24,4 +24,15 @@ cudaError_t make_tmap_3d(CUtensorMap* map, const void* base, CUtensorMapDataType
                          uint64_t mid, uint64_t outer, uint64_t mid_bytes, uint64_t outer_bytes,
                          uint32_t box_inner, uint32_t box_mid, CUtensorMapSwizzle swizzle);
 
+// Im2col variant (rank 3 to 5, channels innermost: {C, W, N}, {C, W, H, N} or
+// {C, W, H, D, N}): dims and elem_strides have `rank` entries, strides_bytes
+// rank - 1; lower / upper are the bounding-box corners of the base pixel
+// positions, innermost spatial dimension first (rank - 2 entries). A copy
+// delivers `pixels` rows of `channels` elements; elements outside the tensor
+// read as zero.
+cudaError_t make_tmap_im2col(CUtensorMap* map, const void* base, CUtensorMapDataType dtype, int rank,
+                             const uint64_t* dims, const uint64_t* strides_bytes, const int* lower, const int* upper,
+                             uint32_t channels, uint32_t pixels, const uint32_t* elem_strides,
+                             CUtensorMapSwizzle swizzle);
+
 }  // namespace qmm

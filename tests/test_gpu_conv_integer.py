@@ -1,5 +1,7 @@
-"""ConvInteger (im2col pre-pass + the SM-pair MatMulInteger GEMM) against the
-oracle, bit for bit: every signedness pair, zero points absent / scalar /
+"""ConvInteger against the oracle, bit for bit, on both routes -- the implicit
+GEMM (fp16 NHWC input gathered by im2col tensor copies, for groups of whole
+64-channel blocks) and the materialised im2col pre-pass + the SM-pair
+MatMulInteger GEMM (the other shapes): every signedness pair, zero points absent / scalar /
 per output channel, padding, strides, dilations, groups (depthwise
 included), rank-3 NCL inputs, output extents that leave ragged pixel tiles,
 long reductions at the exact-chunk edge, int32 wrap-around, empty outputs and
@@ -57,6 +59,68 @@ def test_conv_integer_matches_oracle(xdt, wdt, geom):
     got = run(c)
     assert q.last_kernel() == KERNEL
     assert_equal(got, want(c), f"conv {xdt}x{wdt} geometry {geom}")
+
+
+IM2COL = "conv_f16_nhwc+gemm_tc05_pair_f16ops_conv_im2col"
+TMA_GEOMETRIES = [
+    ((2, 64, 12, 12), (40, 64, 3, 3), [1, 1, 1, 1], [1, 1], [1, 1], 1),
+    ((1, 128, 18, 15), (72, 128, 3, 2), [2, 0, 1, 3], [2, 3], [1, 2], 1),     # asymmetric pads, strides, dilations
+    ((2, 128, 10, 10), (96, 64, 3, 3), [1, 2, 1, 0], [1, 1], [2, 1], 2),      # two groups of 64 channels
+    ((2, 64, 16, 30), (300, 64, 1, 1), [0, 0, 0, 0], [1, 1], [1, 1], 1),      # 1x1, M > 256: ragged pair row tile
+    ((1, 64, 30, 31), (16, 64, 7, 7), [3, 3, 3, 3], [2, 2], [1, 1], 1),       # 7x7, stride 2
+    ((2, 192, 14, 14), (64, 192, 5, 5), [2, 2, 2, 2], [1, 1], [1, 1], 1),     # K = 4800: many exact chunks
+    ((1, 64, 36, 36), (8, 64, 3, 3), [0, 1, 2, 0], [3, 2], [2, 3], 1),        # stride 3, dilation 3
+]
+
+
+@pytest.mark.parametrize("xdt,wdt", [("u8", "s8"), ("s8", "s8"), ("u8", "u8"), ("s8", "u8")])
+@pytest.mark.parametrize("geom", range(len(TMA_GEOMETRIES)))
+def test_conv_integer_implicit_gemm_matches_oracle(xdt, wdt, geom):
+    xs, ws, pads, strides, dils, group = TMA_GEOMETRIES[geom]
+    c = W.conv_integer_case(xs, ws, pads, strides, dils, group, seed=geom + 11 * len(xdt + wdt),
+                            x_dtype=DT[xdt], w_dtype=DT[wdt])
+    got = run(c)
+    assert q.last_kernel() == IM2COL
+    assert_equal(got, want(c), f"implicit-GEMM conv {xdt}x{wdt} geometry {geom}")
+
+
+@pytest.mark.parametrize("zp", ["none", "x", "w", "w1"])
+def test_conv_integer_implicit_gemm_zero_point_forms(zp):
+    c = W.conv_integer_case((2, 128, 10, 10), (96, 64, 3, 3), [1, 2, 1, 0], [1, 1], [2, 1], 2, seed=5)
+    assert_equal(run(c, zp), want(c, zp), f"implicit GEMM, zero points {zp}")
+    assert q.last_kernel() == IM2COL
+
+
+@pytest.mark.parametrize("L,k,pads,stride,dil", [(52, 3, [1, 1], 1, 1), (301, 5, [2, 0], 2, 2)])
+def test_conv_integer_implicit_gemm_rank3(L, k, pads, stride, dil):
+    c = W.conv_integer_case((3, 64, L), (40, 64, k), pads, [stride], [dil], 1, seed=L + 1)
+    got = run(c)
+    assert q.last_kernel() == IM2COL
+    assert_equal(got, want(c), f"implicit-GEMM rank-3 L={L} k={k}")
+
+
+def test_conv_integer_implicit_gemm_extremes_and_wrap():
+    """Shifted operands at the extremes (255 - 0 and -128 - 127): each exact
+    fp32 chunk of 256 taps sums to 256 * 65025 < 2^24; and a reduction long
+    enough to wrap int32."""
+    C = 1024
+    x = np.full((1, C, 4, 4), 255, np.uint8)
+    w = np.full((8, C, 3, 3), -128, np.int8)
+    c = W.ConvIntegerCase(x=x, w=w, x_zp=np.array([0], np.uint8), w_zp=np.full(8, 127, np.int8), pads=[1, 1, 1, 1],
+                          strides=None, dilations=None, group=1)
+    got = run(c)
+    assert q.last_kernel() == IM2COL
+    assert_equal(got, want(c), "extreme values, 9216 taps")
+    C = 4096
+    x = np.full((1, C, 4, 4), 255, np.uint8)
+    w = np.full((2, C, 3, 3), -128, np.int8)
+    c = W.ConvIntegerCase(x=x, w=w, x_zp=np.array([0], np.uint8), w_zp=np.array([127, 127], np.int8), pads=None,
+                          strides=None, dilations=None, group=1)
+    got = run(c)
+    assert q.last_kernel() == IM2COL
+    total = 255 * (-255) * C * 9
+    assert total < -2**31
+    assert (got == (total + 2**31) % 2**32 - 2**31).all()
 
 
 @pytest.mark.parametrize("zp", ["none", "x", "w", "w1"])

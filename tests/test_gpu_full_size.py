@@ -78,7 +78,7 @@ def test_conv_integer_full_size(case):
     y = q.conv_integer(dev(c.x), dev(c.w), dev(c.x_zp), dev(c.w_zp), pads=c.pads, strides=c.strides,
                        dilations=c.dilations, group=c.group)
     q.check_device_error()
-    assert q.last_kernel() == "im2col_f16+gemm_tc05_pair_f16ops_matmul_integer"
+    assert q.last_kernel() == "conv_f16_nhwc+gemm_tc05_pair_f16ops_conv_im2col"
     got = host(y)
     imgs = sample(c.x.shape[0], 2, 3)
     chans = sample(c.w.shape[0], 12, 4)
