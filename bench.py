@@ -548,7 +548,7 @@ def case_setups(q, torch, peaks):
                 tops = ops / (ms * 1e-3) / 1e12
                 return {"us": ms * 1e3, "value": tops, "unit": "TOPS", "frac_tensor": tops / tc,
                         "note": f"x {list(c.x.shape)} u8, w {list(c.w.shape)} s8, scalar x_zp, per-channel w_zp; "
-                                "im2col pre-pass + SM-pair MatMulInteger GEMM"}
+                                "implicit GEMM: fp16 NHWC input, im2col tensor copies into the SM-pair GEMM"}
             call = lambda: q.conv_integer(x, w, xz, wz, pads=c.pads, strides=c.strides,  # noqa: E731
                                           dilations=c.dilations, group=c.group, out=y, workspace=wsc)
             return call, True, report
