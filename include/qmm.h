@@ -94,11 +94,19 @@ qmm_status qmm_w8_dequant(const void* A, int a_dtype, const int8_t* B, int64_t M
  * activations are split into two bf16 parts (hi + lo, about 2^-16 relative)
  * along a doubled K that rereads the weight. Same accuracy bound as above.
  *
+ * For 3 to 16 bf16 rows (K % 8 == 0, N % 16 == 0) the workspace serves the
+ * decode GEMV instead: a pre-pass scales each activation row by the power of
+ * two that puts its largest magnitude in [2^14, 2^15) and stores it as exact
+ * fp16 (values below 2^-17 of the row maximum lose low bits, far inside the
+ * bound above), and the GEMV multiplies fp16 activations by the weight
+ * widened to fp16 in registers, undoing the row scale in its epilogue.
+ *
  *  workspace   at least qmm_w8_dequant_workspace_bytes(a_dtype, M, K, N) bytes,
  *              16-byte aligned, caller-owned.
- * The size function returns 0 when the path does not apply (M < 64, K or N
- * not a multiple of 16); the call then runs qmm_w8_dequant and ignores the
- * workspace. The same happens for an unaligned A (bf16: 16 bytes) or B.
+ * The size function returns 0 when neither path applies (M < 64 other than the
+ * decode rows above, K or N not a multiple of 16); the call then runs
+ * qmm_w8_dequant and ignores the workspace. The same happens for an unaligned
+ * A (bf16: 16 bytes) or B.
  */
 size_t qmm_w8_dequant_workspace_bytes(int a_dtype, int64_t M, int64_t K, int64_t N);
 qmm_status qmm_w8_dequant_ws(const void* A, int a_dtype, const int8_t* B, int64_t M, int64_t K, int64_t N,
@@ -270,11 +278,19 @@ qmm_status matmul_integer_ws(const void* A, int a_dtype, const void* B, int b_dt
  *  w_zero_point device, w_zp_count (0, 1 or M) values of w's type
  *  y            device int32 [N,M,oH,oW], oH = (H + pt + pb - dh*(kH-1) - 1)/sh + 1 (same for W)
  *  workspace    at least conv_integer_workspace_bytes(...) bytes, 16-byte aligned
- * Kernels: the weight as exact fp16 with its row sums, an im2col pre-pass that
- * writes each image's [C*kH*kW, oH*oW] matrix as exact fp16 (padded positions
+ * Kernels, when each group has a whole number of 64-channel blocks (C/group %
+ * 64 == 0), oH*oW % 4 == 0, strides <= 8 and the padded window's bounding box
+ * is within 128 pixels of the input's edges: an implicit GEMM. x - x_zp is
+ * written as fp16 channels-innermost (NHWC) and w - w_zp as fp16 in (kh, kw,
+ * c) order; the SM-pair GEMM gathers each stage's 128 output pixels x 64
+ * channels of one tap with an im2col tensor copy (padding reads as zero, i.e.
+ * as x_zp before the shift) and stores the exact sums into NCHW. Otherwise:
+ * the weight as exact fp16 with its row sums, an im2col pre-pass that writes
+ * each image's [C*kH*kW, oH*oW] matrix as exact fp16 (padded positions
  * holding x_zp) with its column sums, then the SM-pair MatMulInteger GEMM with
  * A = the weight (per-row zero point w_zp), B = the im2col matrix (zero point
  * x_zp), one batch per (image, group), its rows written straight into NCHW.
+ * conv_integer_workspace_bytes sizes the route the call will take.
  * Errors: QMM_ERR_INVALID_ARG for a bad dtype, geometry (group not dividing C
  * and M, non-positive extents, strides or dilations, negative pads), zero-point
  * count, null pointer or too small a workspace; QMM_ERR_UNSUPPORTED above
