@@ -316,12 +316,44 @@ __device__ __forceinline__ int zp_value(const void* zp, int i) {
   return U ? (int)static_cast<const uint8_t*>(zp)[i] : (int)static_cast<const int8_t*>(zp)[i];
 }
 
+// The weight's share of the launch below: one thread per element of
+// w16 [M][(r*kW + s)*Cg + c].
+struct ConvW16 {
+  const uint8_t* w;
+  int M, Cg, kH, kW;
+  const void* wzp;
+  int wzp_count;
+  __half* w16;
+};
+
+template <bool U>
+__device__ __forceinline__ void conv_w16_elements(const ConvW16& a, long long first, long long count) {
+  const long long Kg = (long long)a.kH * a.kW * a.Cg;
+  const long long total = (long long)a.M * Kg;
+  for (long long idx = first + threadIdx.x; idx < total && idx < first + count; idx += kThreads) {
+    const int m = (int)(idx / Kg);
+    const int k = (int)(idx - (long long)m * Kg);
+    const int tap = k / a.Cg, c = k - tap * a.Cg;
+    const int r = tap / a.kW, sx = tap - r * a.kW;
+    const int zp = a.wzp_count == 0 ? 0 : zp_value<U>(a.wzp, a.wzp_count == 1 ? 0 : m);
+    const int v = byte_value<U>(a.w[(((size_t)m * a.Cg + c) * a.kH + r) * a.kW + sx]);
+    a.w16[idx] = __int2half_rn(v - zp);
+  }
+}
+
 // One CTA per 64 pixels x 64 channels of one image, transposed through shared
 // memory: reads 64 channel rows of 64 bytes, writes 64 pixel rows of 64 fp16.
-template <bool U>
-__global__ void __launch_bounds__(kThreads) conv_x16_kernel(const uint8_t* __restrict__ x, int C, int HW,
-                                                            const void* xzp, __half* __restrict__ x16, bool vec) {
+// The CTAs of the last z slice (blockIdx.z == Nb) instead convert the weight,
+// w_per elements each, so both operands take one launch.
+template <bool U, bool WU>
+__global__ void __launch_bounds__(kThreads) conv_x16_kernel(const uint8_t* __restrict__ x, int C, int HW, int Nb,
+                                                            const void* xzp, __half* __restrict__ x16, bool vec,
+                                                            const ConvW16 wa, long long w_per) {
   asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
+  if ((int)blockIdx.z == Nb) {
+    conv_w16_elements<WU>(wa, ((long long)blockIdx.y * gridDim.x + blockIdx.x) * w_per, w_per);
+    return;
+  }
   __shared__ uint8_t tile[64][64 + 16];
   const int p0 = blockIdx.x * 64, c0 = blockIdx.y * 64, n = blockIdx.z;
   const int zp = xzp ? zp_value<U>(xzp, 0) : 0;
@@ -351,49 +383,25 @@ __global__ void __launch_bounds__(kThreads) conv_x16_kernel(const uint8_t* __res
   }
 }
 
-// One thread per element of w16 [M][(r*kW + s)*Cg + c].
-template <bool U>
-__global__ void __launch_bounds__(kThreads) conv_w16_kernel(const uint8_t* __restrict__ w, int M, int Cg, int kH,
-                                                            int kW, const void* wzp, int wzp_count,
-                                                            __half* __restrict__ w16) {
-  asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
-  const long long Kg = (long long)kH * kW * Cg;
-  const long long idx = (long long)blockIdx.x * kThreads + threadIdx.x;
-  if (idx >= (long long)M * Kg) return;
-  const int m = (int)(idx / Kg);
-  const int k = (int)(idx - (long long)m * Kg);
-  const int tap = k / Cg, c = k - tap * Cg;
-  const int r = tap / kW, sx = tap - r * kW;
-  const int zp = wzp_count == 0 ? 0 : zp_value<U>(wzp, wzp_count == 1 ? 0 : m);
-  const int v = byte_value<U>(w[(((size_t)m * Cg + c) * kH + r) * kW + sx]);
-  w16[idx] = __int2half_rn(v - zp);
-}
-
 }  // namespace convk
 
-cudaError_t launch_conv_x16(const void* x, bool u8, int Nb, int C, int HW, const void* xzp, __half* x16,
-                            cudaStream_t s) {
+cudaError_t launch_conv_operands(const void* x, bool xu, int Nb, int C, int HW, const void* xzp, __half* x16,
+                                 const void* w, bool wu, int M, int Cg, int kH, int kW, const void* wzp,
+                                 int wzp_count, __half* w16, cudaStream_t s) {
   using namespace convk;
-  if (Nb <= 0 || C <= 0 || HW <= 0) return cudaSuccess;
-  if (C % 64 != 0 || Nb > 65535 || C / 64 > 65535) return cudaErrorInvalidValue;
+  if (Nb <= 0 || C <= 0 || HW <= 0 || M <= 0) return cudaSuccess;
+  if (C % 64 != 0 || Nb >= 65535 || C / 64 > 65535) return cudaErrorInvalidValue;
   const bool vec = HW % 16 == 0 && (reinterpret_cast<uintptr_t>(x) % 16) == 0;
-  const dim3 grid((HW + 63) / 64, C / 64, Nb);
+  const dim3 grid((HW + 63) / 64, C / 64, Nb + 1);   // z == Nb: the weight, split over that slice's CTAs
+  const long long wtotal = (long long)M * kH * kW * Cg;
+  const long long slice = (long long)grid.x * grid.y;
+  const long long w_per = ((wtotal + slice - 1) / slice + kThreads - 1) / kThreads * kThreads;
+  ConvW16 wa{static_cast<const uint8_t*>(w), M, Cg, kH, kW, wzp, wzp_count, w16};
   const uint8_t* p = static_cast<const uint8_t*>(x);
-  if (u8) conv_x16_kernel<true><<<grid, kThreads, 0, s>>>(p, C, HW, xzp, x16, vec);
-  else conv_x16_kernel<false><<<grid, kThreads, 0, s>>>(p, C, HW, xzp, x16, vec);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_conv_w16(const void* w, bool u8, int M, int Cg, int kH, int kW, const void* wzp, int wzp_count,
-                            __half* w16, cudaStream_t s) {
-  using namespace convk;
-  const long long total = (long long)M * kH * kW * Cg;
-  if (total <= 0) return cudaSuccess;
-  const long long blocks = (total + kThreads - 1) / kThreads;
-  if (blocks > INT_MAX) return cudaErrorInvalidValue;
-  const uint8_t* p = static_cast<const uint8_t*>(w);
-  if (u8) conv_w16_kernel<true><<<(unsigned)blocks, kThreads, 0, s>>>(p, M, Cg, kH, kW, wzp, wzp_count, w16);
-  else conv_w16_kernel<false><<<(unsigned)blocks, kThreads, 0, s>>>(p, M, Cg, kH, kW, wzp, wzp_count, w16);
+  if (xu && wu) conv_x16_kernel<true, true><<<grid, kThreads, 0, s>>>(p, C, HW, Nb, xzp, x16, vec, wa, w_per);
+  else if (xu) conv_x16_kernel<true, false><<<grid, kThreads, 0, s>>>(p, C, HW, Nb, xzp, x16, vec, wa, w_per);
+  else if (wu) conv_x16_kernel<false, true><<<grid, kThreads, 0, s>>>(p, C, HW, Nb, xzp, x16, vec, wa, w_per);
+  else conv_x16_kernel<false, false><<<grid, kThreads, 0, s>>>(p, C, HW, Nb, xzp, x16, vec, wa, w_per);
   return cudaGetLastError();
 }
 

@@ -157,10 +157,10 @@ cudaError_t launch_im2col(const Im2colArgs& a, bool x_u8, int* sum_scratch, cuda
 // null for 0); w [M][Cg][kH][kW] -> w16 [M][(r*kW + s)*Cg + c] fp16 holding
 // w - w_zp[m] (wzp: device bytes of the w type, wzp_count 0, 1 or M). Every
 // difference lies in [-255, 255], exact in fp16.
-cudaError_t launch_conv_x16(const void* x, bool u8, int Nb, int C, int HW, const void* xzp, __half* x16,
-                            cudaStream_t s);
-cudaError_t launch_conv_w16(const void* w, bool u8, int M, int Cg, int kH, int kW, const void* wzp, int wzp_count,
-                            __half* w16, cudaStream_t s);
+// Both in one launch (the weight's CTAs ride along in an extra z slice).
+cudaError_t launch_conv_operands(const void* x, bool xu, int Nb, int C, int HW, const void* xzp, __half* x16,
+                                 const void* w, bool wu, int M, int Cg, int kH, int kW, const void* wzp,
+                                 int wzp_count, __half* w16, cudaStream_t s);
 // rows x cols 8-bit (dense) -> fp16 at `pitch`, with optional int32 row sums.
 cudaError_t launch_rows_pitched(const void* src, bool u8, int rows, int cols, __half* dst, long long pitch,
                                 int* rowsum, cudaStream_t s);

@@ -877,8 +877,8 @@ qmm_status conv_integer(const void* x, int x_dtype, const void* w, int w_dtype, 
     // then the pair GEMM gathering each stage's windows with im2col copies
     __half* x16 = reinterpret_cast<__half*>(base + pl.off_x16);
     const int Cg = (int)(C / group);
-    cudaError_t e = launch_conv_w16(w, wu, (int)M, Cg, (int)kH, (int)kW, w_zero_point, (int)w_zp_count, w16, s);
-    if (e == cudaSuccess) e = launch_conv_x16(x, xu, (int)N, (int)C, (int)(H * W), x_zero_point, x16, s);
+    cudaError_t e = launch_conv_operands(x, xu, (int)N, (int)C, (int)(H * W), x_zero_point, x16, w, wu, (int)M, Cg,
+                                         (int)kH, (int)kW, w_zero_point, (int)w_zp_count, w16, s);
     CUtensorMap tx{};
     if (e == cudaSuccess) {
       const uint64_t dims[4] = {(uint64_t)C, (uint64_t)W, (uint64_t)H, (uint64_t)N};
