@@ -65,6 +65,7 @@ struct Shared {
   uint64_t acc_full[2];   // per accumulator buffer: the pair's commit
   uint64_t acc_empty[2];  // even CTA: one arrival per drain warp of both CTAs
   uint64_t teardown;
+  uint64_t accld[NEW][2];   // accumulating A8W8: per drain warp, its two acc_in staging buffers
   uint32_t tmem_base;
   int abort_flag;
   // per drain warp, the current tile's operands of its CPW columns:
@@ -76,8 +77,9 @@ struct Shared {
   float col_bias[NEW][CPW_MAX];
 };
 
-// Ring stages of an instantiation: the 4-byte-output (MatMulInteger) ones give
-// one stage to the C staging buffers of their TMA-store epilogue.
+// Ring stages of an instantiation: the MatMulInteger ones (4-byte outputs) and
+// the accumulating A8W8 one give one stage to per-warp staging buffers (C for
+// the TMA-store epilogue, acc_in for the accumulator's TMA loads).
 template <bool TS>
 __host__ __device__ constexpr int ring_stages() { return TS ? NS - 1 : NS; }
 template <bool TS>
@@ -88,7 +90,7 @@ static_assert(smem_bytes<false>() <= 232448 && smem_bytes<true>() <= 232448, "sh
 
 enum : unsigned {
   SITE_EMPTY = 0x400, SITE_FULL = 0x401, SITE_ACC_FULL = 0x402, SITE_ACC_EMPTY = 0x403, SITE_TEARDOWN = 0x404,
-  SITE_FINAL = 0x405
+  SITE_FINAL = 0x405, SITE_ACCLD = 0x407
 };
 
 struct TileCoord {
@@ -371,6 +373,106 @@ __device__ __forceinline__ void epilogue_tma(const GemmF16Args& p, const Shared&
   }
 }
 
+// Accumulating A8W8 epilogue with acc_in arriving by TMA: per 16-column group
+// one lane copies the warp's 32 rows x 16 int32 of acc_in into a staging
+// buffer (64-byte swizzle, two buffers, the next group's copy in flight while
+// this one is used), every lane adds its row's 16 values to its sums, then
+// acc_out (optional) and the scaled C are stored as in the plain epilogue.
+// Coalesced box copies replace 28 per-lane 16-byte loads of separate rows,
+// which filled the load queue and held up the drains. nacc counts this warp's
+// copies (buffer = count & 1, phase parity = (count >> 1) & 1).
+template <int CPW>
+__device__ __forceinline__ void epilogue_acc_tma(const GemmF16Args& p, Shared& sm, uint32_t (&sums)[CPW],
+                                                 const TileCoord tc, int warp, int q, int h, int lane, int c_vec,
+                                                 uint32_t stg, const CUtensorMap* tm_acc, int& nacc) {
+  const int row0 = tc.m0 + q * 32;
+  if (row0 >= p.M) return;   // warp-uniform
+  const int row = row0 + lane;
+  const bool rv = row < p.M;
+  const size_t crow = ((size_t)tc.b * p.M + (size_t)(rv ? row : 0)) * (size_t)p.N;
+  const uint64_t pol = l2_policy_evict_first();
+  const float as = (p.C && rv) ? __ldg(p.act_scale + (p.act_count == 1 ? 0 : row % p.zp_row_mod)) : 0.f;
+  const int n_first = tc.n0 + h * CPW;
+  const int ng = p.N > n_first ? min(CPW / 16, (p.N - n_first + 15) / 16) : 0;
+  auto issue = [&](int gi) {
+    if (lane == 0) {
+      const int k = nacc + gi, buf = k & 1;
+      mbar_arrive_expect_tx(&sm.accld[warp][buf], 32u * 16u * 4u);
+      tma_load_3d(stg + (uint32_t)buf * 2048u, tm_acc, n_first + 16 * gi, row0, tc.b, &sm.accld[warp][buf]);
+    }
+  };
+  if (ng > 0) issue(0);
+  if (ng > 1) issue(1);
+  const uint32_t swz = (uint32_t)((lane >> 1) & 3);
+#pragma unroll
+  for (int g = 0; g < CPW / 16; ++g) {
+    if (g >= ng) break;
+    const int nb = n_first + g * 16;
+    const int k = nacc + g, buf = k & 1;
+    uint32_t* o = &sums[g * 16];
+    if (mbar_wait(&sm.accld[warp][buf], (uint32_t)((k >> 1) & 1), &sm.abort_flag, p.err, SITE_ACCLD)) {
+      const uint32_t b = stg + (uint32_t)buf * 2048u + (uint32_t)lane * 64u;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const uint4 x = ld_shared_v4(b + (((uint32_t)j ^ swz) << 4));
+        o[4 * j] += x.x;
+        o[4 * j + 1] += x.y;
+        o[4 * j + 2] += x.z;
+        o[4 * j + 3] += x.w;
+      }
+    }
+    fence_proxy_async_smem();   // this buffer's reads are done before the next copy overwrites it
+    __syncwarp();
+    if (g + 2 < ng) issue(g + 2);
+    if (!rv) continue;
+    const bool full_acc = (nb + 16 <= p.N) && (c_vec & 2);
+    if (p.acc_out) {
+      int* dst = p.acc_out + crow + nb;
+      if (full_acc) {
+#pragma unroll
+        for (int i = 0; i < 16; i += 4) st_global_v4_hint(dst + i, o[i], o[i + 1], o[i + 2], o[i + 3], pol);
+      } else {
+        for (int i = 0; i < 16; ++i)
+          if (nb + i < p.N) dst[i] = (int)o[i];
+      }
+    }
+    if (!p.C) continue;
+    const bool full = (nb + 16 <= p.N) && (c_vec & 1);
+    float f[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      f[i] = __fmul_rn(__fmul_rn(__int2float_rn((int)o[i]), as), __uint_as_float(sm.col_op[warp][g * 16 + i]));
+    if (p.c_f32) {
+      float* out = reinterpret_cast<float*>(p.C) + crow + nb;
+      if (full) {
+#pragma unroll
+        for (int i = 0; i < 16; i += 4)
+          st_global_v4_hint(out + i, __float_as_uint(f[i]), __float_as_uint(f[i + 1]), __float_as_uint(f[i + 2]),
+                            __float_as_uint(f[i + 3]), pol);
+      } else {
+        for (int i = 0; i < 16; ++i)
+          if (nb + i < p.N) out[i] = f[i];
+      }
+    } else {
+      __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.C) + crow + nb;
+      uint32_t pk[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+        pk[i] = *reinterpret_cast<uint32_t*>(&b2);
+      }
+      if (full) {
+        st_global_v4_hint(out, pk[0], pk[1], pk[2], pk[3], pol);
+        st_global_v4_hint(out + 8, pk[4], pk[5], pk[6], pk[7], pol);
+      } else {
+        for (int i = 0; i < 16; ++i)
+          if (nb + i < p.N) out[i] = __float2bfloat16_rn(f[i]);
+      }
+    }
+  }
+  nacc += ng;
+}
+
 // Accumulating A8W8: start this thread's running sums (one row, CPW columns)
 // from the caller's int32 accumulator (0 outside the problem). Issued before
 // the wait for the tile's first chunk, so the loads overlap the MMAs.
@@ -405,7 +507,8 @@ __global__ void __launch_bounds__(NT, 1)
     gemm_f16pair_kernel(const GemmF16Args p, const int cs, const int c_vec, const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, const __grid_constant__ CUtensorMap tmC) {
   constexpr bool TS = MMI;                 // 4-byte outputs leave through the TMA-store epilogue
-  constexpr int kNS = ring_stages<TS>();
+  constexpr bool STG = MMI || ACC;         // per-warp staging buffers (C out, or acc_in in)
+  constexpr int kNS = ring_stages<STG>();
   constexpr int BNH = BN / 2;   // B columns of each CTA
   constexpr int CPW = BN / 2;   // accumulator columns per drain warp
   static_assert(BN % 32 == 0 && BN <= BN_MAX && BNH <= 128, "pair tile width");
@@ -414,7 +517,7 @@ __global__ void __launch_bounds__(NT, 1)
   const uint32_t sbase = (raw + 1023u) & ~1023u;
   uint8_t* sbase_ptr = smem_raw + (sbase - raw);
   const uint32_t stg_base = sbase + (uint32_t)(kNS * STAGE_BYTES);   // C staging (TS), 1024-byte aligned
-  Shared& sm = *reinterpret_cast<Shared*>(sbase_ptr + kNS * STAGE_BYTES + (TS ? STG_TOTAL : 0));
+  Shared& sm = *reinterpret_cast<Shared*>(sbase_ptr + kNS * STAGE_BYTES + (STG ? STG_TOTAL : 0));
 
   const int t = threadIdx.x;
   const int warp = t >> 5;
@@ -442,6 +545,10 @@ __global__ void __launch_bounds__(NT, 1)
       mbar_init(&sm.acc_empty[i], PAIR_ARRIVALS);
     }
     mbar_init(&sm.teardown, 1);
+    for (int i = 0; i < NEW; ++i) {
+      mbar_init(&sm.accld[i][0], 1);
+      mbar_init(&sm.accld[i][1], 1);
+    }
     sm.abort_flag = 0;
     fence_mbarrier_init();
   }
@@ -556,13 +663,15 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t acc_empty_leader0 = mapa_shared(smem_u32(&sm.acc_empty[0]), 0);
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     uint32_t sums[CPW];
-    int nst = 0;   // TMA stores this warp has issued
+    int nst = 0;    // TMA stores this warp has issued
+    int nacc = 0;   // acc_in copies this warp has issued
     int tl = 0, c = 0;
     TileCoord tc = tile_coord<BN>(p, 0, cid, ncl, (int)rank);
     if (my_tiles > 0) stage_columns<CPW, BU, MMI, FA, ACC, DQ>(p, sm, tc, warp, h, lane);
     for (int d = 0; d < total_chunks; ++d) {
       const int ab = d & 1;
-      if (ACC && c == 0) preload_acc<CPW>(p, tc, q, h, lane, sums, c_vec);
+      // acc_in joins the sums before the first chunk, or in the epilogue by TMA (c_vec bit 2)
+      if (ACC && c == 0 && !(c_vec & 4)) preload_acc<CPW>(p, tc, q, h, lane, sums, c_vec);
       if (!mbar_wait_cluster(&sm.acc_full[ab], (uint32_t)((d >> 1) & 1), &sm.abort_flag, p.err, SITE_ACC_FULL))
         break;
       tc_fence_after();
@@ -578,7 +687,7 @@ __global__ void __launch_bounds__(NT, 1)
             sums[g * 16 + i] = acc[i];
           } else {
             const uint32_t v = (uint32_t)__float2int_rn(__uint_as_float(acc[i]));
-            sums[g * 16 + i] = (c == 0 && !ACC) ? v : sums[g * 16 + i] + v;
+            sums[g * 16 + i] = (c == 0 && (!ACC || (c_vec & 4))) ? v : sums[g * 16 + i] + v;
           }
         }
       }
@@ -589,6 +698,9 @@ __global__ void __launch_bounds__(NT, 1)
         if (TS && (c_vec & 1))
           epilogue_tma<CPW, AU, BU, DQ>(p, sm, sums, tc, warp, q, h, lane, stg_base + (uint32_t)warp * STG_BYTES,
                                         &tmC, nst);
+        else if (ACC && (c_vec & 4))
+          epilogue_acc_tma<CPW>(p, sm, sums, tc, warp, q, h, lane, c_vec, stg_base + (uint32_t)warp * STG_BYTES,
+                                &tmC, nacc);
         else
           epilogue<CPW, AU, BU, MMI, FA, ACC, DQ>(p, sm, sums, tc, warp, q, h, lane, c_vec);
         __syncwarp();   // the warp's staged operands are read: restage for the next tile
@@ -633,7 +745,7 @@ struct DeviceLaunchInfo {
 template <int BN, bool AU, bool BU, bool MMI, bool FA = false, bool ACC = false, bool DQ = false, bool CV = false>
 cudaError_t launch_one(const GemmF16Args& a, int cs, int c_vec, const CUtensorMap& ta, const CUtensorMap& tb,
                        const CUtensorMap& tc, cudaStream_t s) {
-  constexpr size_t SMEM_BYTES = smem_bytes<MMI>();
+  constexpr size_t SMEM_BYTES = smem_bytes<MMI || ACC>();
   auto kern = gemm_f16pair_kernel<BN, AU, BU, MMI, FA, ACC, DQ, CV>;
   static std::mutex mu;
   static DeviceLaunchInfo info[64];
@@ -744,7 +856,7 @@ cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool
   const int cs = chunk_k / BK;
   const int celem = (mmi || a.c_f32) ? 4 : 2;
   const bool acc_al = ((reinterpret_cast<uintptr_t>(a.acc_in) | reinterpret_cast<uintptr_t>(a.acc_out)) % 16) == 0;
-  const int c_vec = (((reinterpret_cast<uintptr_t>(a.C) % 16) == 0) && (((long long)a.N * celem) % 16 == 0) ? 1 : 0) |
+  int c_vec = (((reinterpret_cast<uintptr_t>(a.C) % 16) == 0) && (((long long)a.N * celem) % 16 == 0) ? 1 : 0) |
                     ((acc_al && a.N % 4 == 0) ? 2 : 0);
   CUtensorMap ta{}, tb{}, tc{};
   cudaError_t e = make_maps(a, &ta, &tb);
@@ -753,6 +865,14 @@ cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool
     e = make_tmap_3d(&tc, a.C, CU_TENSOR_MAP_DATA_TYPE_INT32, (uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.batch,
                      4ull * (uint64_t)a.N, 4ull * (uint64_t)a.M * (uint64_t)a.N, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
     if (e != cudaSuccess) return e;
+  }
+  // accumulating A8W8: acc_in as {N, M, batch} int32, box 16 x 32, copied in by
+  // the epilogue (c_vec bit 2) when its rows are 16-byte multiples
+  if (!mmi && a.acc_in && (reinterpret_cast<uintptr_t>(a.acc_in) % 16) == 0 && a.N % 4 == 0) {
+    e = make_tmap_3d(&tc, a.acc_in, CU_TENSOR_MAP_DATA_TYPE_INT32, (uint64_t)a.N, (uint64_t)a.M, (uint64_t)a.batch,
+                     4ull * (uint64_t)a.N, 4ull * (uint64_t)a.M * (uint64_t)a.N, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
+    if (e != cudaSuccess) return e;
+    c_vec |= 4;
   }
   *kernel_name = mmi ? (a.act_scale ? "gemm_tc05_pair_f16ops_matmul_integer_dequant"
                            : "gemm_tc05_pair_f16ops_matmul_integer")
