@@ -176,6 +176,39 @@ qmm_status qmm_a8w8_packed(int64_t M, int64_t K, int64_t N, const float* act_sca
                            size_t workspace_bytes, void* stream);
 
 /*
+ * qmm_a8w8 from HOST buffers, with the copies overlapped with the work: the
+ * same operation and bit-identical results as qmm_a8w8_ws, for callers whose
+ * operands and result live in host memory.
+ *
+ *  hA, hB                 host int8 [M,K] and [K,N]
+ *  h_act_scale            host float[act_count], 1 or M
+ *  h_weight_scale         host float[w_count], 1 or N
+ *  hC                     host [M,N] float (QMM_F32) or bf16 bits (QMM_BF16)
+ *  workspace              device, at least qmm_a8w8_host_workspace_bytes(...)
+ *                         bytes, 16-byte aligned: the device copies of the
+ *                         operands, scales and result, then the two-pass
+ *                         path's workspace
+ * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
+ * the copies to run asynchronously; they must stay valid and unchanged until
+ * the work on `stream` completes (hC is written by then).
+ * Where the two-pass path applies (qmm_a8w8_workspace_bytes(M, K, N) > 0), A
+ * is processed in row panels sized so each panel's pair tiles fill whole
+ * waves of the GPU: B, the scales and A's panels are copied in on one internal
+ * copy stream, each panel's pre-pass and GEMM run on `stream` as soon as its
+ * rows have arrived, and each panel's rows of C are copied back on a second
+ * internal stream as soon as they are written, so the copies in both
+ * directions overlap the GEMMs of the other panels. Elsewhere the call copies
+ * in, runs qmm_a8w8 and copies out on `stream`. Calls on one device enqueue one
+ * at a time (the internal streams and events are shared).
+ * Errors: as qmm_a8w8_ws, plus QMM_ERR_CUDA when a copy cannot be enqueued.
+ */
+size_t qmm_a8w8_host_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t act_count, int64_t w_count,
+                                     int c_dtype);
+qmm_status qmm_a8w8_host(const int8_t* hA, const int8_t* hB, int64_t M, int64_t K, int64_t N,
+                         const float* h_act_scale, int64_t act_count, const float* h_weight_scale, int64_t w_count,
+                         void* hC, int c_dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Accumulating A8W8. PyPTO PR #1920, "What Changed", "A8W8 matmul-dequant-acc
  * op" (an INT32 accumulator input beside the INT8 operands, [M] or [M,1]
  * activation scales, [N] or [1,N] weight scales, FP32 or BF16 output, a_trans /

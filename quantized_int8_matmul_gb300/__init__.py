@@ -68,6 +68,9 @@ def _load() -> ctypes.CDLL:
     lib.dynamic_quantize_matmul.argtypes = [vp, i64, i64, vp, ci, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, sz, vp]
     lib.qmm_a8w8_pack.argtypes = [vp, vp, i64, i64, i64, vp, sz, vp]
     lib.qmm_a8w8_packed.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, ci, vp, sz, vp]
+    lib.qmm_a8w8_host_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, ci]
+    lib.qmm_a8w8_host_workspace_bytes.restype = sz
+    lib.qmm_a8w8_host.argtypes = [vp, vp, i64, i64, i64, vp, i64, vp, i64, vp, ci, vp, sz, vp]
     lib.matmul_integer_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, i64]
     lib.matmul_integer_workspace_bytes.restype = sz
     lib.matmul_integer_ws.argtypes = [vp, ci, vp, ci, i64, i64, i64, i64, i64, i64, vp, i64, vp, i64, vp, vp, sz, vp]
@@ -228,6 +231,46 @@ def qmm_a8w8_pack(A, B, workspace, stream=None):
     st = _lib.qmm_a8w8_pack(_ptr(A), _ptr(B), M, K, N, _ptr(workspace), workspace.numel() * workspace.element_size(),
                             _stream(stream))
     _check("qmm_a8w8_pack", st)
+
+
+def _need_host(t, dtypes, name):
+    if t.is_cuda:
+        raise ValueError(f"{name} must be a host (CPU) tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype} not in {dtypes}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def qmm_a8w8_host_workspace_bytes(M, K, N, act_count, w_count, out_dtype=torch.bfloat16) -> int:
+    return int(_lib.qmm_a8w8_host_workspace_bytes(M, K, N, act_count, w_count, _TORCH_TO_QMM[out_dtype]))
+
+
+def qmm_a8w8_host(A, B, act_scale, weight_scale, out=None, out_dtype=torch.bfloat16, stream=None,
+                  workspace="auto"):
+    """qmm_a8w8 on host (CPU) tensors: the copies to and from the GPU are
+    pipelined with the computation (row panels of A). Pinned host tensors let
+    the copies run asynchronously; the result is complete once `stream` (the
+    current CUDA stream by default) has finished. workspace: "auto" or a CUDA
+    uint8 tensor of at least qmm_a8w8_host_workspace_bytes(...) bytes."""
+    _need_host(A, (torch.int8,), "A")
+    _need_host(B, (torch.int8,), "B")
+    _need_host(act_scale, (torch.float32,), "act_scale")
+    _need_host(weight_scale, (torch.float32,), "weight_scale")
+    M, K = A.shape
+    K2, N = B.shape
+    if K2 != K:
+        raise ValueError("inner dimensions differ")
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, pin_memory=True)
+    _need_host(out, (torch.float32, torch.bfloat16), "out")
+    nbytes = qmm_a8w8_host_workspace_bytes(M, K, N, act_scale.numel(), weight_scale.numel(), out.dtype)
+    ws, wsb = _workspace(workspace, nbytes, torch.device("cuda", torch.cuda.current_device()))
+    st = _lib.qmm_a8w8_host(_ptr(A), _ptr(B), M, K, N, _ptr(act_scale), act_scale.numel(), _ptr(weight_scale),
+                            weight_scale.numel(), _ptr(out), _TORCH_TO_QMM[out.dtype], _ptr(ws), wsb,
+                            _stream(stream))
+    _check("qmm_a8w8_host", st)
+    return out
 
 
 def qmm_a8w8_packed(M, K, N, act_scale, weight_scale, workspace, out=None, out_dtype=torch.bfloat16, stream=None):

@@ -749,6 +749,188 @@ qmm_status qmm_a8w8_packed(int64_t M, int64_t K, int64_t N, const float* act_sca
                        kPackedA8W8);
 }
 
+// ---------------------------------------------------------------------------
+// A8W8 from host buffers: the copies pipelined with the two-pass GEMM.
+// ---------------------------------------------------------------------------
+namespace {
+
+constexpr int kHostMaxPanels = 8;
+
+// Device layout of the host call's workspace: the operands, scales and output
+// on the device, then the two-pass path's workspace.
+struct HostPlan {
+  bool two_pass = false;
+  int64_t Mp = 0;   // rows per panel
+  int panels = 0;
+  size_t off_b = 0, off_act = 0, off_w = 0, off_c = 0, off_pack = 0, bytes = 0;
+  PrepassPlan pl;
+};
+
+HostPlan host_plan(int64_t M, int64_t K, int64_t N, int64_t act_count, int64_t w_count, int c_dtype) {
+  HostPlan h;
+  const size_t celem = c_dtype == QMM_F32 ? 4 : 2;
+  h.off_b = round256((size_t)M * K);
+  h.off_act = h.off_b + round256((size_t)K * N);
+  h.off_w = h.off_act + round256((size_t)std::max<int64_t>(act_count, 1) * 4);
+  h.off_c = h.off_w + round256((size_t)std::max<int64_t>(w_count, 1) * 4);
+  h.off_pack = h.off_c + round256((size_t)M * N * celem);
+  h.pl = prepass_plan(1, M, K, N, 0, 0, M);
+  h.two_pass = h.pl.use;
+  h.bytes = h.off_pack + (h.two_pass ? h.pl.bytes : 0);
+  if (h.two_pass) {
+    // row panels whose pair tiles fill whole waves of the resident pairs: the
+    // copy of panel i + 1 and the read-back of panel i - 1 overlap panel i's GEMM
+    const int64_t n_tiles = (N + 223) / 224;   // pair tiles across N at the narrower tile width
+    const int64_t pairs = std::max(1, num_sms() / 2);
+    int64_t Mp = std::max<int64_t>(1, pairs / n_tiles) * 256;
+    Mp = std::max(Mp, (M + kHostMaxPanels - 1) / kHostMaxPanels);
+    Mp = (Mp + 255) / 256 * 256;
+    h.Mp = Mp;
+    h.panels = (int)((M + Mp - 1) / Mp);
+  }
+  return h;
+}
+
+// Per device: the copy streams and events of the pipeline, made once. A mutex
+// serialises the enqueueing of calls on one device (the events are reused).
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t in[kHostMaxPanels] = {}, out[kHostMaxPanels] = {};
+  std::mutex mu;
+};
+HostPipe g_pipe[kMaxDevices];
+
+cudaError_t host_pipe(int dev, HostPipe** out) {
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  HostPipe& h = g_pipe[dev];
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!h.ready) {
+    const unsigned ef = cudaEventDisableTiming;
+    cudaError_t e = cudaStreamCreateWithFlags(&h.h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h.d2h, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.start, ef);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.done, ef);
+    for (int i = 0; i < kHostMaxPanels && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&h.in[i], ef);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.out[i], ef);
+    }
+    if (e != cudaSuccess) return e;
+    h.ready = true;
+  }
+  *out = &h;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+size_t qmm_a8w8_host_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t act_count, int64_t w_count,
+                                     int c_dtype) {
+  if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N) || M == 0 || N == 0) return 0;
+  if (c_dtype != QMM_F32 && c_dtype != QMM_BF16) return 0;
+  return host_plan(M, K, N, act_count, w_count, c_dtype).bytes;
+}
+
+qmm_status qmm_a8w8_host(const int8_t* hA, const int8_t* hB, int64_t M, int64_t K, int64_t N,
+                         const float* h_act_scale, int64_t act_count, const float* h_weight_scale, int64_t w_count,
+                         void* hC, int c_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return QMM_ERR_INVALID_ARG;
+  if (c_dtype != QMM_F32 && c_dtype != QMM_BF16) return QMM_ERR_INVALID_ARG;
+  if (act_count != 1 && act_count != M) return QMM_ERR_INVALID_ARG;
+  if (w_count != 1 && w_count != N) return QMM_ERR_INVALID_ARG;
+  if (M == 0 || N == 0) {
+    t_last_kernel = "none";
+    return QMM_OK;
+  }
+  if (!h_act_scale || !h_weight_scale || !hC || (K > 0 && (!hA || !hB))) return QMM_ERR_INVALID_ARG;
+  const HostPlan hp = host_plan(M, K, N, act_count, w_count, c_dtype);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < hp.bytes) return QMM_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  int8_t* dA = reinterpret_cast<int8_t*>(base);
+  int8_t* dB = reinterpret_cast<int8_t*>(base + hp.off_b);
+  float* dAct = reinterpret_cast<float*>(base + hp.off_act);
+  float* dW = reinterpret_cast<float*>(base + hp.off_w);
+  uint8_t* dC = base + hp.off_c;
+  const size_t celem = c_dtype == QMM_F32 ? 4 : 2;
+  const int8_t* cA = static_cast<const int8_t*>(hA);
+  uint8_t* cC = static_cast<uint8_t*>(hC);
+  cudaGetLastError();
+  if (!hp.two_pass) {
+    // outside the two-pass path: copy in, one fused kernel, copy out
+    cudaError_t e = cudaMemcpyAsync(dA, hA, (size_t)M * K, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dB, hB, (size_t)K * N, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dAct, h_act_scale, (size_t)act_count * 4, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(dW, h_weight_scale, (size_t)w_count * 4, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return finish_launch(e, "none");
+    const qmm_status st = qmm_a8w8(dA, dB, M, K, N, dAct, act_count, dW, w_count, dC, c_dtype, stream);
+    if (st != QMM_OK) return st;
+    const char* name = t_last_kernel;
+    e = cudaMemcpyAsync(hC, dC, (size_t)M * N * celem, cudaMemcpyDeviceToHost, s);
+    return finish_launch(e, name);
+  }
+  unsigned* err = err_word();
+  if (!err) return QMM_ERR_CUDA;
+  HostPipe* hpipe = nullptr;
+  cudaError_t e = host_pipe(current_device(), &hpipe);
+  if (e != cudaSuccess) return finish_launch(e, "none");
+  std::lock_guard<std::mutex> lk(hpipe->mu);
+  uint8_t* pbase = base + hp.off_pack;
+  __half* a16 = reinterpret_cast<__half*>(pbase);
+  __half* b16 = reinterpret_cast<__half*>(pbase + hp.pl.off_b);
+  // copies in, on the copy stream after the caller's earlier work: B and the
+  // scales, then A panel by panel
+  e = cudaEventRecord(hpipe->start, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hpipe->h2d, hpipe->start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hpipe->d2h, hpipe->start, 0);
+  if (e == cudaSuccess) e = cudaMemcpyAsync(dB, hB, (size_t)K * N, cudaMemcpyHostToDevice, hpipe->h2d);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(dW, h_weight_scale, (size_t)w_count * 4, cudaMemcpyHostToDevice, hpipe->h2d);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(dAct, h_act_scale, (size_t)act_count * 4, cudaMemcpyHostToDevice, hpipe->h2d);
+  for (int i = 0; i < hp.panels && e == cudaSuccess; ++i) {
+    const int64_t r0 = i * hp.Mp, rows = std::min(hp.Mp, M - r0);
+    e = cudaMemcpyAsync(dA + r0 * K, cA + r0 * K, (size_t)rows * K, cudaMemcpyHostToDevice, hpipe->h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(hpipe->in[i], hpipe->h2d);
+  }
+  // per panel on the caller's stream: pack (with B on the first), GEMM; its
+  // rows of C go back on the second copy stream as soon as they are written
+  const char* gname = "none";
+  for (int i = 0; i < hp.panels && e == cudaSuccess; ++i) {
+    const int64_t r0 = i * hp.Mp, rows = std::min(hp.Mp, M - r0);
+    e = cudaStreamWaitEvent(s, hpipe->in[i], 0);
+    if (e == cudaSuccess)
+      e = launch_convert_bulk(dA + r0 * K, false, a16 + r0 * K, rows * K, dB, false, b16, i == 0 ? K * N : 0,
+                              err, s);
+    GemmF16Args f{};
+    f.A16 = a16 + r0 * K;
+    f.B16 = b16;
+    f.batch = 1;
+    f.M = (int)rows;
+    f.K = (int)K;
+    f.N = (int)N;
+    f.C = dC + (size_t)r0 * N * celem;
+    f.c_f32 = c_dtype == QMM_F32;
+    f.act_scale = dAct + (act_count == 1 ? 0 : r0);
+    f.act_count = (int)act_count;
+    f.w_scale = dW;
+    f.w_count = (int)w_count;
+    f.zp_row_mod = (int)rows;
+    f.err = err;
+    if (e == cudaSuccess) e = launch_gemm_f16pair(f, false, false, false, chunk_k_for(false, false), s, &gname);
+    if (e == cudaSuccess) e = cudaEventRecord(hpipe->out[i], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hpipe->d2h, hpipe->out[i], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(cC + (size_t)r0 * N * celem, dC + (size_t)r0 * N * celem, (size_t)rows * N * celem,
+                          cudaMemcpyDeviceToHost, hpipe->d2h);
+  }
+  // the caller's stream resumes once the last rows are back
+  if (e == cudaSuccess) e = cudaEventRecord(hpipe->done, hpipe->d2h);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hpipe->done, 0);
+  return finish_launch(e, "h2d_pipelined+f16_prepass+gemm_tc05_pair_f16ops_a8w8");
+}
+
 size_t qmm_a8w8_acc_workspace_bytes(int64_t M, int64_t K, int64_t N) {
   if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return 0;
   const size_t general = acc_plan(M, K, N).bytes;
