@@ -126,3 +126,34 @@ def test_dql_rejects_bad_arguments(qmm):
     assert call(n=10**7, wb=8) == qmm.QMM_ERR_INVALID_ARG                # workspace too small
     assert call(rs=P, rl=7) == qmm.QMM_ERR_INVALID_ARG                   # 100 % 7 != 0
     assert call(rs=P, rl=0) == qmm.QMM_ERR_INVALID_ARG
+
+
+def test_a8w8_host_workspace_holds_the_operands_and_the_two_pass_workspace(qmm):
+    lib = qmm.lib()
+    M, K, N = 4096, 4096, 4096
+    host = lib.qmm_a8w8_host_workspace_bytes(M, K, N, M, N, qmm.QMM_BF16)
+    operands = M * K + K * N + 4 * (M + N) + 2 * M * N
+    assert host >= operands + lib.qmm_a8w8_workspace_bytes(M, K, N)
+    # outside the two-pass path: the device copies only
+    small = lib.qmm_a8w8_host_workspace_bytes(100, 64, 64, 1, 1, qmm.QMM_F32)
+    assert 100 * 64 + 64 * 64 + 4 * 100 * 64 <= small < 100 * 64 + 64 * 64 + 4 * 100 * 64 + 6 * 256
+    assert lib.qmm_a8w8_host_workspace_bytes(M, K, N, M, N, 7) == 0      # not an output type
+    assert lib.qmm_a8w8_host_workspace_bytes(0, K, N, 1, 1, qmm.QMM_BF16) == 0
+
+
+def test_a8w8_host_rejects_bad_arguments(qmm):
+    lib = qmm.lib()
+    ws = ctypes.c_void_p(4096)
+
+    def call(M=4, K=8, N=8, ac=1, wc=1, c=1, A=P, C=P, w=ws, wb=1 << 20):
+        return lib.qmm_a8w8_host(A, P, M, K, N, P, ac, P, wc, C, c, w, wb, None)
+
+    assert call(ac=3) == qmm.QMM_ERR_INVALID_ARG
+    assert call(wc=2) == qmm.QMM_ERR_INVALID_ARG
+    assert call(c=2) == qmm.QMM_ERR_INVALID_ARG
+    assert call(A=None) == qmm.QMM_ERR_INVALID_ARG
+    assert call(C=None) == qmm.QMM_ERR_INVALID_ARG
+    assert call(w=None) == qmm.QMM_ERR_INVALID_ARG
+    assert call(w=ctypes.c_void_p(4100)) == qmm.QMM_ERR_INVALID_ARG      # workspace not 16-byte aligned
+    assert call(wb=64) == qmm.QMM_ERR_INVALID_ARG                        # workspace too small
+    assert call(N=0) == qmm.QMM_OK
