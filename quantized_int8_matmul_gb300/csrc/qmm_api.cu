@@ -116,6 +116,54 @@ void fold_batch(int64_t batch, int64_t M, int64_t K, int64_t a_bstride, int64_t 
   }
 }
 
+// A second stream per device for a pre-pass that does not depend on the one on
+// the caller's stream (B's conversion beside A's): forked after the caller's
+// earlier work, joined before the GEMM. The events are reused, so a mutex
+// covers the enqueueing from fork to join.
+struct AuxStream {
+  bool ready = false;
+  cudaStream_t s = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex mu;
+};
+AuxStream g_aux[kMaxDevices];
+
+AuxStream* aux_stream() {
+  const int d = current_device();
+  if (d < 0 || d >= kMaxDevices) return nullptr;
+  AuxStream& a = g_aux[d];
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!a.ready) {
+    if (cudaStreamCreateWithFlags(&a.s, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a.fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&a.join, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return nullptr;
+    }
+    a.ready = true;
+  }
+  return &a;
+}
+
+// Runs side(aux stream) and main(s) concurrently, s continuing after both; on
+// any failure to fork, both run in order on s.
+template <class Side, class Main>
+cudaError_t fork_join(cudaStream_t s, Side side, Main main) {
+  AuxStream* ax = aux_stream();
+  if (!ax) {
+    cudaError_t e = side(s);
+    return e == cudaSuccess ? main(s) : e;
+  }
+  std::lock_guard<std::mutex> lk(ax->mu);
+  cudaError_t e = cudaEventRecord(ax->fork, s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ax->s, ax->fork, 0);
+  if (e == cudaSuccess) e = side(ax->s);
+  if (e == cudaSuccess) e = cudaEventRecord(ax->join, ax->s);
+  if (e == cudaSuccess) e = main(s);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ax->join, 0);
+  return e;
+}
+
 // The pre-pass: fp16 copies of A and B (and the sums the zero points need).
 cudaError_t run_pack(const PrepassPlan& pl, const void* A, bool au, const void* B, bool bu, bool need_rs,
                      bool need_cs, void* ws, int K, int N, cudaStream_t s) {
@@ -126,11 +174,16 @@ cudaError_t run_pack(const PrepassPlan& pl, const void* A, bool au, const void* 
   int* cs = reinterpret_cast<int*>(base + pl.off_cs);
   if (!need_rs && !need_cs)   // one launch for both operands, staged by bulk copies
     return launch_convert_bulk(A, au, a16, pl.rowsA * K, B, bu, b16, pl.matsB * K * N, err_word(), s);
-  cudaError_t e = need_rs ? launch_convert_rows(A, au, a16, pl.rowsA, K, rs, s)
-                          : launch_convert_flat(A, au, a16, pl.rowsA * K, nullptr, bu, nullptr, 0, s);
-  if (e != cudaSuccess) return e;
-  if (need_cs) return launch_convert_cols(B, bu, b16, (int)pl.matsB, K, N, cs, s);
-  return launch_convert_flat(nullptr, au, nullptr, 0, B, bu, b16, pl.matsB * K * N, s);
+  // with sums, A's and B's conversions are separate kernels: run them side by side
+  auto side = [&](cudaStream_t st) {
+    return need_cs ? launch_convert_cols(B, bu, b16, (int)pl.matsB, K, N, cs, st)
+                   : launch_convert_flat(nullptr, au, nullptr, 0, B, bu, b16, pl.matsB * K * N, st);
+  };
+  auto main = [&](cudaStream_t st) {
+    return need_rs ? launch_convert_rows(A, au, a16, pl.rowsA, K, rs, st)
+                   : launch_convert_flat(A, au, a16, pl.rowsA * K, nullptr, bu, nullptr, 0, st);
+  };
+  return fork_join(s, side, main);
 }
 
 // The GEMM on packed operands.
@@ -1185,20 +1238,21 @@ qmm_status dynamic_quantize_matmul(const float* x, int64_t M, int64_t K, const v
   int* cs = reinterpret_cast<int*>(base + pl.off_cs);
   float* ys = y_scale ? y_scale : reinterpret_cast<float*>(base + pl.off_sz);
   uint8_t* yz = y_zero_point ? y_zero_point : base + pl.off_sz + 16;
-  // the weight: exact fp16 copy and column sums (the y_zp term)
-  cudaError_t e;
-  if (N % 16 == 0 && aligned16(W)) {
-    e = launch_convert_cols(W, wu, b16, 1, (int)K, (int)N, cs, s);
-  } else {
+  // the weight (exact fp16 copy and column sums, the y_zp term) on a side stream,
+  // beside the activations' DynamicQuantizeLinear straight into the fp16
+  // operand with rowsum(y)
+  auto side = [&](cudaStream_t st) {
+    if (N % 16 == 0 && aligned16(W)) return launch_convert_cols(W, wu, b16, 1, (int)K, (int)N, cs, st);
     const ConvPlane none{nullptr, 0, 0, 0, 0, nullptr, 0};
     const ConvPlane pb{W, N, (int)K, (int)N, 0, b16, pl.Np};
-    e = launch_convert_planes(none, false, pb, wu, s);
-    if (e == cudaSuccess) e = launch_colsum(W, wu, (int)K, (int)N, cs, s);
-  }
-  // the activations: DynamicQuantizeLinear straight into the fp16 operand, with rowsum(y)
-  if (e == cudaSuccess)
-    e = launch_dql_rows_f16(x, M, K, a16, pl.Kp, ys, yz, rs, reinterpret_cast<float*>(base),
-                            dql_num_partials(M * K), s);
+    cudaError_t e2 = launch_convert_planes(none, false, pb, wu, st);
+    return e2 == cudaSuccess ? launch_colsum(W, wu, (int)K, (int)N, cs, st) : e2;
+  };
+  auto main = [&](cudaStream_t st) {
+    return launch_dql_rows_f16(x, M, K, a16, pl.Kp, ys, yz, rs, reinterpret_cast<float*>(base),
+                               dql_num_partials(M * K), st);
+  };
+  cudaError_t e = fork_join(s, side, main);
   GemmF16Args f{};
   f.A16 = a16;
   f.B16 = b16;

@@ -106,6 +106,38 @@ def test_captured_call_replays_exactly():
         assert_equal(host(out), O.a8w8(w.A, w.B, w.act_scale, w.weight_scale, "bf16"), "graph replay")
 
 
+def test_captured_matmul_integer_with_zero_points_replays_exactly():
+    """With zero points the two conversions run on two streams (forked and
+    joined with events); captured into a CUDA graph, the fork and join become
+    graph edges and replays with new inputs stay exact."""
+    rng = np.random.default_rng(17)
+    M, K, N = 600, 512, 400
+    A0, B0 = rand(rng, "u8", (M, K)), rand(rng, "s8", (K, N))
+    a_zp, b_zp = rand(rng, "u8", (1,)), rand(rng, "s8", (N,))
+    A, B, za, zb = dev(A0), dev(B0), dev(a_zp), dev(b_zp)
+    out = torch.empty((M, N), dtype=torch.int32, device="cuda")
+    ws = torch.empty(q.matmul_integer_workspace_bytes(1, M, K, N, 0, 0), dtype=torch.uint8, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        q.matmul_integer(A, B, za, zb, out=out, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, capture_error_mode="relaxed"):
+        q.matmul_integer(A, B, za, zb, out=out, workspace=ws)
+    assert q.last_kernel() == TWO_PASS_MMI
+    for seed in (1, 2):
+        r = np.random.default_rng(seed)
+        An, Bn = rand(r, "u8", (M, K)), rand(r, "s8", (K, N))
+        A.copy_(dev(An))
+        B.copy_(dev(Bn))
+        g.replay()
+        torch.cuda.synchronize()
+        q.check_device_error()
+        assert_equal(host(out), O.matmul_integer(An, Bn, a_zp, b_zp), f"graph replay {seed}")
+
+
 @pytest.mark.parametrize("adt,bdt", [("s8", "s8"), ("u8", "s8"), ("s8", "u8"), ("u8", "u8")])
 @pytest.mark.parametrize("zp", ["none", "scalar", "vector", "a_only", "b_only"])
 @pytest.mark.parametrize("M,K,N", [(260, 1040, 272), (513, 272, 400)])
