@@ -145,21 +145,21 @@ AuxStream* aux_stream() {
   return &a;
 }
 
-// Runs side(aux stream) and main(s) concurrently, s continuing after both; on
-// any failure to fork, both run in order on s.
-template <class Side, class Main>
-cudaError_t fork_join(cudaStream_t s, Side side, Main main) {
+// Runs side(aux stream) and primary(s) concurrently, s continuing after both;
+// when no side stream can be made, both run in order on s.
+template <class Side, class Primary>
+cudaError_t fork_join(cudaStream_t s, Side side, Primary primary) {
   AuxStream* ax = aux_stream();
   if (!ax) {
     cudaError_t e = side(s);
-    return e == cudaSuccess ? main(s) : e;
+    return e == cudaSuccess ? primary(s) : e;
   }
   std::lock_guard<std::mutex> lk(ax->mu);
   cudaError_t e = cudaEventRecord(ax->fork, s);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(ax->s, ax->fork, 0);
   if (e == cudaSuccess) e = side(ax->s);
   if (e == cudaSuccess) e = cudaEventRecord(ax->join, ax->s);
-  if (e == cudaSuccess) e = main(s);
+  if (e == cudaSuccess) e = primary(s);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ax->join, 0);
   return e;
 }
@@ -179,11 +179,11 @@ cudaError_t run_pack(const PrepassPlan& pl, const void* A, bool au, const void* 
     return need_cs ? launch_convert_cols(B, bu, b16, (int)pl.matsB, K, N, cs, st)
                    : launch_convert_flat(nullptr, au, nullptr, 0, B, bu, b16, pl.matsB * K * N, st);
   };
-  auto main = [&](cudaStream_t st) {
+  auto primary = [&](cudaStream_t st) {
     return need_rs ? launch_convert_rows(A, au, a16, pl.rowsA, K, rs, st)
                    : launch_convert_flat(A, au, a16, pl.rowsA * K, nullptr, bu, nullptr, 0, st);
   };
-  return fork_join(s, side, main);
+  return fork_join(s, side, primary);
 }
 
 // The GEMM on packed operands.
@@ -1248,11 +1248,11 @@ qmm_status dynamic_quantize_matmul(const float* x, int64_t M, int64_t K, const v
     cudaError_t e2 = launch_convert_planes(none, false, pb, wu, st);
     return e2 == cudaSuccess ? launch_colsum(W, wu, (int)K, (int)N, cs, st) : e2;
   };
-  auto main = [&](cudaStream_t st) {
+  auto primary = [&](cudaStream_t st) {
     return launch_dql_rows_f16(x, M, K, a16, pl.Kp, ys, yz, rs, reinterpret_cast<float*>(base),
                                dql_num_partials(M * K), st);
   };
-  cudaError_t e = fork_join(s, side, main);
+  cudaError_t e = fork_join(s, side, primary);
   GemmF16Args f{};
   f.A16 = a16;
   f.B16 = b16;
