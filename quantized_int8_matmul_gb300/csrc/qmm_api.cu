@@ -849,7 +849,7 @@ HostPlan host_plan(int64_t M, int64_t K, int64_t N, int64_t act_count, int64_t w
 struct HostPipe {
   bool ready = false;
   cudaStream_t h2d = nullptr, d2h = nullptr;
-  cudaEvent_t start = nullptr, done = nullptr;
+  cudaEvent_t start = nullptr, done = nullptr, b_in = nullptr;
   cudaEvent_t in[kHostMaxPanels] = {}, out[kHostMaxPanels] = {};
   std::mutex mu;
 };
@@ -865,6 +865,7 @@ cudaError_t host_pipe(int dev, HostPipe** out) {
     if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&h.d2h, cudaStreamNonBlocking);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.start, ef);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.done, ef);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.b_in, ef);
     for (int i = 0; i < kHostMaxPanels && e == cudaSuccess; ++i) {
       e = cudaEventCreateWithFlags(&h.in[i], ef);
       if (e == cudaSuccess) e = cudaEventCreateWithFlags(&h.out[i], ef);
@@ -942,20 +943,23 @@ qmm_status qmm_a8w8_host(const int8_t* hA, const int8_t* hB, int64_t M, int64_t 
     e = cudaMemcpyAsync(dW, h_weight_scale, (size_t)w_count * 4, cudaMemcpyHostToDevice, hpipe->h2d);
   if (e == cudaSuccess)
     e = cudaMemcpyAsync(dAct, h_act_scale, (size_t)act_count * 4, cudaMemcpyHostToDevice, hpipe->h2d);
+  if (e == cudaSuccess) e = cudaEventRecord(hpipe->b_in, hpipe->h2d);
   for (int i = 0; i < hp.panels && e == cudaSuccess; ++i) {
     const int64_t r0 = i * hp.Mp, rows = std::min(hp.Mp, M - r0);
     e = cudaMemcpyAsync(dA + r0 * K, cA + r0 * K, (size_t)rows * K, cudaMemcpyHostToDevice, hpipe->h2d);
     if (e == cudaSuccess) e = cudaEventRecord(hpipe->in[i], hpipe->h2d);
   }
-  // per panel on the caller's stream: pack (with B on the first), GEMM; its
-  // rows of C go back on the second copy stream as soon as they are written
+  // on the caller's stream: B's conversion as soon as B has arrived (while the
+  // first panel of A is still being copied), then per panel its pre-pass and
+  // GEMM; its rows of C go back on the second copy stream as soon as written
   const char* gname = "none";
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hpipe->b_in, 0);
+  if (e == cudaSuccess) e = launch_convert_bulk(nullptr, false, nullptr, 0, dB, false, b16, K * N, err, s);
   for (int i = 0; i < hp.panels && e == cudaSuccess; ++i) {
     const int64_t r0 = i * hp.Mp, rows = std::min(hp.Mp, M - r0);
     e = cudaStreamWaitEvent(s, hpipe->in[i], 0);
     if (e == cudaSuccess)
-      e = launch_convert_bulk(dA + r0 * K, false, a16 + r0 * K, rows * K, dB, false, b16, i == 0 ? K * N : 0,
-                              err, s);
+      e = launch_convert_bulk(dA + r0 * K, false, a16 + r0 * K, rows * K, nullptr, false, nullptr, 0, err, s);
     GemmF16Args f{};
     f.A16 = a16 + r0 * K;
     f.B16 = b16;
