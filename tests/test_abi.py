@@ -157,3 +157,39 @@ def test_a8w8_host_rejects_bad_arguments(qmm):
     assert call(w=ctypes.c_void_p(4100)) == qmm.QMM_ERR_INVALID_ARG      # workspace not 16-byte aligned
     assert call(wb=64) == qmm.QMM_ERR_INVALID_ARG                        # workspace too small
     assert call(N=0) == qmm.QMM_OK
+
+
+def _i64s(*v):
+    return (ctypes.c_int64 * len(v))(*v)
+
+
+def test_conv_workspace_follows_the_route(qmm):
+    """Groups of whole 64-channel blocks take the implicit GEMM, whose workspace
+    holds the fp16 NHWC input and weight only; other shapes hold the im2col
+    matrix, which is larger by about the kernel's tap count."""
+    lib = qmm.lib()
+    pads, strides, dils = _i64s(1, 1, 1, 1), _i64s(1, 1), _i64s(1, 1)
+    N, C, H, W, M = 8, 256, 56, 56, 256
+    implicit = lib.conv_integer_workspace_bytes(N, C, H, W, M, 3, 3, pads, strides, dils, 1)
+    assert 2 * (N * H * W * C + M * C * 9) <= implicit < 2 * (N * H * W * C + M * C * 9) + 1024
+    # 48 channels per group: not whole 64-channel blocks -> the im2col matrix (9x the input in fp16)
+    im2col = lib.conv_integer_workspace_bytes(N, 48, H, W, M, 3, 3, pads, strides, dils, 1)
+    assert im2col >= 2 * N * 48 * 9 * H * W
+    # an output row that is not a 16-byte multiple (oH*oW % 4 != 0) also takes the im2col route
+    odd = lib.conv_integer_workspace_bytes(1, 64, 5, 5, 8, 3, 3, pads, strides, dils, 1)
+    assert odd >= 2 * 64 * 9 * 25
+
+
+def test_w8_dequant_workspace_follows_the_route(qmm):
+    lib = qmm.lib()
+    K, N = 8192, 28672
+    kp = (K + 15) // 16 * 16
+    for M in (3, 4, 16):   # decode rows, bf16: the GEMV's fp16 activations and row scales
+        b = lib.qmm_w8_dequant_workspace_bytes(qmm.QMM_BF16, M, K, N)
+        assert 2 * M * kp <= b <= 2 * M * kp + 512
+    for M in (1, 2):       # one or two rows keep the CUDA-core kernel: no workspace
+        assert lib.qmm_w8_dequant_workspace_bytes(qmm.QMM_BF16, M, K, N) == 0
+    assert lib.qmm_w8_dequant_workspace_bytes(qmm.QMM_F32, 4, K, N) == 0     # fp32 decode rows
+    assert lib.qmm_w8_dequant_workspace_bytes(qmm.QMM_BF16, 4, K + 4, N) == 0  # K % 8 != 0
+    # prefill (M >= 64): the exact bf16 weight copy
+    assert lib.qmm_w8_dequant_workspace_bytes(qmm.QMM_BF16, 4096, K, N) >= 2 * K * N
