@@ -175,50 +175,124 @@ def time_gpu_split(first, second, steps, warmup, flush=None):
     return [a.elapsed_time(c) for a, b, c in ev], [b.elapsed_time(c) for a, b, c in ev]
 
 
-def cpu_baseline_a8w8(budget_s=12.0, max_rows=4096):
-    """The oracle as it stands on a bounded sample of rows of the 4096^3 workload."""
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+_ORACLE_W = None
+
+
+def _oracle_worker_init():
+    """Process-pool worker: one copy of the 4096^3 A8W8 workload per process."""
+    global _ORACLE_W
+    _ORACLE_W = W.a8w8_4096()
+
+
+def _oracle_rows(task):
+    """The oracle as it stands on rows [r0, r1) x all columns; returns the seconds taken."""
     from oracle import qmm_oracle as O
-    w = W.a8w8_4096()
-    rows, t = 0, 0.0
-    step = 8
-    while t < budget_s and rows < max_rows:
-        sl = slice(rows, rows + step)
+    r0, r1 = task
+    w = _ORACLE_W
+    t0 = time.perf_counter()
+    O.a8w8(w.A[r0:r1], w.B, w.act_scale[r0:r1], w.weight_scale, "bf16")
+    return time.perf_counter() - t0
+
+
+def oracle_pool(cores):
+    """A spawn pool (never forked from a process that holds a CUDA context), one
+    single-threaded oracle process per host core, each with the workload loaded."""
+    import multiprocessing as mp
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    pool = mp.get_context("spawn").Pool(cores, initializer=_oracle_worker_init)
+    pool.map(_oracle_rows, [(0, 1)] * cores)   # every worker loaded and warm
+    return pool
+
+
+def cpu_baseline_a8w8(budget_s=12.0, rows_per_task=4):
+    """The oracle as it stands, on all host cores, over a bounded sample of the
+    rows of the 4096^3 workload (row blocks handed out until the budget is spent)."""
+    cores = host_cores()
+    pool = oracle_pool(cores)
+    try:
+        tasks = [(r, r + rows_per_task) for r in range(0, M, rows_per_task)]
+        rows, t_end = 0, 0.0
         t0 = time.perf_counter()
-        O.a8w8(w.A[sl], w.B, w.act_scale[sl], w.weight_scale, "bf16")
-        t += time.perf_counter() - t0
-        rows += step
+        for _ in pool.imap_unordered(_oracle_rows, tasks):
+            rows += rows_per_task
+            t_end = time.perf_counter() - t0
+            if t_end > budget_s:
+                break
+    finally:
+        pool.terminate()
+        pool.join()
     ops = 2.0 * rows * K * N
-    return {"value": ops / t / 1e12, "unit": "TOPS", "cores": 1, "kind": "oracle",
-            "sample": f"{rows} of 4096 rows of the 4096^3 A8W8 workload (numpy int64 matmul + float32 "
-                      f"epilogue, single thread), {t:.1f} s"}
+    return {"value": ops / t_end / 1e12, "unit": "TOPS", "cores": cores, "kind": "oracle",
+            "sample": f"{rows} of 4096 rows of the 4096^3 A8W8 workload in blocks of {rows_per_task} rows, one "
+                      f"single-threaded oracle process per host core (numpy int64 matmul + float32 epilogue), "
+                      f"{t_end:.1f} s wall"}
 
 
 def run_reference(args, rank):
+    """The oracle on the host cores, each step one output row (all 4096 columns)
+    per core of the 4096^3 A8W8 workload."""
     if rank != 0:
         return
-    from oracle import qmm_oracle as O
-    w = W.a8w8_4096()
+    cores = host_cores()
+    pool = oracle_pool(cores)
     times = []
-    cols = 512                      # one step: one row x 512 columns of the output
-    for i in range(args.warmup + args.steps):
-        r = i % M
-        c0 = (i * cols) % N
-        t0 = time.perf_counter()
-        O.a8w8(w.A[r:r + 1], w.B[:, c0:c0 + cols], w.act_scale[r:r + 1], w.weight_scale[c0:c0 + cols], "bf16")
-        dt = time.perf_counter() - t0
-        if i >= args.warmup:
-            times.append(dt)
-    per_step_ops = 2.0 * K * cols
+    try:
+        for i in range(args.warmup + args.steps):
+            r0 = (i * cores) % M
+            tasks = [((r0 + c) % M, (r0 + c) % M + 1) for c in range(cores)]
+            t0 = time.perf_counter()
+            pool.map(_oracle_rows, tasks)
+            dt = time.perf_counter() - t0
+            if i >= args.warmup:
+                times.append(dt)
+    finally:
+        pool.terminate()
+        pool.join()
+    per_step_ops = 2.0 * K * N * cores
     mean = statistics.mean(times)
     value = per_step_ops / mean / 1e12
+    sample = f"{cores} output rows x 4096 columns of the 4096^3 A8W8 workload per step, one row per host core"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TOPS", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "int64 (oracle)", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "step": "one row x 512 columns of the output"},
-            "cpu_baseline": {"value": value, "unit": "TOPS", "cores": 1, "kind": "oracle",
-                             "sample": "one row x 512 columns of the 4096^3 A8W8 workload per step"},
+            "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "step": sample},
+            "cpu_baseline": {"value": value, "unit": "TOPS", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def int8_mma_peak(q, torch, launches=6, iters=4096):
+    """Rate of the legacy int8 tensor path (mma.sync m16n8k32 s8) measured with
+    CUDA events: the median of `launches` timed launches after one warm-up."""
+    q.int8_mma_peak_launch(64)
+    torch.cuda.synchronize()
+    rates = []
+    for _ in range(launches):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        ops = q.int8_mma_peak_launch(iters)
+        b.record()
+        b.synchronize()
+        rates.append(ops / (a.elapsed_time(b) * 1e-3) / 1e12)
+    return statistics.median(rates)
+
+
+def cublas_int8_tops(torch, A, B, steps=20):
+    """cuBLAS int8 GEMM (torch._int_mm, int32 out) on the same operands, for context."""
+    try:
+        torch._int_mm(A, B)
+        torch.cuda.synchronize()
+        ts = time_gpu(lambda: torch._int_mm(A, B), steps, 3)
+        return OPS / (statistics.median(ts) * 1e-3) / 1e12
+    except (RuntimeError, AttributeError):
+        return None
 
 
 def main():
@@ -343,6 +417,13 @@ def main():
     h2d = hA.numel() + hB.numel() + 4 * (ha.numel() + hw.numel())
     d2h = 2 * hC.numel()
 
+    # the int8 denominators the metric names: the legacy int8 tensor path's
+    # rate (mma.sync s8, measured here), and cuBLAS's int8 GEMM on the operands
+    t0p = time.time()
+    imma_tops = int8_mma_peak(q, torch)
+    cublas_tops = cublas_int8_tops(torch, A, B)
+    clocks.mark(t0p, time.time())
+
     rows = {}
     if not args.no_secondary:
         rows = secondary(q, torch, flush, clocks, peaks)
@@ -368,13 +449,18 @@ def main():
         "roofline": {"bound": "tensor", "kernel": gemm_kernel, "achieved": achieved, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                      "traffic": kernel_traffic(gemm_kernel), "kernel_ms": gemm_ms,
-                     "peak_source": f"{peaks_src} dense bf16 (burst); fp16 kind::f16 runs at the same rate"},
+                     "peak_source": f"{peaks_src} dense bf16 (burst); fp16 kind::f16 runs at the same rate",
+                     "int8_imma_peak": imma_tops, "frac_int8_imma": achieved / imma_tops,
+                     "int8_peak_source": "measured in this run: mma.sync m16n8k32 s8 (sm_103a has no tcgen05 "
+                                         "kind::i8); the exact fp16 tcgen05 path runs above it",
+                     "cublas_int8_gemm_tops": cublas_tops},
         "cpu_baseline": cpu,
         "e2e": {"value": world * OPS / (e2e_ms * 1e-3) / 1e12, "unit": "TOPS", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,   # per step: the pre-pass + the GEMM
         "clocks": clk,
         "rows": rows,
+        "configs": config_summary(rows, value, mean_ms, achieved, peaks, imma_tops),
     }
     print(json.dumps(line), flush=True)
     if dist is not None:
@@ -577,14 +663,43 @@ def case_setups(q, torch, peaks):
             "conv_integer_1d_k3_4x512x3000": conv(W.conv1d_k3_4x512x3000)}
 
 
-SECONDARY = ["a8w8_4096x4096x4096_bf16_single_pass", "decode_gemv_M1", "decode_gemv_M4", "decode_gemv_M16",
-             "dql_8192x4096",
-             "matmul_integer_8192x4096x11008", "batched_matmul_integer_65536x1024x1024",
-             "w8_prefill_bf16_4096x8192x28672", "w8_dequant_f32_64x256x192", "a8w8_acc_4096x4096x4096_bf16",
-             "a8w8_acc_4096x4096x4096_bf16_b_trans", "a8w8_acc_decode_M1_8192x28672_b_trans",
-             "a8w8_acc_decode_M1_8192x28672", "a8w8_acc_decode_M16_8192x28672_b_trans",
-             "conv_integer_3x3_8x256x56x56", "conv_integer_1d_k3_4x512x3000",
-             "dql_matmul_dequant_fused_8192x4096x11008"]
+# The rows beyond the five configurations first, then the five (their compact
+# summary closes the JSON line).
+SECONDARY = ["a8w8_4096x4096x4096_bf16_single_pass", "w8_prefill_bf16_4096x8192x28672",
+             "a8w8_acc_4096x4096x4096_bf16", "a8w8_acc_4096x4096x4096_bf16_b_trans",
+             "a8w8_acc_decode_M1_8192x28672_b_trans", "a8w8_acc_decode_M1_8192x28672",
+             "a8w8_acc_decode_M16_8192x28672_b_trans", "conv_integer_3x3_8x256x56x56",
+             "conv_integer_1d_k3_4x512x3000", "dql_matmul_dequant_fused_8192x4096x11008",
+             "w8_dequant_f32_64x256x192", "dql_8192x4096", "matmul_integer_8192x4096x11008",
+             "batched_matmul_integer_65536x1024x1024", "decode_gemv_M1", "decode_gemv_M4", "decode_gemv_M16"]
+
+
+def config_summary(rows, value, step_ms, gemm_achieved, peaks, imma_tops):
+    """Compact figures of the five benchmark configurations (the line's last key)."""
+    def r3(v):
+        return None if v is None else float(f"{v:.3g}")
+
+    def pick(name, *keys):
+        r = rows.get(name)
+        if r is None:
+            return None
+        out = {k: r3(r[k]) if isinstance(r.get(k), float) else r.get(k) for k in keys if k in r}
+        out["kernel"] = r.get("kernel")
+        return out
+
+    hbm = peaks["hbm_gbs"]
+    s = {"peaks": {"hbm_gbs": hbm, "bf16_tflops": peaks["bf16_tflops"], "int8_imma_tops": r3(imma_tops)},
+         "cfg1_w8_f32_64x256x192": pick("w8_dequant_f32_64x256x192", "us"),
+         "cfg2_a8w8_4096": {"us": r3(step_ms * 1e3), "TOPS": r3(value),
+                            "gemm_frac_bf16": r3(gemm_achieved / peaks["bf16_tflops"]),
+                            "gemm_frac_int8_imma": r3(gemm_achieved / imma_tops)},
+         "cfg3_dql_8192x4096": pick("dql_8192x4096", "us", "value", "frac"),
+         "cfg3_mmi_8192x4096x11008": pick("matmul_integer_8192x4096x11008", "us", "value", "frac"),
+         "cfg5_batched_mmi_65536x1024x1024": pick("batched_matmul_integer_65536x1024x1024", "us", "value",
+                                                  "frac_tensor", "frac_hbm")}
+    for m in (1, 4, 16):
+        s[f"cfg4_gemv_M{m}_8192x28672"] = pick(f"decode_gemv_M{m}", "us", "value", "frac")
+    return s
 
 
 def secondary(q, torch, flush, clocks, peaks):

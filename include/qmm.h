@@ -175,6 +175,7 @@ qmm_status qmm_a8w8_packed(int64_t M, int64_t K, int64_t N, const float* act_sca
                            const float* weight_scale, int64_t w_count, void* C, int c_dtype, const void* workspace,
                            size_t workspace_bytes, void* stream);
 
+
 /*
  * qmm_a8w8 from HOST buffers, with the copies overlapped with the work: the
  * same operation and bit-identical results as qmm_a8w8_ws, for callers whose
@@ -420,6 +421,37 @@ qmm_status dynamic_quantize_linear(const float* x, int64_t n, uint8_t* y, float*
 qmm_status dynamic_quantize_linear_noalloc(const float* x, int64_t n, uint8_t* y, float* y_scale,
                                            uint8_t* y_zero_point, int32_t* row_sums, int64_t row_len,
                                            void* stream);
+
+/*
+ * Failure-path test hook (no operation of the pages). Runs qmm_a8w8_packed
+ * with one fault planted on the host side of the launch: the first SM pair
+ * issues neither the arrival nor the copies of its first operand stage, so
+ * that pair's MMA issuer waits for data that never comes. Its wait runs out
+ * after wait_limit_ns (1 us .. 100 ms; the pair's other waits after four
+ * times that), the pair records site 0x401 (operand stage never filled) in the
+ * device error word, abandons its tiles, drains, frees its tensor memory and
+ * returns; every other pair computes its tiles as usual. Nothing traps and
+ * the context stays usable: qmm_check_device_error() then returns
+ * QMM_ERR_TIMEOUT with qmm_last_device_error() == 0x401. The output tiles
+ * of the stalled pair are left unwritten. Arguments as for
+ * qmm_a8w8_packed; QMM_ERR_INVALID_ARG for a limit outside the range.
+ */
+qmm_status qmm_test_a8w8_packed_stall(int64_t M, int64_t K, int64_t N, const float* act_scale, int64_t act_count,
+                                      const float* weight_scale, int64_t w_count, void* C, int c_dtype,
+                                      const void* workspace, size_t workspace_bytes, uint64_t wait_limit_ns,
+                                      void* stream);
+
+/*
+ * Measurement aid (no operation of the pages): enqueue one launch of a kernel
+ * that issues nothing but warp-level integer MMAs (mma.sync m16n8k32,
+ * s8 x s8 -> s32, register operands, eight independent accumulators per warp)
+ * on every SM, `iters` rounds per warp. *ops receives the integer operations
+ * the launch performs (2*16*8*32 per MMA); divided by the launch's
+ * event-timed duration it gives the rate of the legacy int8 tensor path, the
+ * denominator of an "% of int8 tensor peak" figure. QMM_ERR_INVALID_ARG when
+ * iters < 1 or ops is NULL.
+ */
+qmm_status qmm_int8_mma_peak_launch(int iters, double* ops, void* stream);
 
 /* Human-readable name of a status. Never NULL. */
 const char* qmm_status_string(int status);

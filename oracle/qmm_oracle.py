@@ -48,12 +48,6 @@ def wrap_int32(x: np.ndarray) -> np.ndarray:
     return (((x + (1 << 31)) % INT32_MOD) - (1 << 31)).astype(np.int32)
 
 
-def bf16_bits_to_f32(bits: np.ndarray) -> np.ndarray:
-    """Widen bf16 bit patterns (uint16) to the float32 values they denote."""
-    b = np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)
-    return b.view(np.float32)
-
-
 def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round float32 to bf16, nearest with ties to even, returning uint16 bits.
 
@@ -200,7 +194,11 @@ def _a8w8_epilogue(acc: np.ndarray, act_scale, weight_scale, out: str):
 
 
 def a8w8_exact(A: np.ndarray, B: np.ndarray, act_scale, weight_scale) -> np.ndarray:
-    """float64 value of act_scale[m] * weight_scale[n] * acc[m,n] (no float32 steps)."""
+    """float64 value of act_scale[m] * weight_scale[n] * acc[m,n] (no float32 steps).
+
+    The real-valued result the float32 chain of a8w8 approximates; acc is the
+    int32 accumulator of a8w8_acc and the scales keep the [M] rows / [N]
+    columns orientation of [P2]'s review comments."""
     acc = a8w8_acc(A, B).astype(np.float64)
     M, N = acc.shape
     a_s = _as_vector(act_scale, M, "act_scale").astype(np.float64)

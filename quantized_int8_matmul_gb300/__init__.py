@@ -89,6 +89,8 @@ def _load() -> ctypes.CDLL:
     lib.qmm_check_device_error.restype = ci
     lib.qmm_num_sms.restype = ci
     lib.qmm_abi_version.restype = ci
+    lib.qmm_int8_mma_peak_launch.argtypes = [ci, ctypes.POINTER(ctypes.c_double), vp]
+    lib.qmm_int8_mma_peak_launch.restype = ci
     return lib
 
 
@@ -121,6 +123,14 @@ def _need(t, dtypes, name):
         raise ValueError(f"{name}: dtype {t.dtype} not in {dtypes}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def int8_mma_peak_launch(iters: int, stream=None) -> float:
+    """Enqueue the int8 warp-MMA throughput kernel (a measurement aid) and
+    return the integer operations it performs; time it with CUDA events."""
+    ops = ctypes.c_double(0.0)
+    _check("qmm_int8_mma_peak_launch", _lib.qmm_int8_mma_peak_launch(int(iters), ctypes.byref(ops), _stream(stream)))
+    return ops.value
 
 
 def last_kernel() -> str:

@@ -60,17 +60,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait for the phase with the given parity to complete. Returns false if the
-// CTA is aborting or the wait exceeded kWaitLimitNs (then the error word gets
+// CTA is aborting or the wait exceeded limit_ns (then the error word gets
 // `site` and the abort flag is raised). abort_flag may be null (not checked).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned* err, unsigned site) {
+                                          unsigned* err, unsigned site, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0) {
       if (abort_flag && *abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         if (abort_flag) *abort_flag = 1;
         record_error(err, site);
         return false;
@@ -403,14 +403,14 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t pa
 // mbar_wait with cluster-scope acquire, for phases completed by arrivals from
 // the peer CTA or by the pair's tensor-core commits.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                                  unsigned* err, unsigned site) {
+                                                  unsigned* err, unsigned site, uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait_cluster(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait_cluster(bar, parity)) return true;
     if ((it & 15u) == 0) {
       if (abort_flag && *abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         if (abort_flag) *abort_flag = 1;
         record_error(err, site);
         return false;

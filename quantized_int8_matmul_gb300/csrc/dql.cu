@@ -139,8 +139,11 @@ __device__ __forceinline__ ScaleZp reduce_partials(const float* __restrict__ par
 // System/6000 processor", IBM J. Res. Dev. 34(1), 1990): with r = RN(1/scale),
 // q = RN(x*r) is within an ulp of x/scale, e = x - q*scale is exact as one
 // FMA, and RN(q + e*r) is the correctly rounded quotient (a quotient of two
-// floats is never exactly halfway between two floats). Valid while 1/scale is
-// finite and normal; the callers fall back to IEEE division otherwise.
+// floats is never exactly halfway between two floats). The residual e is only
+// exact while it stays out of the subnormal range: for a quotient of at least
+// 1/4 (smaller ones quantize to 0 either way) that holds when scale >= 2^-100,
+// i.e. r <= 2^100. Outside that range (and when 1/scale is not a normal float)
+// the callers fall back to IEEE division.
 __device__ __forceinline__ float div_markstein(float x, float scale, float r) {
   const float q = __fmul_rn(x, r);
   const float e = __fmaf_rn(-q, scale, x);
@@ -172,10 +175,11 @@ __device__ __forceinline__ uint32_t quant4(const float4 v, float scale, float r,
          (quant1(v.w, scale, zp) << 24);
 }
 
-// RN(1/scale) when it is finite and normal (and 1/r is finite), else 0 (= use IEEE division).
+// RN(1/scale) when it is a normal float no larger than 2^100 (the residual of
+// div_markstein is then exact), else 0 (= use IEEE division).
 __device__ __forceinline__ float safe_recip(float scale) {
   const float r = __frcp_rn(scale);
-  return (isfinite(r) && fabsf(r) >= 1.17549435e-38f && fabsf(r) <= 1.0e37f) ? r : 0.f;
+  return (isfinite(r) && fabsf(r) >= 1.17549435e-38f && fabsf(r) <= 0x1p100f) ? r : 0.f;
 }
 
 __global__ void __launch_bounds__(THREADS) dql_quantize_kernel(const float* __restrict__ x, long long n, int vec,

@@ -13,7 +13,9 @@
 // library holds it (8 KiB) until the process exits. Host code cannot use the
 // variable's name as a device address, so the address is looked up once per
 // device with cudaGetSymbolAddress, on the first call made with that device
-// current. That first call should therefore come before any stream capture.
+// current (and again if that device's context has been made anew, as after a
+// cudaDeviceReset, since the array may then sit elsewhere). That first call
+// should therefore come before any stream capture.
 // All calls share the one array and it keeps the last call's contents; this
 // is harmless because pass 1 writes every partial that pass 2 reads, so
 // nothing in it needs to start at zero. Calls whose kernels overlap on the
@@ -35,19 +37,25 @@ static __device__ __align__(256) float g_dql_scratch[kNoAllocFloats];
 constexpr int kMaxDev = 64;
 std::mutex g_scratch_mu;
 float* g_scratch_ptr[kMaxDev] = {};
+unsigned long long g_scratch_ctx[kMaxDev] = {};
 
-// Device address of g_dql_scratch for the current device (looked up once).
+// Device address of g_dql_scratch for the current device: looked up on the
+// first call, and again whenever the device's current context is not the one
+// the cached address was taken in.
 cudaError_t scratch_for_current_device(float** out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  unsigned long long ctx = 0;
+  const bool have = current_context_id(&ctx);
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
+  if (!g_scratch_ptr[dev] || !have || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_dql_scratch);
     if (e != cudaSuccess) return e;
     g_scratch_ptr[dev] = static_cast<float*>(p);
+    g_scratch_ctx[dev] = current_context_id(&ctx) ? ctx : 0;   // the lookup made the context current
   }
   *out = g_scratch_ptr[dev];
   return cudaSuccess;

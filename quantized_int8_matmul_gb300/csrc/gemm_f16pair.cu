@@ -560,6 +560,10 @@ __global__ void __launch_bounds__(NT, 1)
   cluster_sync_all();
   tc_fence_after();
   const uint32_t tbase = sm.tmem_base;
+  // wait limits: the MMA thread's, and every other role's (longer under the
+  // stall test, so that the MMA thread's wait is the one that runs out first)
+  const uint64_t lim = p.wait_ns ? p.wait_ns : kWaitLimitNs;
+  const uint64_t lim2 = p.stall_test ? 4 * lim : lim;
   // launched as a programmatic dependent of the pre-pass: everything above ran
   // while it finished; nothing below reads its output before it completes
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -577,7 +581,7 @@ __global__ void __launch_bounds__(NT, 1)
           const int ab = d & 1;   // accumulator buffer of this chunk
           if (d >= 2) {
             ok = mbar_wait_cluster(&sm.acc_empty[ab], (uint32_t)(((d >> 1) - 1) & 1), &sm.abort_flag, p.err,
-                                   SITE_ACC_EMPTY);
+                                   SITE_ACC_EMPTY, lim);
             if (!ok) break;
           }
           tc_fence_after();
@@ -586,7 +590,8 @@ __global__ void __launch_bounds__(NT, 1)
           const int s_end = min(spt, s_beg + cs);
           for (int s = s_beg; s < s_end; ++s, ++g) {
             const int slot = g % kNS;
-            ok = mbar_wait_cluster(&sm.full[slot], (uint32_t)((g / kNS) & 1), &sm.abort_flag, p.err, SITE_FULL);
+            ok = mbar_wait_cluster(&sm.full[slot], (uint32_t)((g / kNS) & 1), &sm.abort_flag, p.err, SITE_FULL,
+                                   lim);
             if (!ok) break;
             tc_fence_after();
             const uint32_t a_addr = sbase + (uint32_t)slot * STAGE_BYTES;
@@ -620,8 +625,15 @@ __global__ void __launch_bounds__(NT, 1)
       for (; g < total_stages; ++g) {
         const int slot = g % kNS;
         if (g >= kNS &&
-            !mbar_wait(&sm.empty[slot], (uint32_t)(((g / kNS) - 1) & 1), &sm.abort_flag, p.err, SITE_EMPTY))
+            !mbar_wait(&sm.empty[slot], (uint32_t)(((g / kNS) - 1) & 1), &sm.abort_flag, p.err, SITE_EMPTY, lim2))
           break;
+        if (p.stall_test && cid == 0 && g == 0) {   // test hook: this stage never fills
+          if (++s == spt) {
+            s = 0;
+            tc = tile_coord<BN>(p, ++tl, cid, ncl, (int)rank);
+          }
+          continue;
+        }
         const uint32_t bar = full_leader0 + (uint32_t)slot * 8u;
         if (rank == 0) mbar_arrive_expect_tx(&sm.full[slot], 2u * STAGE_BYTES);
         const uint32_t dst = sbase + (uint32_t)slot * STAGE_BYTES;
@@ -653,7 +665,7 @@ __global__ void __launch_bounds__(NT, 1)
       // of the last stages complete, no copy of either CTA is in flight.
       if (rank == 0)
         for (int j = (g > kNS ? g - kNS : 0); j < g; ++j)
-          mbar_wait_cluster(&sm.full[j % kNS], (uint32_t)((j / kNS) & 1), nullptr, p.err, SITE_FINAL);
+          mbar_wait_cluster(&sm.full[j % kNS], (uint32_t)((j / kNS) & 1), nullptr, p.err, SITE_FINAL, lim2);
     }
     __syncwarp();
   } else {
@@ -672,7 +684,8 @@ __global__ void __launch_bounds__(NT, 1)
       const int ab = d & 1;
       // acc_in joins the sums before the first chunk, or in the epilogue by TMA (c_vec bit 2)
       if (ACC && c == 0 && !(c_vec & 4)) preload_acc<CPW>(p, tc, q, h, lane, sums, c_vec);
-      if (!mbar_wait_cluster(&sm.acc_full[ab], (uint32_t)((d >> 1) & 1), &sm.abort_flag, p.err, SITE_ACC_FULL))
+      if (!mbar_wait_cluster(&sm.acc_full[ab], (uint32_t)((d >> 1) & 1), &sm.abort_flag, p.err, SITE_ACC_FULL,
+                             lim2))
         break;
       tc_fence_after();
       const uint32_t t_acc = tbase + lane_off + (uint32_t)ab * ACC_COLS + (uint32_t)(h * CPW);
@@ -725,7 +738,7 @@ __global__ void __launch_bounds__(NT, 1)
     tc_fence_after();
     if (lane == 0) {
       tc_commit_pair_mc(&sm.teardown, 0x1);
-      mbar_wait(&sm.teardown, 0u, nullptr, p.err, SITE_TEARDOWN);
+      mbar_wait(&sm.teardown, 0u, nullptr, p.err, SITE_TEARDOWN, lim2);
     }
     __syncwarp();
   }

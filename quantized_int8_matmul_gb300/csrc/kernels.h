@@ -84,6 +84,12 @@ struct GemmF16Args {
   int cv_oW, cv_sh, cv_sw, cv_pt, cv_pl, cv_dh, cv_dw, cv_kW;
   int cv_cb;   // 64-channel blocks per group
   int cv_G, cv_Cg;
+  // failure-path test hook (0 = off): the first cluster issues neither the
+  // arrival nor the copies of its first ring stage, so its MMA thread's wait
+  // for that stage runs out after wait_ns (the other roles' waits after
+  // 4 * wait_ns) and the kernel takes its abort path
+  int stall_test;
+  unsigned long long wait_ns;   // 0: the default limit of every wait
 };
 cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool mmi, int chunk_k, cudaStream_t s,
                                 const char** kernel_name);
@@ -272,5 +278,8 @@ cudaError_t launch_dql(const float* x, long long n, uint8_t* y, float* y_scale, 
                        const char** kernel_name);
 
 int num_sms();
+// The unique id of the calling thread's current CUDA context; false when no
+// context is current (or the driver offers no such query).
+bool current_context_id(unsigned long long* id);
 
 }  // namespace qmm

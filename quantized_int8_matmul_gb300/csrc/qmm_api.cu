@@ -30,6 +30,7 @@ thread_local unsigned t_last_device_error = 0;
 
 std::mutex g_mu;
 unsigned* g_err_ptr[kMaxDevices] = {};
+unsigned long long g_err_ctx[kMaxDevices] = {};
 int g_sms[kMaxDevices] = {};
 
 int current_device() {
@@ -38,14 +39,21 @@ int current_device() {
   return d;
 }
 
+// Device address of the error word in the current context. The address is
+// cached per device together with the context it was taken in: after a
+// cudaDeviceReset the primary context (and the module holding the word) is
+// made anew and the address is looked up again.
 unsigned* err_word() {
   const int d = current_device();
   if (d < 0 || d >= kMaxDevices) return nullptr;
+  unsigned long long ctx = 0;
+  const bool have = current_context_id(&ctx);
   std::lock_guard<std::mutex> lk(g_mu);
-  if (!g_err_ptr[d]) {
+  if (!g_err_ptr[d] || !have || ctx != g_err_ctx[d]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_qmm_error_word) != cudaSuccess) return nullptr;
     g_err_ptr[d] = static_cast<unsigned*>(p);
+    g_err_ctx[d] = current_context_id(&ctx) ? ctx : 0;   // the lookup made the context current
   }
   return g_err_ptr[d];
 }
@@ -157,11 +165,17 @@ cudaError_t fork_join(cudaStream_t s, Side side, Primary primary) {
   std::lock_guard<std::mutex> lk(ax->mu);
   cudaError_t e = cudaEventRecord(ax->fork, s);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(ax->s, ax->fork, 0);
-  if (e == cudaSuccess) e = side(ax->s);
-  if (e == cudaSuccess) e = cudaEventRecord(ax->join, ax->s);
-  if (e == cudaSuccess) e = primary(s);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ax->join, 0);
-  return e;
+  if (e != cudaSuccess) return e;   // nothing forked
+  // Once forked, s always waits for the side stream again, whatever failed in
+  // between: a stream capture stays joined, and s never runs ahead of side
+  // work that uses the same workspace. The first error is returned.
+  const cudaError_t es = side(ax->s);
+  const cudaError_t er = cudaEventRecord(ax->join, ax->s);
+  const cudaError_t ep = es == cudaSuccess ? primary(s) : cudaSuccess;
+  const cudaError_t ew = er == cudaSuccess ? cudaStreamWaitEvent(s, ax->join, 0) : er;
+  for (cudaError_t x : {es, ep, er, ew})
+    if (x != cudaSuccess) return x;
+  return cudaSuccess;
 }
 
 // The pre-pass: fp16 copies of A and B (and the sums the zero points need).
@@ -348,6 +362,28 @@ DqmPlan dqm_plan(int64_t M, int64_t K, int64_t N) {
   return pl;
 }
 }  // namespace
+
+bool current_context_id(unsigned long long* id) {
+  using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+  using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+  static std::once_flag once;
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext c = nullptr;
+  if (!get_current || !get_id || get_current(&c) != CUDA_SUCCESS || !c) return false;
+  return get_id(c, id) == CUDA_SUCCESS;
+}
 
 int num_sms() {
   const int d = current_device();
@@ -770,9 +806,10 @@ qmm_status qmm_a8w8_pack(const int8_t* A, const int8_t* B, int64_t M, int64_t K,
   return finish_launch(run_pack(pl, A, false, B, false, false, false, workspace, (int)K, (int)N, s), kPackName);
 }
 
-qmm_status qmm_a8w8_packed(int64_t M, int64_t K, int64_t N, const float* act_scale, int64_t act_count,
-                           const float* weight_scale, int64_t w_count, void* C, int c_dtype, const void* workspace,
-                           size_t workspace_bytes, void* stream) {
+namespace {
+qmm_status a8w8_packed_impl(int64_t M, int64_t K, int64_t N, const float* act_scale, int64_t act_count,
+                            const float* weight_scale, int64_t w_count, void* C, int c_dtype, const void* workspace,
+                            size_t workspace_bytes, void* stream, int stall_test, uint64_t wait_ns) {
   if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return QMM_ERR_INVALID_ARG;
   const PrepassPlan pl = prepass_plan(1, M, K, N, 0, 0, M);
   if (!pl.use) return QMM_ERR_UNSUPPORTED;
@@ -798,8 +835,27 @@ qmm_status qmm_a8w8_packed(int64_t M, int64_t K, int64_t N, const float* act_sca
   f.w_count = (int)w_count;
   f.zp_row_mod = (int)M;
   f.err = err;
+  f.stall_test = stall_test;
+  f.wait_ns = wait_ns;
   return finish_launch(run_packed_gemm(pl, workspace, f, false, false, false, chunk_k_for(false, false), s),
                        kPackedA8W8);
+}
+}  // namespace
+
+qmm_status qmm_a8w8_packed(int64_t M, int64_t K, int64_t N, const float* act_scale, int64_t act_count,
+                           const float* weight_scale, int64_t w_count, void* C, int c_dtype, const void* workspace,
+                           size_t workspace_bytes, void* stream) {
+  return a8w8_packed_impl(M, K, N, act_scale, act_count, weight_scale, w_count, C, c_dtype, workspace,
+                          workspace_bytes, stream, 0, 0);
+}
+
+qmm_status qmm_test_a8w8_packed_stall(int64_t M, int64_t K, int64_t N, const float* act_scale, int64_t act_count,
+                                      const float* weight_scale, int64_t w_count, void* C, int c_dtype,
+                                      const void* workspace, size_t workspace_bytes, uint64_t wait_limit_ns,
+                                      void* stream) {
+  if (wait_limit_ns < 1000 || wait_limit_ns > 100000000ull) return QMM_ERR_INVALID_ARG;
+  return a8w8_packed_impl(M, K, N, act_scale, act_count, weight_scale, w_count, C, c_dtype, workspace,
+                          workspace_bytes, stream, 1, wait_limit_ns);
 }
 
 // ---------------------------------------------------------------------------

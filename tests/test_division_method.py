@@ -25,8 +25,24 @@ def _round_f32_exact(value):
     return min(cands, key=lambda v: (abs(Fraction(float(v)) - value), int(np.array(v).view(np.int32)) & 1))
 
 
-def corrected_quotient(x, b):
-    r = (f32(1) / b).astype(f32)
+R_MAX = f32(2.0 ** 100)        # the kernel's bound on r = RN(1/b) for the fast path
+R_MIN = f32(2.0 ** -126)
+
+
+def corrected_quotient(x, b, guard=True):
+    """The kernel's quotient: Markstein's sequence where r is a normal float no
+    larger than 2^100 (guard=False: wherever r is finite and normal), IEEE
+    division elsewhere. float32 roundings, subnormals included, are numpy's."""
+    with np.errstate(over="ignore", divide="ignore", invalid="ignore", under="ignore"):
+        r = (f32(1) / b).astype(f32)
+        fast = np.isfinite(r) & (np.abs(r) >= R_MIN)
+        if guard:
+            fast &= np.abs(r) <= R_MAX
+        out = _markstein(x, b, np.where(fast, r, f32(1)))
+        return np.where(fast, out, (x / b).astype(f32))
+
+
+def _markstein(x, b, r):
     q = (x * r).astype(f32)
     # x - q*b: q*b has at most 48 significant bits, so the float64 difference is
     # exact whenever the residual is small, which is the case here
@@ -40,6 +56,12 @@ def corrected_quotient(x, b):
     for i in np.nonzero(np.abs(s - mid) <= np.abs(mid) * 2.0 ** -50)[0]:
         out[i] = _round_f32_exact(Fraction(float(e[i])) * Fraction(float(r[i])) + Fraction(float(q[i])))
     return out
+
+
+def _mismatches(x, b, guard=True):
+    got = corrected_quotient(x, b, guard)
+    ref = (x / b).astype(f32)
+    return np.count_nonzero(got.view(np.int32) != ref.view(np.int32))
 
 
 def _assert_same(x, b, what):
@@ -77,3 +99,36 @@ def test_dql_shaped_scales_and_inputs():
         scale = f32(f32(hi - lo) / f32(255))
         x = rng.uniform(lo, hi, 200_000).astype(f32)
         _assert_same(x, np.full_like(x, scale), "dql-shaped")
+
+
+def _near_midpoints(rng, n, b):
+    """Inputs whose quotient by b lies within two ulps of a float32 midpoint in [1/4, 256)."""
+    qv = rng.integers(0x3E800000, 0x43800000, n).astype(np.int32).view(f32)
+    half_ulp = (np.nextafter(qv, f32(np.inf)).astype(np.float64) - qv.astype(np.float64)) / 2
+    x = ((qv.astype(np.float64) + half_ulp) * b.astype(np.float64)).astype(f32)
+    return (x.view(np.int32) + rng.integers(-2, 3, n).astype(np.int32)).view(f32)
+
+
+def test_tiny_scales_need_the_bound_on_the_reciprocal():
+    """Below scale = 2^-100 the residual x - q*b falls into float32's subnormal
+    range and loses bits: without the bound some quotients next to midpoints
+    come out one ulp off, with it (IEEE division there) none do."""
+    rng = np.random.default_rng(14)
+    n = 400_000
+    e = rng.integers(-126, -104, n)
+    b = np.ldexp(rng.uniform(1, 2, n), e).astype(f32)
+    x = _near_midpoints(rng, n, b)
+    assert _mismatches(x, b, guard=False) > 0
+    assert _mismatches(x, b, guard=True) == 0
+
+
+def test_scales_across_the_float_range_match_ieee_division():
+    """Scales from subnormal (2^-149) up to 2^120, quotients next to midpoints."""
+    rng = np.random.default_rng(15)
+    n = 600_000
+    e = rng.integers(-149, 121, n)
+    b = np.ldexp(rng.uniform(1, 2, n), e).astype(f32)
+    b = np.where(b == 0, f32(2.0 ** -149), b).astype(f32)
+    x = _near_midpoints(rng, n, b)
+    ok = np.isfinite(x) & (x != 0)
+    assert _mismatches(x[ok], b[ok]) == 0

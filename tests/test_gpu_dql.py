@@ -102,3 +102,21 @@ def test_quotients_near_halfway(seed):
     x = np.clip(x, lo, hi).astype(np.float32)
     x[:2] = [lo, hi]
     check(x, f"near-halfway seed={seed}")
+
+
+@pytest.mark.parametrize("log2_scale", [-125, -112, -101, -99, 60])
+def test_quotients_near_halfway_at_extreme_scales(log2_scale):
+    """Ranges around 255 * 2^log2_scale: scales whose reciprocal is above 2^100
+    are divided by IEEE division, the rest by the corrected reciprocal; either
+    way every byte, the scale and the zero point equal the oracle's."""
+    rng = np.random.default_rng(200 - log2_scale)
+    width = np.float32(np.ldexp(255.0 * rng.uniform(1.0, 1.9), log2_scale))
+    lo = -np.float32(width * np.float32(rng.uniform(0.2, 0.8)))
+    hi = np.float32(width + lo)
+    scale = np.float32(np.float32(hi - lo) / np.float32(255))
+    k = rng.integers(-250, 250, 100000).astype(np.float64)
+    base = ((k + 0.5) * np.float64(scale)).astype(np.float32)
+    x = (base.view(np.int32) + rng.integers(-3, 4, base.size).astype(np.int32)).view(np.float32)
+    x = np.clip(x, lo, hi).astype(np.float32)
+    x[:2] = [lo, hi]
+    check(x, f"near-halfway 2^{log2_scale}")

@@ -193,6 +193,46 @@ def test_a8w8_acc_wraps():
     assert int(O.a8w8_acc(A, B)[0, 0]) == 16384 * K - 2**32
 
 
+def _exact_scaled(acc: int, a: float, w: float) -> Fraction:
+    return Fraction(acc) * Fraction(a) * Fraction(w)
+
+
+@pytest.mark.parametrize("shape", [(3, 29, 5), (4, 16, 4)])
+def test_a8w8_exact_against_rationals(shape):
+    """a8w8_exact is the real value acc * act_scale[m] * weight_scale[n]: each
+    element within 2 ulps (two float64 roundings) of the exact rational, with
+    row-only and column-only scales so that swapping the two orientations, even
+    when M == N, moves every element by far more."""
+    M, K, N = shape
+    rng = np.random.default_rng(21)
+    A = rng.integers(-127, 128, (M, K), dtype=np.int8)
+    B = rng.integers(-127, 128, (K, N), dtype=np.int8)
+    a_s = (np.arange(1, M + 1) * 0.25).astype(np.float32)            # rows: 0.25, 0.5, ...
+    w_s = (np.arange(1, N + 1) * 0.001 + 0.003).astype(np.float32)    # columns, a different law
+    got = O.a8w8_exact(A, B, a_s, w_s)
+    assert got.dtype == np.float64 and got.shape == (M, N)
+    for m in range(M):
+        for n in range(N):
+            acc = sum(int(A[m, k]) * int(B[k, n]) for k in range(K))
+            want = _exact_scaled(acc, float(a_s[m]), float(w_s[n]))
+            err = abs(Fraction(float(got[m, n])) - want)
+            assert err <= 2 * Fraction(math.ulp(float(want))), (m, n)
+    if M == N:   # the square case: a last-dimension broadcast would give this instead
+        assert not np.allclose(O.a8w8_exact(A, B, w_s, a_s), got)
+
+
+def test_a8w8_exact_scalar_scales_and_wrapped_accumulator():
+    """Scalar scales broadcast; the accumulator is the wrapped int32 one (the
+    value the float32 chain starts from), here past 2^31."""
+    K = 133200                       # 127 * 127 * K > 2^31
+    A = np.full((1, K), 127, np.int8)
+    B = np.full((K, 2), 127, np.int8)
+    got = O.a8w8_exact(A, B, [0.5], [0.25])
+    wrapped = 16129 * K - 2**32
+    assert wrapped < 0
+    assert got.tolist() == [[wrapped * 0.125, wrapped * 0.125]]
+
+
 def test_a8w8_error_bound_value():
     A = np.array([[2, -3]], np.int8)
     B = np.array([[5], [7]], np.int8)

@@ -5,14 +5,18 @@ must not call cudaMalloc). It keeps its partials in a fixed array inside the
 library instead of a caller workspace, so these tests check, through the C
 ABI, that two calls in a row give exactly what the workspace entry point gives
 -- the second call must not be affected by what the first left in the shared
-array. This file is collected last on purpose."""
+array -- and that both equal the CPU oracle byte for byte. This file is
+collected last on purpose."""
 import ctypes
+import json
+import os
 
 import numpy as np
 import pytest
 import torch
 
 import qmm_workloads as W
+from oracle import qmm_oracle as O
 
 pytestmark = pytest.mark.gpu
 q = pytest.importorskip("quantized_int8_matmul_gb300")
@@ -47,6 +51,17 @@ def inputs():
     return torch.from_numpy(big).cuda(), torch.from_numpy(small).cuda()
 
 
+def check_oracle(x, y, s, zp, rs=None, row_len=None):
+    """The bytes, the scale's bits, the zero point (and the row sums) equal the oracle's."""
+    xh = x.cpu().numpy()
+    wy, ws, wzp = O.dynamic_quantize_linear(xh)
+    assert s.cpu().numpy().view(np.uint32)[0] == np.float32(ws).view(np.uint32)
+    assert int(zp.item()) == int(wzp)
+    assert np.array_equal(y.cpu().numpy().reshape(-1), wy.reshape(-1))
+    if rs is not None:
+        assert np.array_equal(rs.cpu().numpy(), O.row_sums(wy.reshape(-1), row_len))
+
+
 def test_two_calls_in_a_row_match_the_workspace_entry_point():
     xs = inputs()
     got = [noalloc(x) for x in xs]           # two no-alloc calls back to back
@@ -56,6 +71,21 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point():
         torch.cuda.synchronize()
         assert torch.equal(s, ws) and torch.equal(zp, wzp)
         assert torch.equal(y, wy)
+        check_oracle(x, y, s, zp)
+
+
+def test_ties_to_even_through_the_no_alloc_entry_point():
+    """The page's ties-to-even rule on the zero point (-lo/scale = 2.5 -> 2) and
+    on the quotients, after a large call has filled the shared array."""
+    big, _ = inputs()
+    noalloc(big)
+    with open(os.path.join(os.path.dirname(__file__), "golden", "dql_ties.json")) as f:
+        g = json.load(f)
+    x = torch.tensor(g["x"], dtype=torch.float32, device="cuda")
+    y, s, zp, _ = noalloc(x)
+    torch.cuda.synchronize()
+    assert y.cpu().tolist() == g["y"] and int(zp.item()) == g["zero_point"] and float(s.item()) == g["scale"]
+    check_oracle(x, y, s, zp)
 
 
 def test_two_calls_in_a_row_with_row_sums():
@@ -67,6 +97,7 @@ def test_two_calls_in_a_row_with_row_sums():
         torch.cuda.synchronize()
         assert torch.equal(s, ws) and torch.equal(zp, wzp)
         assert torch.equal(y, wy) and torch.equal(rs, wrs)
+        check_oracle(x, y, s, zp, rs, x.shape[1])
 
 
 def test_rejects_malformed_arguments():
