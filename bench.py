@@ -509,6 +509,25 @@ def case_setups(q, torch, peaks):
             return (lambda: q.qmm_w8_dequant(Ad, Wd, sd, None, out=Cd, workspace=wsg)), False, report
         return setup
 
+    def gemv_packed(Mg):
+        def setup():
+            g = W.decode_gemv(Mg)
+            Ad = torch.from_numpy(g.A_bits.view(np.int16)).view(torch.bfloat16).cuda()
+            Wd = torch.from_numpy(g.W).cuda()
+            sd = torch.from_numpy(g.scale).cuda()
+            Cd = torch.empty((Mg, 28672), dtype=torch.bfloat16, device="cuda")
+            packed = q.qmm_w8_pack_decode_weight(Wd)   # once, outside the timed calls (a frozen weight)
+            del Wd
+            nbytes = 8192 * 28672 + Mg * 8192 * 2 + 28672 * 4 + Mg * 28672 * 2
+            wsg = torch.empty(q.qmm_w8_dequant_packed_workspace_bytes(Mg, 8192), dtype=torch.uint8, device="cuda")
+
+            def report(ms):
+                gbs = nbytes / (ms * 1e-3) / 1e9
+                return {"us": ms * 1e3, "value": gbs, "unit": "GB/s", "bound": "hbm", "frac": gbs / hbm,
+                        "algorithmic_bytes": nbytes, "note": "weight re-laid out once for the decode kernel"}
+            return (lambda: q.qmm_w8_dequant_packed(Ad, packed, 28672, sd, out=Cd, workspace=wsg)), False, report
+        return setup
+
     def dql():
         d = W.dql_matmul_integer_8192x4096x11008()
         x = torch.from_numpy(d.x).cuda()
@@ -651,6 +670,8 @@ def case_setups(q, torch, peaks):
             "a8w8_4096x4096x4096_bf16_single_pass": a8w8_single_pass,
             "w8_prefill_bf16_4096x8192x28672": w8_prefill,
             "decode_gemv_M1": gemv(1), "decode_gemv_M4": gemv(4), "decode_gemv_M16": gemv(16),
+            "decode_gemv_packed_M1": gemv_packed(1), "decode_gemv_packed_M4": gemv_packed(4),
+            "decode_gemv_packed_M16": gemv_packed(16),
             "dql_8192x4096": dql, "matmul_integer_8192x4096x11008": mmi,
             "batched_matmul_integer_65536x1024x1024": batched, "w8_dequant_f32_64x256x192": w8,
             "a8w8_acc_4096x4096x4096_bf16": a8w8_acc(4096, 4096, 4096, False),
@@ -671,7 +692,8 @@ SECONDARY = ["a8w8_4096x4096x4096_bf16_single_pass", "w8_prefill_bf16_4096x8192x
              "a8w8_acc_decode_M16_8192x28672_b_trans", "conv_integer_3x3_8x256x56x56",
              "conv_integer_1d_k3_4x512x3000", "dql_matmul_dequant_fused_8192x4096x11008",
              "w8_dequant_f32_64x256x192", "dql_8192x4096", "matmul_integer_8192x4096x11008",
-             "batched_matmul_integer_65536x1024x1024", "decode_gemv_M1", "decode_gemv_M4", "decode_gemv_M16"]
+             "batched_matmul_integer_65536x1024x1024", "decode_gemv_M1", "decode_gemv_M4", "decode_gemv_M16",
+             "decode_gemv_packed_M1", "decode_gemv_packed_M4", "decode_gemv_packed_M16"]
 
 
 def config_summary(rows, value, step_ms, gemm_achieved, peaks, imma_tops):
@@ -699,6 +721,8 @@ def config_summary(rows, value, step_ms, gemm_achieved, peaks, imma_tops):
                                                   "frac_tensor", "frac_hbm")}
     for m in (1, 4, 16):
         s[f"cfg4_gemv_M{m}_8192x28672"] = pick(f"decode_gemv_M{m}", "us", "value", "frac")
+    for m in (1, 4, 16):
+        s[f"cfg4_gemv_packed_M{m}"] = pick(f"decode_gemv_packed_M{m}", "us", "frac")
     return s
 
 

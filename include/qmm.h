@@ -453,6 +453,38 @@ qmm_status qmm_test_a8w8_packed_stall(int64_t M, int64_t K, int64_t N, const flo
  */
 qmm_status qmm_int8_mma_peak_launch(int iters, double* ops, void* stream);
 
+/*
+ * Decode form (a) on a weight packed once. TrainDeeploy PR #53 ("matmul that
+ * dequantises an int8 weight in-kernel", section "The kernel"): the same
+ * operation and tolerance as qmm_w8_dequant for bf16 activations, 1 <= M <= 16
+ * rows, with the int8 weight W [K,N] first re-laid out once (as for any frozen
+ * weight) into the order the decode kernel's tensor-core fragments read it:
+ * the same K x N bytes (K padded to 16, N to 64), each biased by 128, so that
+ * a warp reads each 16-row step as one contiguous KB and widens every byte to
+ * fp16 with about one instruction. The per-call work reads the packed weight
+ * once and never forms a dequantised copy.
+ *   qmm_w8_decode_pack_bytes(K, N)       bytes of the packed weight (0: shape
+ *                                        unsupported: K or N not a multiple of 8)
+ *   qmm_w8_pack_decode_weight(W, K, N, packed, bytes, stream)
+ *                                        W int8 [K,N] device -> packed (caller-owned,
+ *                                        16-byte aligned device memory)
+ *   qmm_w8_dequant_packed_workspace_bytes(M, K)
+ *                                        the activations' fp16 copy (rows padded to 8 or 16)
+ *   qmm_w8_dequant_packed(A, M, K, N, packed, bytes, scale, scale_count,
+ *                         zero_point, zp_count, C, c_dtype, workspace, bytes, stream)
+ *       A bf16 [M,K] (16-byte aligned), scale / zero_point / C as for
+ *       qmm_w8_dequant. QMM_ERR_UNSUPPORTED outside 1 <= M <= 16, K % 8, N % 8;
+ *       QMM_ERR_INVALID_ARG for short or unaligned buffers.
+ */
+size_t qmm_w8_decode_pack_bytes(int64_t K, int64_t N);
+qmm_status qmm_w8_pack_decode_weight(const int8_t* W, int64_t K, int64_t N, void* packed, size_t packed_bytes,
+                                     void* stream);
+size_t qmm_w8_dequant_packed_workspace_bytes(int64_t M, int64_t K);
+qmm_status qmm_w8_dequant_packed(const void* A, int64_t M, int64_t K, int64_t N, const void* packed,
+                                 size_t packed_bytes, const float* scale, int64_t scale_count,
+                                 const int32_t* zero_point, int64_t zp_count, void* C, int c_dtype, void* workspace,
+                                 size_t workspace_bytes, void* stream);
+
 /* Human-readable name of a status. Never NULL. */
 const char* qmm_status_string(int status);
 

@@ -89,6 +89,14 @@ def _load() -> ctypes.CDLL:
     lib.qmm_check_device_error.restype = ci
     lib.qmm_num_sms.restype = ci
     lib.qmm_abi_version.restype = ci
+    lib.qmm_w8_decode_pack_bytes.argtypes = [i64, i64]
+    lib.qmm_w8_decode_pack_bytes.restype = sz
+    lib.qmm_w8_pack_decode_weight.argtypes = [vp, i64, i64, vp, sz, vp]
+    lib.qmm_w8_pack_decode_weight.restype = ci
+    lib.qmm_w8_dequant_packed_workspace_bytes.argtypes = [i64, i64]
+    lib.qmm_w8_dequant_packed_workspace_bytes.restype = sz
+    lib.qmm_w8_dequant_packed.argtypes = [vp, i64, i64, i64, vp, sz, vp, i64, vp, i64, vp, ci, vp, sz, vp]
+    lib.qmm_w8_dequant_packed.restype = ci
     lib.qmm_int8_mma_peak_launch.argtypes = [ci, ctypes.POINTER(ctypes.c_double), vp]
     lib.qmm_int8_mma_peak_launch.restype = ci
     return lib
@@ -123,6 +131,48 @@ def _need(t, dtypes, name):
         raise ValueError(f"{name}: dtype {t.dtype} not in {dtypes}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def qmm_w8_pack_decode_weight(W, packed=None, stream=None):
+    """Re-lay a frozen int8 weight W [K, N] once for the decode GEMV (same bytes, padded)."""
+    _need(W, (torch.int8,), "W")
+    K, N = W.shape
+    nbytes = int(_lib.qmm_w8_decode_pack_bytes(K, N))
+    if nbytes == 0:
+        raise QmmError("qmm_w8_pack_decode_weight", QMM_ERR_UNSUPPORTED)
+    if packed is None:
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    _check("qmm_w8_pack_decode_weight",
+           _lib.qmm_w8_pack_decode_weight(_ptr(W), K, N, _ptr(packed), packed.numel(), _stream(stream)))
+    return packed
+
+
+def qmm_w8_dequant_packed(A, packed, N, scale, zero_point=None, out=None, out_dtype=torch.bfloat16,
+                          workspace=None, stream=None):
+    """Decode form (a), C = scale * (A @ W - zp * rowsum(A)), on a weight packed
+    by qmm_w8_pack_decode_weight; A bf16 [M, K], 1 <= M <= 16."""
+    _need(A, (torch.bfloat16,), "A")
+    _need(scale, (torch.float32,), "scale")
+    M, K = A.shape
+    zc = 0
+    if zero_point is not None:
+        _need(zero_point, (torch.int32,), "zero_point")
+        zc = zero_point.numel()
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=A.device)
+    _need(out, (torch.float32, torch.bfloat16), "out")
+    nbytes = int(_lib.qmm_w8_dequant_packed_workspace_bytes(M, K))
+    if workspace is None:
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=A.device)
+    st = _lib.qmm_w8_dequant_packed(_ptr(A), M, K, N, _ptr(packed), packed.numel(), _ptr(scale), scale.numel(),
+                                    _ptr(zero_point), zc, _ptr(out), _TORCH_TO_QMM[out.dtype], _ptr(workspace),
+                                    workspace.numel(), _stream(stream))
+    _check("qmm_w8_dequant_packed", st)
+    return out
+
+
+def qmm_w8_dequant_packed_workspace_bytes(M: int, K: int) -> int:
+    return int(_lib.qmm_w8_dequant_packed_workspace_bytes(M, K))
 
 
 def int8_mma_peak_launch(iters: int, stream=None) -> float:

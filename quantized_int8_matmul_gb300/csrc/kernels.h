@@ -221,6 +221,16 @@ cudaError_t launch_gemv_prep(const uint16_t* A, int M, int K, void* workspace, c
 // the prep's workspace.
 cudaError_t launch_gemv_f16(GemvArgs a, void* workspace, cudaStream_t s, const char** kernel_name);
 
+// Decode GEMV on a weight packed once (gemv_packed.cu): the packed layout holds
+// each lane's MMA fragments in order, biased, K padded to 16 and N to 64.
+size_t gemv_packed_weight_bytes(long long K, long long N);
+// workspace of the activations' fp16 copy: M padded to 8 or 16 rows of Kp
+size_t gemv_packed_workspace_bytes(long long M, long long K);
+cudaError_t launch_gemv_pack(const int8_t* W, long long K, long long N, void* packed, cudaStream_t s);
+// 1 <= M <= 16, K % 8 == 0, N % 8 == 0; g.W unused (the packed weight is given)
+cudaError_t launch_gemv_packed(const GemvArgs& g, const void* packed, void* workspace, cudaStream_t s,
+                               const char** kernel_name);
+
 // ---------------------------------------------------------------------------
 // Decode-shaped form (a) for M <= 4 on the CUDA cores: TMA-staged weight,
 // packed fp32 FMAs, CTA pairs splitting K and reducing through distributed

@@ -517,6 +517,56 @@ bool gemv_f16_shape(int a_dtype, int64_t M, int64_t K, int64_t N) {
   return a_dtype == QMM_BF16 && M >= 3 && M <= 16 && K >= 8 && K % 8 == 0 && N >= 16 && N % 16 == 0;
 }
 
+size_t qmm_w8_decode_pack_bytes(int64_t K, int64_t N) {
+  if (K < 8 || N < 8 || !dim_ok(K) || !dim_ok(N) || K % 8 != 0 || N % 8 != 0) return 0;
+  return gemv_packed_weight_bytes(K, N);
+}
+
+qmm_status qmm_w8_pack_decode_weight(const int8_t* W, int64_t K, int64_t N, void* packed, size_t packed_bytes,
+                                     void* stream) {
+  const size_t need = qmm_w8_decode_pack_bytes(K, N);
+  if (need == 0) return QMM_ERR_UNSUPPORTED;
+  if (!W || !packed || !aligned16(packed) || packed_bytes < need) return QMM_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  return finish_launch(launch_gemv_pack(W, K, N, packed, s), "gemv_w8_pack");
+}
+
+size_t qmm_w8_dequant_packed_workspace_bytes(int64_t M, int64_t K) {
+  if (M < 1 || M > 16 || K < 8 || !dim_ok(K) || K % 8 != 0) return 0;
+  return gemv_packed_workspace_bytes(M, K);
+}
+
+qmm_status qmm_w8_dequant_packed(const void* A, int64_t M, int64_t K, int64_t N, const void* packed,
+                                 size_t packed_bytes, const float* scale, int64_t scale_count,
+                                 const int32_t* zero_point, int64_t zp_count, void* C, int c_dtype, void* workspace,
+                                 size_t workspace_bytes, void* stream) {
+  if (M < 1 || M > 16 || K < 8 || N < 8 || !dim_ok(K) || !dim_ok(N) || K % 8 != 0 || N % 8 != 0)
+    return QMM_ERR_UNSUPPORTED;
+  if (c_dtype != QMM_F32 && c_dtype != QMM_BF16) return QMM_ERR_INVALID_ARG;
+  if (scale_count != 1 && scale_count != N) return QMM_ERR_INVALID_ARG;
+  if (zp_count != 0 && zp_count != 1 && zp_count != N) return QMM_ERR_INVALID_ARG;
+  if (!A || !aligned16(A) || !scale || !C || (zp_count > 0 && !zero_point)) return QMM_ERR_INVALID_ARG;
+  if (!packed || !aligned16(packed) || packed_bytes < gemv_packed_weight_bytes(K, N)) return QMM_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < gemv_packed_workspace_bytes(M, K))
+    return QMM_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  GemvArgs g{};
+  g.A = static_cast<const uint16_t*>(A);
+  g.M = (int)M;
+  g.K = (int)K;
+  g.N = (int)N;
+  g.scale = scale;
+  g.scale_count = (int)scale_count;
+  g.zp = zero_point;
+  g.zp_count = (int)zp_count;
+  g.C = C;
+  g.c_f32 = c_dtype == QMM_F32;
+  const char* name = "none";
+  return finish_launch(launch_gemv_packed(g, packed, workspace, s, &name), name);
+}
+
 size_t qmm_w8_dequant_workspace_bytes(int a_dtype, int64_t M, int64_t K, int64_t N) {
   if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return 0;
   if (a_dtype != QMM_F32 && a_dtype != QMM_BF16) return 0;

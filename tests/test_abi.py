@@ -193,3 +193,16 @@ def test_w8_dequant_workspace_follows_the_route(qmm):
     assert lib.qmm_w8_dequant_workspace_bytes(qmm.QMM_BF16, 4, K + 4, N) == 0  # K % 8 != 0
     # prefill (M >= 64): the exact bf16 weight copy
     assert lib.qmm_w8_dequant_workspace_bytes(qmm.QMM_BF16, 4096, K, N) >= 2 * K * N
+
+
+def test_decode_pack_sizes_follow_the_layout(qmm):
+    """The packed decode weight: K padded to 16-row steps, N to 64-column
+    slabs; shapes outside the path (K or N not a multiple of 8) give 0."""
+    lib = qmm.lib()
+    assert lib.qmm_w8_decode_pack_bytes(8192, 28672) == 8192 * 28672
+    assert lib.qmm_w8_decode_pack_bytes(1000, 200) == 1008 * 256
+    assert lib.qmm_w8_decode_pack_bytes(1000, 100) == 0
+    assert lib.qmm_w8_decode_pack_bytes(12, 64) == 0
+    assert lib.qmm_w8_dequant_packed_workspace_bytes(4, 8192) >= 8 * 8192 * 2
+    assert lib.qmm_w8_dequant_packed_workspace_bytes(9, 8192) >= 16 * 8192 * 2
+    assert lib.qmm_w8_dequant_packed_workspace_bytes(17, 8192) == 0
