@@ -637,6 +637,26 @@ def case_setups(q, torch, peaks):
                             "* y_scale*w_scale[n] + bias[n], one call; weight converted every call"}
         return (lambda: q.dynamic_quantize_matmul(x, Bd, w_s, bz, bias, out=Cf, workspace=wsd)), False, report
 
+    def dq_chain_packed():
+        d = W.dql_matmul_integer_8192x4096x11008()
+        rng = np.random.default_rng(9)
+        x, Bd, bz = torch.from_numpy(d.x).cuda(), torch.from_numpy(d.B).cuda(), torch.from_numpy(d.b_zp).cuda()
+        w_s = torch.from_numpy(rng.uniform(0.001, 0.01, 11008).astype(np.float32)).cuda()
+        bias = torch.from_numpy(rng.standard_normal(11008).astype(np.float32)).cuda()
+        Cf = torch.empty((8192, 11008), dtype=torch.float32, device="cuda")
+        pw = q.dynamic_quantize_matmul_pack_weight(Bd)   # once, outside the timed calls
+        wsd = torch.empty(q.dynamic_quantize_matmul_packed_workspace_bytes(8192, 4096), dtype=torch.uint8,
+                          device="cuda")
+        ops = 2.0 * 8192 * 4096 * 11008
+
+        def report(ms):
+            tops = ops / (ms * 1e-3) / 1e12
+            return {"us": ms * 1e3, "value": tops, "unit": "TOPS", "frac_tensor": tops / tc,
+                    "note": "the fused chain on a weight packed once (fp16 copy + column sums); per call: "
+                            "DynamicQuantizeLinear into the fp16 operand, then the GEMM with its epilogue"}
+        return (lambda: q.dynamic_quantize_matmul_packed(x, pw, w_s, bz, bias, out=Cf, workspace=wsd)), False, \
+            report
+
     def conv(make):
         def setup():
             c = make()
@@ -680,6 +700,7 @@ def case_setups(q, torch, peaks):
             "a8w8_acc_decode_M1_8192x28672": a8w8_acc(1, 8192, 28672, False),
             "a8w8_acc_decode_M16_8192x28672_b_trans": a8w8_acc(16, 8192, 28672, True),
             "dql_matmul_dequant_fused_8192x4096x11008": dq_chain,
+            "dql_matmul_dequant_fused_packed_8192x4096x11008": dq_chain_packed,
             "conv_integer_3x3_8x256x56x56": conv(W.conv2d_3x3_8x256x56x56),
             "conv_integer_1d_k3_4x512x3000": conv(W.conv1d_k3_4x512x3000)}
 
@@ -691,6 +712,7 @@ SECONDARY = ["a8w8_4096x4096x4096_bf16_single_pass", "w8_prefill_bf16_4096x8192x
              "a8w8_acc_decode_M1_8192x28672_b_trans", "a8w8_acc_decode_M1_8192x28672",
              "a8w8_acc_decode_M16_8192x28672_b_trans", "conv_integer_3x3_8x256x56x56",
              "conv_integer_1d_k3_4x512x3000", "dql_matmul_dequant_fused_8192x4096x11008",
+             "dql_matmul_dequant_fused_packed_8192x4096x11008",
              "w8_dequant_f32_64x256x192", "dql_8192x4096", "matmul_integer_8192x4096x11008",
              "batched_matmul_integer_65536x1024x1024", "decode_gemv_M1", "decode_gemv_M4", "decode_gemv_M16",
              "decode_gemv_packed_M1", "decode_gemv_packed_M4", "decode_gemv_packed_M16"]

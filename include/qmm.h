@@ -372,6 +372,36 @@ qmm_status dynamic_quantize_matmul(const float* x, int64_t M, int64_t K, const v
                                    uint8_t* y_zero_point, void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The same chain on a weight packed once. TrainDeeploy PR #53, first
+ * paragraph: the weight is a frozen constant, so its exact fp16 copy and
+ * column sums need not be redone on every call.
+ *   dynamic_quantize_matmul_pack_weight  writes, into `packed` (device, at
+ *       least dynamic_quantize_matmul_weight_bytes(K, N) bytes, 16-byte
+ *       aligned, caller-owned), W [K,N] of w_dtype as exact fp16 rows of
+ *       pitch N rounded up to 8, then colsum(W) as int32[N];
+ *   dynamic_quantize_matmul_packed  runs the quantiser on x and the GEMM with
+ *       its epilogue on that buffer: the same results, bit for bit, as
+ *       dynamic_quantize_matmul on the unpacked W. K, N and w_dtype must be
+ *       the ones the buffer was packed with, and the buffer must not change
+ *       in between (neither is checked on the device). The workspace holds
+ *       y's fp16 copy, its row sums and the quantiser's partials:
+ *       dynamic_quantize_matmul_packed_workspace_bytes(M, K) bytes, 16-byte
+ *       aligned. The zero points and the scales stay arguments of each call.
+ * Errors: as dynamic_quantize_matmul, plus QMM_ERR_INVALID_ARG for a null,
+ * unaligned or too short packed buffer. The size functions return 0 for an
+ * empty or out-of-range extent.
+ */
+size_t dynamic_quantize_matmul_weight_bytes(int64_t K, int64_t N);
+qmm_status dynamic_quantize_matmul_pack_weight(const void* W, int w_dtype, int64_t K, int64_t N, void* packed,
+                                               size_t packed_bytes, void* stream);
+size_t dynamic_quantize_matmul_packed_workspace_bytes(int64_t M, int64_t K);
+qmm_status dynamic_quantize_matmul_packed(const float* x, int64_t M, int64_t K, const void* packed,
+                                          size_t packed_bytes, int w_dtype, int64_t N, const float* w_scale,
+                                          int64_t w_scale_count, const void* w_zero_point, int64_t w_zp_count,
+                                          const float* bias, float* C, float* y_scale, uint8_t* y_zero_point,
+                                          void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * Form (d): DynamicQuantizeLinear, uint8 only. ROCm hip-ep PR #1248, section
  * "What", DynamicQuantizeLinear paragraph (reduce to a scalar min and max,
  * scale (max-min)/255 with a zero range selecting scale 1, ties-to-even zero

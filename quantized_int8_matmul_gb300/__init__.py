@@ -14,6 +14,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+from typing import NamedTuple
 
 import torch
 
@@ -66,6 +67,13 @@ def _load() -> ctypes.CDLL:
     lib.dynamic_quantize_matmul_workspace_bytes.argtypes = [i64, i64, i64]
     lib.dynamic_quantize_matmul_workspace_bytes.restype = sz
     lib.dynamic_quantize_matmul.argtypes = [vp, i64, i64, vp, ci, i64, vp, i64, vp, i64, vp, vp, vp, vp, vp, sz, vp]
+    lib.dynamic_quantize_matmul_weight_bytes.argtypes = [i64, i64]
+    lib.dynamic_quantize_matmul_weight_bytes.restype = sz
+    lib.dynamic_quantize_matmul_pack_weight.argtypes = [vp, ci, i64, i64, vp, sz, vp]
+    lib.dynamic_quantize_matmul_packed_workspace_bytes.argtypes = [i64, i64]
+    lib.dynamic_quantize_matmul_packed_workspace_bytes.restype = sz
+    lib.dynamic_quantize_matmul_packed.argtypes = [vp, i64, i64, vp, sz, ci, i64, vp, i64, vp, i64, vp, vp, vp, vp,
+                                                   vp, sz, vp]
     lib.qmm_a8w8_pack.argtypes = [vp, vp, i64, i64, i64, vp, sz, vp]
     lib.qmm_a8w8_packed.argtypes = [i64, i64, i64, vp, i64, vp, i64, vp, ci, vp, sz, vp]
     lib.qmm_a8w8_host_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, ci]
@@ -509,6 +517,81 @@ def dynamic_quantize_matmul(x, W, w_scale, w_zero_point=None, bias=None, out=Non
     return out, ys, yz
 
 
+class DqmPackedWeight(NamedTuple):
+    """A weight packed once for dynamic_quantize_matmul_packed: the device
+    buffer (exact fp16 copy and column sums) and the extents and dtype it was
+    packed with."""
+    buf: torch.Tensor
+    K: int
+    N: int
+    dtype: torch.dtype
+
+
+def dynamic_quantize_matmul_weight_bytes(K: int, N: int) -> int:
+    return int(_lib.dynamic_quantize_matmul_weight_bytes(K, N))
+
+
+def dynamic_quantize_matmul_packed_workspace_bytes(M: int, K: int) -> int:
+    return int(_lib.dynamic_quantize_matmul_packed_workspace_bytes(M, K))
+
+
+def dynamic_quantize_matmul_pack_weight(W, packed=None, stream=None) -> DqmPackedWeight:
+    """Pack a frozen int8/uint8 weight W [K, N] once for the fused chain."""
+    _need(W, (torch.int8, torch.uint8), "W")
+    if W.dim() != 2:
+        raise ValueError("W [K, N] expected")
+    K, N = W.shape
+    nbytes = dynamic_quantize_matmul_weight_bytes(K, N)
+    if nbytes == 0:
+        raise QmmError("dynamic_quantize_matmul_pack_weight", QMM_ERR_INVALID_ARG)
+    if packed is None:
+        packed = torch.empty(nbytes, dtype=torch.uint8, device=W.device)
+    _check("dynamic_quantize_matmul_pack_weight",
+           _lib.dynamic_quantize_matmul_pack_weight(_ptr(W), _TORCH_TO_QMM[W.dtype], K, N, _ptr(packed),
+                                                    packed.numel() * packed.element_size(), _stream(stream)))
+    return DqmPackedWeight(packed, K, N, W.dtype)
+
+
+def dynamic_quantize_matmul_packed(x, weight: DqmPackedWeight, w_scale, w_zero_point=None, bias=None, out=None,
+                                   stream=None, workspace="auto"):
+    """dynamic_quantize_matmul on a weight packed by
+    dynamic_quantize_matmul_pack_weight: the same results, bit for bit."""
+    _need(x, (torch.float32,), "x")
+    _need(w_scale, (torch.float32,), "w_scale")
+    M, K = x.shape if x.dim() == 2 else (None, None)
+    if M is None or K != weight.K:
+        raise ValueError("x [M, K] expected, K as packed")
+    N = weight.N
+    if w_scale.numel() not in (1, N):
+        raise ValueError("w_scale must have 1 or N values")
+    zc = 0
+    if w_zero_point is not None:
+        _need(w_zero_point, (weight.dtype,), "w_zero_point")
+        zc = w_zero_point.numel()
+    if bias is not None:
+        _need(bias, (torch.float32,), "bias")
+        if bias.numel() != N:
+            raise ValueError("bias must have N values")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float32, device=x.device)
+    _need(out, (torch.float32,), "out")
+    ys = torch.empty(1, dtype=torch.float32, device=x.device)
+    yz = torch.empty(1, dtype=torch.uint8, device=x.device)
+    nbytes = dynamic_quantize_matmul_packed_workspace_bytes(M, K)
+    if isinstance(workspace, str) and workspace == "auto":
+        workspace = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=x.device)
+    if workspace is None:
+        raise ValueError("the packed chain needs a workspace")
+    buf = weight.buf
+    st = _lib.dynamic_quantize_matmul_packed(_ptr(x), M, K, _ptr(buf), buf.numel() * buf.element_size(),
+                                             _TORCH_TO_QMM[weight.dtype], N, _ptr(w_scale), w_scale.numel(),
+                                             _ptr(w_zero_point), zc, _ptr(bias), _ptr(out), _ptr(ys), _ptr(yz),
+                                             _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                             _stream(stream))
+    _check("dynamic_quantize_matmul_packed", st)
+    return out, ys, yz
+
+
 def matmul_integer(A, B, a_zero_point=None, b_zero_point=None, out=None, stream=None, workspace="auto"):
     """Form (c): int32 C = (A - a_zp) @ (B - b_zp), A [...,M,K], B [K,N] (shared) or [...,K,N].
 
@@ -606,6 +689,7 @@ def num_sms() -> int:
 
 __all__ = [
     "qmm_w8_dequant", "qmm_a8w8", "qmm_a8w8_acc", "matmul_integer", "conv_integer", "dynamic_quantize_matmul",
+    "dynamic_quantize_matmul_pack_weight", "dynamic_quantize_matmul_packed", "DqmPackedWeight",
     "dynamic_quantize_linear",
     "dynamic_quantize_linear_workspace_bytes", "last_kernel", "check_device_error", "QmmError", "lib",
     "num_sms", "LIB_PATH",

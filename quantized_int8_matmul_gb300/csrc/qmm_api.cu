@@ -349,17 +349,44 @@ struct DqmPlan {
   size_t off_a = 0, off_b = 0, off_rs = 0, off_cs = 0, off_sz = 0, bytes = 0;
 };
 
-DqmPlan dqm_plan(int64_t M, int64_t K, int64_t N) {
+// with_weight = false leaves out the weight's fp16 copy and column sums (they
+// live in a buffer packed once by dynamic_quantize_matmul_pack_weight)
+DqmPlan dqm_plan(int64_t M, int64_t K, int64_t N, bool with_weight = true) {
   DqmPlan pl;
   pl.Kp = (K + 7) / 8 * 8;
   pl.Np = (N + 7) / 8 * 8;
   pl.off_a = round256(dynamic_quantize_linear_workspace_bytes(M * K));
   pl.off_b = pl.off_a + round256((size_t)M * pl.Kp * 2);
-  pl.off_rs = pl.off_b + round256((size_t)K * pl.Np * 2);
+  pl.off_rs = pl.off_b + (with_weight ? round256((size_t)K * pl.Np * 2) : 0);
   pl.off_cs = pl.off_rs + round256((size_t)M * 4);
-  pl.off_sz = pl.off_cs + round256((size_t)N * 4);
+  pl.off_sz = pl.off_cs + (with_weight ? round256((size_t)N * 4) : 0);
   pl.bytes = pl.off_sz + 256;
   return pl;
+}
+
+// The packed weight of the chain: W as exact fp16 [K][Np] (Np = N rounded up
+// to 8, pad columns unspecified), then colsum(W) as int32[N].
+struct DqmWeight {
+  int64_t Np = 0;
+  size_t off_cs = 0, bytes = 0;
+};
+
+DqmWeight dqm_weight(int64_t K, int64_t N) {
+  DqmWeight w;
+  w.Np = (N + 7) / 8 * 8;
+  w.off_cs = round256((size_t)K * w.Np * 2);
+  w.bytes = w.off_cs + round256((size_t)N * 4);
+  return w;
+}
+
+// W -> exact fp16 copy with pitch Np plus its column sums, on stream st
+cudaError_t dqm_convert_weight(const void* W, bool wu, int64_t K, int64_t N, int64_t Np, __half* b16, int* cs,
+                               cudaStream_t st) {
+  if (N % 16 == 0 && aligned16(W)) return launch_convert_cols(W, wu, b16, 1, (int)K, (int)N, cs, st);
+  const ConvPlane none{nullptr, 0, 0, 0, 0, nullptr, 0};
+  const ConvPlane pb{W, N, (int)K, (int)N, 0, b16, Np};
+  cudaError_t e = launch_convert_planes(none, false, pb, wu, st);
+  return e == cudaSuccess ? launch_colsum(W, wu, (int)K, (int)N, cs, st) : e;
 }
 }  // namespace
 
@@ -1318,56 +1345,38 @@ size_t dynamic_quantize_matmul_workspace_bytes(int64_t M, int64_t K, int64_t N) 
   return dqm_plan(M, K, N).bytes;
 }
 
-qmm_status dynamic_quantize_matmul(const float* x, int64_t M, int64_t K, const void* W, int w_dtype, int64_t N,
-                                   const float* w_scale, int64_t w_scale_count, const void* w_zero_point,
-                                   int64_t w_zp_count, const float* bias, float* C, float* y_scale,
-                                   uint8_t* y_zero_point, void* workspace, size_t workspace_bytes, void* stream) {
+namespace {
+
+// Host checks shared by the chain's two entry points; QMM_OK means "go on",
+// with *nothing = true for an empty output (nothing to launch).
+qmm_status dqm_check(int64_t M, int64_t K, int64_t N, int w_dtype, int64_t w_scale_count, int64_t w_zp_count,
+                     bool* nothing) {
+  *nothing = false;
   if (!dim_ok(M) || !dim_ok(K) || !dim_ok(N)) return QMM_ERR_INVALID_ARG;
   if (w_dtype != QMM_S8 && w_dtype != QMM_U8) return QMM_ERR_INVALID_ARG;
   if (w_scale_count != 1 && w_scale_count != N) return QMM_ERR_INVALID_ARG;
   if (w_zp_count != 0 && w_zp_count != 1 && w_zp_count != N) return QMM_ERR_INVALID_ARG;
   if (M == 0 || N == 0) {
-    t_last_kernel = "none";
+    *nothing = true;
     return QMM_OK;
   }
   if (K == 0) return QMM_ERR_UNSUPPORTED;
-  if (!x || !W || !w_scale || !C || (w_zp_count > 0 && !w_zero_point)) return QMM_ERR_INVALID_ARG;
-  const DqmPlan pl = dqm_plan(M, K, N);
-  if (!workspace || !aligned16(workspace) || workspace_bytes < pl.bytes) return QMM_ERR_INVALID_ARG;
   if (((M + 255) / 256) * ((N + 223) / 224) > (int64_t)INT_MAX || M * K / 32768 > (int64_t)INT_MAX)
     return QMM_ERR_UNSUPPORTED;
-  unsigned* err = err_word();
-  if (!err) return QMM_ERR_CUDA;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaGetLastError();
-  const bool wu = w_dtype == QMM_U8;
-  uint8_t* base = static_cast<uint8_t*>(workspace);
-  __half* a16 = reinterpret_cast<__half*>(base + pl.off_a);
-  __half* b16 = reinterpret_cast<__half*>(base + pl.off_b);
-  int* rs = reinterpret_cast<int*>(base + pl.off_rs);
-  int* cs = reinterpret_cast<int*>(base + pl.off_cs);
-  float* ys = y_scale ? y_scale : reinterpret_cast<float*>(base + pl.off_sz);
-  uint8_t* yz = y_zero_point ? y_zero_point : base + pl.off_sz + 16;
-  // the weight (exact fp16 copy and column sums, the y_zp term) on a side stream,
-  // beside the activations' DynamicQuantizeLinear straight into the fp16
-  // operand with rowsum(y)
-  auto side = [&](cudaStream_t st) {
-    if (N % 16 == 0 && aligned16(W)) return launch_convert_cols(W, wu, b16, 1, (int)K, (int)N, cs, st);
-    const ConvPlane none{nullptr, 0, 0, 0, 0, nullptr, 0};
-    const ConvPlane pb{W, N, (int)K, (int)N, 0, b16, pl.Np};
-    cudaError_t e2 = launch_convert_planes(none, false, pb, wu, st);
-    return e2 == cudaSuccess ? launch_colsum(W, wu, (int)K, (int)N, cs, st) : e2;
-  };
-  auto primary = [&](cudaStream_t st) {
-    return launch_dql_rows_f16(x, M, K, a16, pl.Kp, ys, yz, rs, reinterpret_cast<float*>(base),
-                               dql_num_partials(M * K), st);
-  };
-  cudaError_t e = fork_join(s, side, primary);
+  return QMM_OK;
+}
+
+// The chain's GEMM: acc from y's fp16 copy (rows of pitch Kp) and W's (pitch
+// Np), zero points and sums applied, times y_scale * w_scale[n], plus bias.
+cudaError_t dqm_gemm(const __half* a16, int64_t Kp, const __half* b16, int64_t Np, const int* rs, const int* cs,
+                     const float* ys, const uint8_t* yz, bool wu, int64_t M, int64_t K, int64_t N,
+                     const float* w_scale, int64_t w_scale_count, const void* w_zero_point, int64_t w_zp_count,
+                     const float* bias, float* C, unsigned* err, cudaStream_t s) {
   GemmF16Args f{};
   f.A16 = a16;
   f.B16 = b16;
-  f.a_pitch = (int)pl.Kp;
-  f.b_pitch = (int)pl.Np;
+  f.a_pitch = (int)Kp;
+  f.b_pitch = (int)Np;
   f.batch = 1;
   f.M = (int)M;
   f.K = (int)K;
@@ -1387,8 +1396,109 @@ qmm_status dynamic_quantize_matmul(const float* x, int64_t M, int64_t K, const v
   f.zp_row_mod = (int)M;
   f.err = err;
   const char* gname = "none";
-  if (e == cudaSuccess) e = launch_gemm_f16pair(f, true, wu, true, chunk_k_for(true, wu), s, &gname);
+  return launch_gemm_f16pair(f, true, wu, true, chunk_k_for(true, wu), s, &gname);
+}
+
+}  // namespace
+
+qmm_status dynamic_quantize_matmul(const float* x, int64_t M, int64_t K, const void* W, int w_dtype, int64_t N,
+                                   const float* w_scale, int64_t w_scale_count, const void* w_zero_point,
+                                   int64_t w_zp_count, const float* bias, float* C, float* y_scale,
+                                   uint8_t* y_zero_point, void* workspace, size_t workspace_bytes, void* stream) {
+  bool nothing = false;
+  const qmm_status chk = dqm_check(M, K, N, w_dtype, w_scale_count, w_zp_count, &nothing);
+  if (chk != QMM_OK) return chk;
+  if (nothing) {
+    t_last_kernel = "none";
+    return QMM_OK;
+  }
+  if (!x || !W || !w_scale || !C || (w_zp_count > 0 && !w_zero_point)) return QMM_ERR_INVALID_ARG;
+  const DqmPlan pl = dqm_plan(M, K, N);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < pl.bytes) return QMM_ERR_INVALID_ARG;
+  unsigned* err = err_word();
+  if (!err) return QMM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  const bool wu = w_dtype == QMM_U8;
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  __half* a16 = reinterpret_cast<__half*>(base + pl.off_a);
+  __half* b16 = reinterpret_cast<__half*>(base + pl.off_b);
+  int* rs = reinterpret_cast<int*>(base + pl.off_rs);
+  int* cs = reinterpret_cast<int*>(base + pl.off_cs);
+  float* ys = y_scale ? y_scale : reinterpret_cast<float*>(base + pl.off_sz);
+  uint8_t* yz = y_zero_point ? y_zero_point : base + pl.off_sz + 16;
+  // the weight (exact fp16 copy and column sums, the y_zp term) on a side stream,
+  // beside the activations' DynamicQuantizeLinear straight into the fp16
+  // operand with rowsum(y)
+  auto side = [&](cudaStream_t st) { return dqm_convert_weight(W, wu, K, N, pl.Np, b16, cs, st); };
+  auto primary = [&](cudaStream_t st) {
+    return launch_dql_rows_f16(x, M, K, a16, pl.Kp, ys, yz, rs, reinterpret_cast<float*>(base),
+                               dql_num_partials(M * K), st);
+  };
+  cudaError_t e = fork_join(s, side, primary);
+  if (e == cudaSuccess)
+    e = dqm_gemm(a16, pl.Kp, b16, pl.Np, rs, cs, ys, yz, wu, M, K, N, w_scale, w_scale_count, w_zero_point,
+                 w_zp_count, bias, C, err, s);
   return finish_launch(e, "dql_f16+gemm_tc05_pair_f16ops_matmul_integer_dequant");
+}
+
+size_t dynamic_quantize_matmul_weight_bytes(int64_t K, int64_t N) {
+  if (!dim_ok(K) || !dim_ok(N) || K == 0 || N == 0) return 0;
+  return dqm_weight(K, N).bytes;
+}
+
+qmm_status dynamic_quantize_matmul_pack_weight(const void* W, int w_dtype, int64_t K, int64_t N, void* packed,
+                                               size_t packed_bytes, void* stream) {
+  if (!dim_ok(K) || !dim_ok(N) || K == 0 || N == 0) return QMM_ERR_INVALID_ARG;
+  if (w_dtype != QMM_S8 && w_dtype != QMM_U8) return QMM_ERR_INVALID_ARG;
+  const DqmWeight pw = dqm_weight(K, N);
+  if (!W || !packed || !aligned16(packed) || packed_bytes < pw.bytes) return QMM_ERR_INVALID_ARG;
+  cudaGetLastError();
+  uint8_t* base = static_cast<uint8_t*>(packed);
+  const cudaError_t e = dqm_convert_weight(W, w_dtype == QMM_U8, K, N, pw.Np, reinterpret_cast<__half*>(base),
+                                           reinterpret_cast<int*>(base + pw.off_cs), static_cast<cudaStream_t>(stream));
+  return finish_launch(e, "dqm_weight_f16");
+}
+
+size_t dynamic_quantize_matmul_packed_workspace_bytes(int64_t M, int64_t K) {
+  if (!dim_ok(M) || !dim_ok(K) || M == 0 || K == 0) return 0;
+  return dqm_plan(M, K, 0, false).bytes;
+}
+
+qmm_status dynamic_quantize_matmul_packed(const float* x, int64_t M, int64_t K, const void* packed,
+                                          size_t packed_bytes, int w_dtype, int64_t N, const float* w_scale,
+                                          int64_t w_scale_count, const void* w_zero_point, int64_t w_zp_count,
+                                          const float* bias, float* C, float* y_scale, uint8_t* y_zero_point,
+                                          void* workspace, size_t workspace_bytes, void* stream) {
+  bool nothing = false;
+  const qmm_status chk = dqm_check(M, K, N, w_dtype, w_scale_count, w_zp_count, &nothing);
+  if (chk != QMM_OK) return chk;
+  if (nothing) {
+    t_last_kernel = "none";
+    return QMM_OK;
+  }
+  if (!x || !w_scale || !C || (w_zp_count > 0 && !w_zero_point)) return QMM_ERR_INVALID_ARG;
+  const DqmWeight pw = dqm_weight(K, N);
+  if (!packed || !aligned16(packed) || packed_bytes < pw.bytes) return QMM_ERR_INVALID_ARG;
+  const DqmPlan pl = dqm_plan(M, K, N, false);
+  if (!workspace || !aligned16(workspace) || workspace_bytes < pl.bytes) return QMM_ERR_INVALID_ARG;
+  unsigned* err = err_word();
+  if (!err) return QMM_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaGetLastError();
+  uint8_t* base = static_cast<uint8_t*>(workspace);
+  const uint8_t* wbase = static_cast<const uint8_t*>(packed);
+  __half* a16 = reinterpret_cast<__half*>(base + pl.off_a);
+  int* rs = reinterpret_cast<int*>(base + pl.off_rs);
+  float* ys = y_scale ? y_scale : reinterpret_cast<float*>(base + pl.off_sz);
+  uint8_t* yz = y_zero_point ? y_zero_point : base + pl.off_sz + 16;
+  cudaError_t e = launch_dql_rows_f16(x, M, K, a16, pl.Kp, ys, yz, rs, reinterpret_cast<float*>(base),
+                                      dql_num_partials(M * K), s);
+  if (e == cudaSuccess)
+    e = dqm_gemm(a16, pl.Kp, reinterpret_cast<const __half*>(wbase), pw.Np,
+                 rs, reinterpret_cast<const int*>(wbase + pw.off_cs), ys, yz, w_dtype == QMM_U8, M, K, N, w_scale,
+                 w_scale_count, w_zero_point, w_zp_count, bias, C, err, s);
+  return finish_launch(e, "dql_f16+gemm_tc05_pair_f16ops_matmul_integer_dequant_packed");
 }
 
 size_t dynamic_quantize_linear_workspace_bytes(int64_t n) {

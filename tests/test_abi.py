@@ -206,3 +206,28 @@ def test_decode_pack_sizes_follow_the_layout(qmm):
     assert lib.qmm_w8_dequant_packed_workspace_bytes(4, 8192) >= 8 * 8192 * 2
     assert lib.qmm_w8_dequant_packed_workspace_bytes(9, 8192) >= 16 * 8192 * 2
     assert lib.qmm_w8_dequant_packed_workspace_bytes(17, 8192) == 0
+
+
+def test_packed_chain_sizes_and_host_checks(qmm):
+    """The chain's packed weight holds the fp16 copy (pitch N rounded to 8)
+    and N column sums; the packed call's workspace holds no weight, and the
+    host rejects a short or null packed buffer before any launch."""
+    lib = qmm.lib()
+    assert lib.dynamic_quantize_matmul_weight_bytes(4096, 11008) >= 4096 * 11008 * 2 + 11008 * 4
+    assert lib.dynamic_quantize_matmul_weight_bytes(100, 5) >= 100 * 8 * 2 + 5 * 4
+    assert lib.dynamic_quantize_matmul_weight_bytes(0, 5) == 0
+    full = lib.dynamic_quantize_matmul_workspace_bytes(512, 4096, 11008)
+    act = lib.dynamic_quantize_matmul_packed_workspace_bytes(512, 4096)
+    assert act >= 512 * 4096 * 2 and full - act >= 4096 * 11008 * 2
+    P = ctypes.c_void_p(256)
+    need = lib.dynamic_quantize_matmul_weight_bytes(8, 3)
+    ws = lib.dynamic_quantize_matmul_packed_workspace_bytes(4, 8)
+
+    def call(packed=P, pb=need, wdt=qmm.QMM_S8, w=P, wb=ws):
+        return lib.dynamic_quantize_matmul_packed(P, 4, 8, packed, pb, wdt, 3, P, 1, None, 0, None, P, None, None,
+                                                  w, wb, None)
+    assert call(pb=need - 1) == qmm.QMM_ERR_INVALID_ARG
+    assert call(packed=None) == qmm.QMM_ERR_INVALID_ARG
+    assert call(wdt=qmm.QMM_F32) == qmm.QMM_ERR_INVALID_ARG
+    assert call(wb=ws - 1) == qmm.QMM_ERR_INVALID_ARG
+    assert lib.dynamic_quantize_matmul_pack_weight(P, qmm.QMM_U8, 8, 3, P, need - 1, None) == qmm.QMM_ERR_INVALID_ARG
