@@ -23,12 +23,23 @@
 // register is one byte permute into the mantissa of 1024 plus one half2
 // subtraction away: about one instruction per weight byte, no interleaving,
 // no address predicates (K and N are padded in the packed layout).
+//
+// The activations enter as fp16 copies of the bf16 rows scaled by a power of
+// two per row (exact: the largest magnitude lands in [2^14, 2^15)). A row of
+// up to 8192 values is prepared inside every CTA, into its shared memory,
+// while its first weight loads are in flight; larger row sets are prepared by
+// a small kernel the GEMV overlaps through programmatic dependent launch. The
+// MMAs read each step's activation fragment just before use, from shared
+// memory or from L1 (every CTA on an SM reads the same rows), so the register
+// ring holds weight bytes only.
 #include "common.cuh"
 #include "kernels.h"
 
 #include <algorithm>
 #include <climits>
+#include <map>
 #include <mutex>
+#include <utility>
 
 namespace qmm {
 namespace gvp {
@@ -74,20 +85,23 @@ __global__ void __launch_bounds__(256) pack_kernel(const int8_t* __restrict__ W,
   }
 }
 
-// One CTA per activation row (rows M..Mp-1: zeros): a power-of-two scale 2^s
-// that puts the row's largest magnitude in [2^14, 2^15), then the scaled fp16
-// row in natural K order, zero-padded to Kp.
-__global__ void __launch_bounds__(256) prep_kernel(const uint16_t* __restrict__ A, int M, int K, int Kp,
+// Power-of-two row scale: s puts the row's largest magnitude mx in
+// [2^14, 2^15); 0 for an all-zero or non-finite row; clamped to [-100, 100]
+// so that 2^s and 2^-s are normal floats.
+__device__ __forceinline__ int row_shift(float mx) {
+  const uint32_t ex = (__float_as_uint(mx) >> 23) & 0xFFu;
+  return (mx > 0.f && ex != 0xFFu) ? max(-100, min(100, 14 - ((int)ex - 127))) : 0;
+}
+
+// One CTA per activation row: a power-of-two scale 2^s that puts the row's
+// largest magnitude in [2^14, 2^15), then the scaled fp16 row in natural K
+// order, zero-padded to Kp. (The GEMV reads no row past M.)
+__global__ void __launch_bounds__(256) prep_kernel(const uint16_t* __restrict__ A, int K, int Kp,
                                                    uint16_t* __restrict__ A16, float* __restrict__ inv) {
   asm volatile("griddepcontrol.launch_dependents;");   // the GEMV starts its weight stream meanwhile
   __shared__ float red[8];
   const int row = blockIdx.x;
   uint16_t* d = A16 + (size_t)row * Kp;
-  if (row >= M) {
-    for (int k0 = threadIdx.x * 8; k0 < Kp; k0 += 256 * 8) *reinterpret_cast<uint4*>(d + k0) = make_uint4(0, 0, 0, 0);
-    if (threadIdx.x == 0) inv[row] = 1.f;
-    return;
-  }
   const uint16_t* a = A + (size_t)row * K;
   float mx = 0.f;
   for (int k = threadIdx.x * 8; k < K; k += 256 * 8) {   // K % 8 == 0: 16-byte loads
@@ -106,11 +120,7 @@ __global__ void __launch_bounds__(256) prep_kernel(const uint16_t* __restrict__ 
   mx = red[0];
 #pragma unroll
   for (int i = 1; i < 8; ++i) mx = fmaxf(mx, red[i]);
-  // s: 0 for an all-zero or non-finite row; within [-100, 100] so that 2^s and
-  // 2^-s are normal floats
-  int sh = 0;
-  const uint32_t ex = (__float_as_uint(mx) >> 23) & 0xFFu;
-  if (mx > 0.f && ex != 0xFFu) sh = max(-100, min(100, 14 - ((int)ex - 127)));
+  const int sh = row_shift(mx);
   const float up = __uint_as_float((uint32_t)(127 + sh) << 23);
   if (threadIdx.x == 0) inv[row] = __uint_as_float((uint32_t)(127 - sh) << 23);
   // K % 8 == 0: every 8-element group is wholly inside the row or wholly padding
@@ -148,30 +158,21 @@ __device__ __forceinline__ uint32_t biased_pair_to_half2(uint32_t x) {
   return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-__device__ __forceinline__ uint2 ldg_nc_v2(const void* p) {
+// The activation fragments, read just before their MMAs: every CTA on the SM
+// reads the same rows, so they are kept in L1.
+__device__ __forceinline__ uint2 ldg_v2_l1(const void* p) {
   uint2 v;
-  asm volatile("ld.global.nc.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
+  asm volatile("ld.global.nc.L1::evict_last.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p));
   return v;
 }
 
-// One warp step of one lane: its 32 packed weight bytes and its activation fragments.
+// One warp step of one lane: its 32 packed weight bytes (loaded D steps
+// ahead) and its activation fragments (read just before the MMAs).
 template <int MT>
 struct Step {
   uint4 w[2];
   uint32_t b[MT][2];   // activation rows 8 nt + g, k 4t..4t+3
 };
-
-template <int MT>
-__device__ __forceinline__ void load_step(Step<MT>& st, const uint8_t* wp, const uint16_t* const (&arow)[MT], int k) {
-  st.w[0] = ldg_nc_v4(wp);
-  st.w[1] = ldg_nc_v4(wp + 16);
-#pragma unroll
-  for (int nt = 0; nt < MT; ++nt) {
-    const uint2 v = ldg_nc_v2(arow[nt] + k);
-    st.b[nt][0] = v.x;
-    st.b[nt][1] = v.y;
-  }
-}
 
 template <int MT, bool ZP>
 __device__ __forceinline__ void compute_step(const Step<MT>& st, float (&acc)[4][MT][4], float (&rs)[MT][4]) {
@@ -201,20 +202,93 @@ struct Sizes {
 
 struct PackedArgs {
   const uint8_t* Wp;       // packed weight
-  const uint16_t* A16;     // [Mp][Kp] fp16, rows >= M zero
-  const float* inv;        // [Mp] 2^-s per row
+  const uint16_t* A;       // bf16 bits [M][K] (the in-CTA prep reads these)
+  const uint16_t* A16;     // [M][Kp] fp16 (written by prep_kernel), row pitch Kp
+  const float* inv;        // [M] 2^-s per row
   int M, K, N, Kp;
   const float* scale; int scale_count;
   const int32_t* zp;  int zp_count;
   void* C; int c_f32;
 };
 
+// Eight bf16 values scaled by 2^s (exact) and rounded to fp16.
+__device__ __forceinline__ uint4 bf16x8_to_scaled_f16(const uint4 v, const float up) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const __half2 h2 = __floats2half2_rn(__fmul_rn(__uint_as_float(w[q] << 16), up),
+                                         __fmul_rn(__uint_as_float(w[q] & 0xFFFF0000u), up));
+    o[q] = *reinterpret_cast<const uint32_t*>(&h2);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// The prep inside each CTA (rows 0..M-1 only): every CTA finds each row's
+// largest magnitude over all of K (so the CTAs of a split K share one scale
+// per row, as with prep_kernel), then writes its own K range of the rows as
+// scaled fp16 into shared memory, rows `pitch` halves apart, and 2^-s into
+// inv_s. The fp16 values are those prep_kernel writes.
+template <int NW>
+__device__ __forceinline__ void prep_in_cta(const PackedArgs& p, int k_beg, int k_len, uint16_t* act, int pitch,
+                                            float* inv_s) {
+  __shared__ float rmax[NW][8];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int m = 0; m < p.M; ++m) {
+    const uint16_t* a = p.A + (size_t)m * p.K;
+    float mx = 0.f;
+    for (int k = tid * 8; k < p.K; k += NW * 32 * 8) {   // K % 8 == 0: 16-byte loads
+      const uint4 v = *reinterpret_cast<const uint4*>(a + k);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        mx = fmaxf(mx, fabsf(__uint_as_float(w[i] << 16)));
+        mx = fmaxf(mx, fabsf(__uint_as_float(w[i] & 0xFFFF0000u)));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) rmax[warp][m] = mx;
+  }
+  __syncthreads();
+  for (int m = 0; m < p.M; ++m) {
+    float mx = rmax[0][m];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) mx = fmaxf(mx, rmax[w][m]);
+    const int sh = row_shift(mx);
+    const float up = __uint_as_float((uint32_t)(127 + sh) << 23);
+    if (tid == 0) inv_s[m] = __uint_as_float((uint32_t)(127 - sh) << 23);
+    const uint16_t* a = p.A + (size_t)m * p.K;
+    for (int k = tid * 8; k < k_len; k += NW * 32 * 8) {   // groups of 8 wholly inside K or wholly padding
+      const int kg = k_beg + k;
+      const uint4 v = kg < p.K ? *reinterpret_cast<const uint4*>(a + kg) : make_uint4(0u, 0u, 0u, 0u);
+      *reinterpret_cast<uint4*>(act + (size_t)m * pitch + k) = bf16x8_to_scaled_f16(v, up);
+    }
+  }
+  __syncthreads();
+}
+
+__device__ __forceinline__ uint2 lds_v2(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr));
+  return v;
+}
+
+// Shared-memory pitch (halves) of the in-CTA prep's rows: 16 halves of
+// padding put consecutive rows 8 banks apart.
+__host__ __device__ constexpr int act_pitch(int k_len) { return k_len + 16; }
+
 // grid (slabs, S), cluster (1, S, 1): CTA (slab, ks) covers columns
 // [64 slab, 64 slab + 64) and K steps [ks * spc, (ks + 1) * spc); its NW
 // warps take the steps in turn, each keeping D steps of loads in flight.
-template <int MT, bool ZP, int NW, int D, int MINB>
+// FP: the rows are prepared inside the CTA (prep_in_cta) instead of by
+// prep_kernel; at most 8 rows.
+template <int MT, bool ZP, int NW, int D, int MINB, bool FP>
 __global__ void __launch_bounds__(NW * 32, MINB) gemv_packed_kernel(const PackedArgs p, const int spc) {
+  static_assert(!FP || MT == 1, "in-CTA prep: up to 8 rows");
   constexpr int NV = Sizes<MT, ZP>::NV;
+  extern __shared__ __align__(16) uint16_t act_s[];   // FP: [M][act_pitch(spc * STEP)] fp16
+  __shared__ float inv_s[8];
   __shared__ float red[NW / 2][NV][32];   // the warp reduction (half the warps' values in flight)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int g = lane >> 2, t = lane & 3;
@@ -250,25 +324,36 @@ __global__ void __launch_bounds__(NW * 32, MINB) gemv_packed_kernel(const Packed
     }
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  bool live[MT];   // activation rows past M are zero: not loaded
 #pragma unroll
-  for (int d = 0; d < D; ++d) {
-    const int st = warp + d * NW;
-    if (st < nsteps)
-#pragma unroll
-      for (int nt = 0; nt < MT; ++nt) {
-        const uint2 v = ldg_nc_v2(arow[nt] + st * STEP);
-        ring[d].b[nt][0] = v.x;
-        ring[d].b[nt][1] = v.y;
-      }
+  for (int nt = 0; nt < MT; ++nt) live[nt] = 8 * nt + g < p.M;
+  const int pitch = act_pitch(spc * STEP);
+  uint32_t act_lane = 0;   // FP: this lane's row g, k 4t, in shared memory
+  if (FP) {
+    prep_in_cta<NW>(p, s_beg * STEP, nsteps * STEP, act_s, pitch, inv_s);
+    act_lane = smem_u32(act_s) + (uint32_t)((g * pitch + 4 * t) * 2);
   }
   for (int base = warp; base < nsteps; base += D * NW) {
 #pragma unroll
     for (int d = 0; d < D; ++d) {
       const int st = base + d * NW;
       if (st < nsteps) {
+        // the activation fragments: rows read by every CTA on the SM, so hot in L1
+#pragma unroll
+          for (int nt = 0; nt < MT; ++nt) {
+            const uint2 v = !live[nt] ? make_uint2(0u, 0u)
+                            : FP      ? lds_v2(act_lane + (uint32_t)(st * STEP * 2))
+                                      : ldg_v2_l1(arow[nt] + st * STEP);
+            ring[d].b[nt][0] = v.x;
+            ring[d].b[nt][1] = v.y;
+          }
         compute_step<MT, ZP>(ring[d], acc, rs);
         const int nx = st + D * NW;   // refill the slot just used
-        if (nx < nsteps) load_step<MT>(ring[d], wp + step_offset(slab, s_beg + nx, steps_all), arow, nx * STEP);
+        if (nx < nsteps) {
+          const uint8_t* q = wp + step_offset(slab, s_beg + nx, steps_all);
+          ring[d].w[0] = ldg_nc_v4(q);
+          ring[d].w[1] = ldg_nc_v4(q + 16);
+        }
       }
     }
   }
@@ -331,7 +416,7 @@ __global__ void __launch_bounds__(NW * 32, MINB) gemv_packed_kernel(const Packed
       for (int rp = 0; rp < 2; ++rp) {
         const int m = 8 * nt + 2 * t + rp;
         if (m >= p.M) continue;
-        const float inv = p.inv[m];
+        const float inv = FP ? inv_s[m] : p.inv[m];
         const float rsum = ZP ? v[Sizes<MT, ZP>::NACC + 2 * nt + rp] : 0.f;
         float o[8];
 #pragma unroll
@@ -372,27 +457,39 @@ __global__ void __launch_bounds__(NW * 32, MINB) gemv_packed_kernel(const Packed
   if (S > 1) cluster_sync_all();
 }
 
-template <int MT, bool ZP, int NW, int D, int MINB>
+// Largest shared-memory share of the in-CTA prep's rows per CTA (one row of
+// 8192). Shared memory takes its capacity from L1, which also holds the
+// weight stream's loads in flight: with 4 rows (64 KB per CTA, three CTAs per
+// SM) the 8192 x 28672 decode took 68 us against 51 us through prep_kernel,
+// with 2 rows (33 KB) the two routes tied, with 1 row the in-CTA prep saved
+// about 2 us (the prep kernel's latency before the first MMA).
+constexpr int kFpSmemMax = 16 * 1024 + 512;
+
+template <int MT, bool ZP, int NW, int D, int MINB, bool FP>
 cudaError_t launch_impl(const PackedArgs& a, cudaStream_t s) {
-  auto kern = gemv_packed_kernel<MT, ZP, NW, D, MINB>;
+  auto kern = gemv_packed_kernel<MT, ZP, NW, D, MINB, FP>;
   static std::mutex mu;
-  static int per_sm[64] = {};
+  static std::map<std::pair<int, int>, int> per_sm_of;   // (device, dynamic smem bytes) -> CTAs per SM
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const int steps_all = a.Kp / STEP;
+  // the in-CTA prep's rows for the whole K: the most any split of K needs
+  const int smem_full = FP ? a.M * act_pitch(a.Kp) * 2 : 0;
+  int per_sm = 0;
   {
     std::lock_guard<std::mutex> lk(mu);
-    if (!per_sm[dev]) {
+    auto it = per_sm_of.find({dev, smem_full});
+    if (it == per_sm_of.end()) {
       int n = 0;
-      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NW * 32, 0);
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, NW * 32, smem_full);
       if (e != cudaSuccess) return e;
-      per_sm[dev] = std::max(1, n);
+      it = per_sm_of.emplace(std::make_pair(dev, smem_full), std::max(1, n)).first;
     }
+    per_sm = it->second;
   }
-  const long long slots = (long long)per_sm[dev] * std::max(1, num_sms());
+  const long long slots = (long long)per_sm * std::max(1, num_sms());
   const int slabs = (int)(padded_n(a.N) / SLAB);
-  const int steps_all = a.Kp / STEP;
   // Split K over a cluster only while all CTAs still fit in one wave and
   // every warp keeps at least 2 * D steps.
   int S = 1;
@@ -408,14 +505,18 @@ cudaError_t launch_impl(const PackedArgs& a, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)slabs, (unsigned)S, 1);
   cfg.blockDim = dim3(NW * 32, 1, 1);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = FP ? (size_t)a.M * act_pitch(spc * STEP) * 2 : 0;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
+  cfg.numAttrs = FP ? 1 : 2;   // no prep kernel to overlap with the in-CTA prep
   e = cudaLaunchKernelEx(&cfg, kern, a, spc);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
+
+// The in-CTA prep applies to rows whose whole-K fp16 copy fits the per-CTA
+// shared-memory share.
+bool prep_fits_in_cta(int M, int Kp) { return M <= 8 && (long long)M * act_pitch(Kp) * 2 <= kFpSmemMax; }
 
 }  // namespace gvp
 
@@ -445,13 +546,17 @@ cudaError_t launch_gemv_packed(const GemvArgs& g, const void* packed, void* work
   if (g.M < 1 || g.M > 16 || g.K < 8 || g.K % 8 != 0 || g.N < 8 || g.N % 8 != 0) return cudaErrorInvalidValue;
   const int Mp = g.M <= 8 ? 8 : 16;
   const int Kp = (int)padded_k(g.K);
+  const bool fp = prep_fits_in_cta(g.M, Kp);
   uint16_t* a16 = static_cast<uint16_t*>(workspace);
   float* inv = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + ((size_t)Mp * Kp * 2 + 255) / 256 * 256);
-  prep_kernel<<<Mp, 256, 0, s>>>(g.A, g.M, g.K, Kp, a16, inv);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (!fp) {
+    prep_kernel<<<g.M, 256, 0, s>>>(g.A, g.K, Kp, a16, inv);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   PackedArgs a{};
   a.Wp = static_cast<const uint8_t*>(packed);
+  a.A = g.A;
   a.A16 = a16;
   a.inv = inv;
   a.M = g.M;
@@ -465,12 +570,16 @@ cudaError_t launch_gemv_packed(const GemvArgs& g, const void* packed, void* work
   a.C = g.C;
   a.c_f32 = g.c_f32;
   const bool zp = g.zp_count > 0;
+  if (fp) {
+    *kernel_name = zp ? "gemv_w8_packed_rows_in_cta_zp" : "gemv_w8_packed_rows_in_cta";
+    return zp ? launch_impl<1, true, 8, 4, 3, true>(a, s) : launch_impl<1, false, 8, 4, 3, true>(a, s);
+  }
   if (g.M <= 8) {
     *kernel_name = zp ? "gemv_prep_rows+gemv_w8_packed_zp" : "gemv_prep_rows+gemv_w8_packed";
-    return zp ? launch_impl<1, true, 8, 4, 3>(a, s) : launch_impl<1, false, 8, 4, 3>(a, s);
+    return zp ? launch_impl<1, true, 8, 4, 3, false>(a, s) : launch_impl<1, false, 8, 4, 3, false>(a, s);
   }
   *kernel_name = zp ? "gemv_prep_rows+gemv_w8_packed_m16_zp" : "gemv_prep_rows+gemv_w8_packed_m16";
-  return zp ? launch_impl<2, true, 8, 2, 3>(a, s) : launch_impl<2, false, 8, 2, 3>(a, s);
+  return zp ? launch_impl<2, true, 8, 2, 3, false>(a, s) : launch_impl<2, false, 8, 2, 3, false>(a, s);
 }
 
 }  // namespace qmm

@@ -16,8 +16,15 @@ pytestmark = pytest.mark.gpu
 q = pytest.importorskip("quantized_int8_matmul_gb300")
 
 
-def kernel_name(M, zp):
-    return "gemv_prep_rows+gemv_w8_packed" + ("_m16" if M > 8 else "") + ("_zp" if zp else "")
+def kernel_name(M, K, zp):
+    """Rows whose fp16 copy (row pitch K rounded to 16, plus 16) fits
+    16.5 KiB are prepared inside each CTA; otherwise by a prep kernel."""
+    Kp = -(-K // 16) * 16
+    if M <= 8 and M * (Kp + 16) * 2 <= 16 * 1024 + 512:
+        base = "gemv_w8_packed_rows_in_cta"
+    else:
+        base = "gemv_prep_rows+gemv_w8_packed" + ("_m16" if M > 8 else "")
+    return base + ("_zp" if zp else "")
 
 
 def run(A_bits, A_vals, B, scale, zp, out, cols=None):
@@ -28,7 +35,7 @@ def run(A_bits, A_vals, B, scale, zp, out, cols=None):
     C = q.qmm_w8_dequant_packed(bf16_dev(A_bits), packed, N, dev(scale), None if zp is None else dev(zp),
                                 out_dtype=out)
     q.check_device_error()
-    assert q.last_kernel() == kernel_name(M, zp is not None)
+    assert q.last_kernel() == kernel_name(M, K, zp is not None)
     got = host(C)
     gotf = bf16_bits_to_f64(got) if out == torch.bfloat16 else got.astype(np.float64)
     zpv = np.zeros(1, np.int32) if zp is None else zp
@@ -39,7 +46,7 @@ def run(A_bits, A_vals, B, scale, zp, out, cols=None):
         gotf = gotf[:, cols]
     exact = O.w8_dequant(A_vals, B, scale, zpv)
     bound = O.w8_dequant_error_bound(A_vals, B, scale, zpv)
-    assert_within(gotf, exact, bound, 7 if out == torch.bfloat16 else 23, kernel_name(M, zp is not None))
+    assert_within(gotf, exact, bound, 7 if out == torch.bfloat16 else 23, kernel_name(M, K, zp is not None))
     return C
 
 
@@ -59,6 +66,18 @@ def test_packed_decode_ragged_shapes(K, N):
     zero padding (a biased 0) and the prep's zero rows meet at the edges."""
     w = W.decode_gemv(5, K=K, N=N, seed=K + N)
     z = np.arange(-5, N - 5, dtype=np.int32) % 11 - 5
+    run(w.A_bits, w.A, w.W, w.scale, z, torch.float32)
+
+
+@pytest.mark.parametrize("M,K,N", [(1, 8192, 640), (2, 4096, 640), (4, 2056, 136), (3, 16384, 192),
+                                   (8, 1024, 256), (8, 8192, 640), (5, 8192, 1024), (2, 8192, 640)])
+def test_packed_decode_split_k_and_both_preps(M, K, N):
+    """Few slabs, so K is split over a cluster (up to 8 CTAs): with the rows
+    prepared inside each CTA (every CTA scales by the whole row's maximum and
+    keeps only its K range) and, for rows too large for that, by the prep
+    kernel."""
+    w = W.decode_gemv(M, K=K, N=N, seed=M * 7 + K)
+    z = (np.arange(N, dtype=np.int32) % 7) - 3
     run(w.A_bits, w.A, w.W, w.scale, z, torch.float32)
 
 
