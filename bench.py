@@ -698,6 +698,7 @@ def case_setups(q, torch, peaks):
             "a8w8_acc_4096x4096x4096_bf16_b_trans": a8w8_acc(4096, 4096, 4096, True),
             "a8w8_acc_decode_M1_8192x28672_b_trans": a8w8_acc(1, 8192, 28672, True),
             "a8w8_acc_decode_M1_8192x28672": a8w8_acc(1, 8192, 28672, False),
+            "a8w8_acc_decode_M8_8192x28672_b_trans": a8w8_acc(8, 8192, 28672, True),
             "a8w8_acc_decode_M16_8192x28672_b_trans": a8w8_acc(16, 8192, 28672, True),
             "dql_matmul_dequant_fused_8192x4096x11008": dq_chain,
             "dql_matmul_dequant_fused_packed_8192x4096x11008": dq_chain_packed,
@@ -710,7 +711,8 @@ def case_setups(q, torch, peaks):
 SECONDARY = ["a8w8_4096x4096x4096_bf16_single_pass", "w8_prefill_bf16_4096x8192x28672",
              "a8w8_acc_4096x4096x4096_bf16", "a8w8_acc_4096x4096x4096_bf16_b_trans",
              "a8w8_acc_decode_M1_8192x28672_b_trans", "a8w8_acc_decode_M1_8192x28672",
-             "a8w8_acc_decode_M16_8192x28672_b_trans", "conv_integer_3x3_8x256x56x56",
+             "a8w8_acc_decode_M8_8192x28672_b_trans", "a8w8_acc_decode_M16_8192x28672_b_trans",
+             "conv_integer_3x3_8x256x56x56",
              "conv_integer_1d_k3_4x512x3000", "dql_matmul_dequant_fused_8192x4096x11008",
              "dql_matmul_dequant_fused_packed_8192x4096x11008",
              "w8_dequant_f32_64x256x192", "dql_8192x4096", "matmul_integer_8192x4096x11008",

@@ -19,9 +19,13 @@ KERNEL = "f16_prepass+gemm_tc05_pair_f16ops_a8w8_acc"
 
 
 def expected_kernel(M, K, N, b_trans):
-    """Decode shapes (M <= 16) whose rows suit the weight-streaming kernels take them."""
+    """Decode shapes (M <= 16) whose rows suit the weight-streaming kernels
+    take them: with B stored [N,K], up to 3 rows on dp4a, 4..16 rows on the
+    tensor cores."""
     if 1 <= M <= 16 and (K % 16 == 0 if b_trans else (K % 4 == 0 and N % 4 == 0)):
-        return "gemv_acc_a8w8_kmajor" if b_trans else "gemv_acc_a8w8_nmajor"
+        if b_trans:
+            return "gemv_acc_a8w8_kmajor" if M < 4 else "gemv_acc_prep+gemv_acc_a8w8_kmajor_tc"
+        return "gemv_acc_a8w8_nmajor"
     return KERNEL
 
 
@@ -158,7 +162,7 @@ def test_argument_errors():
 
 
 DECODE = [(1, 64, 256), (1, 4096, 1000), (2, 1040, 132), (5, 2048, 4), (8, 512, 520), (16, 1024, 264),
-          (1, 8192, 4100)]
+          (1, 8192, 4100), (9, 3088, 72), (16, 16, 100), (12, 4096, 2048)]
 
 
 @pytest.mark.parametrize("M,K,N", DECODE)
@@ -194,3 +198,20 @@ def test_decode_wraps_and_optional_operands(b_trans):
                           out_dtype=None) is None
     q.check_device_error()
     assert_equal(host(acc3), want_acc(w.acc_in, A, B), "decode, acc_out only")
+
+
+@pytest.mark.parametrize("M", [4, 8, 16])
+def test_decode_tensor_core_route_at_the_exactness_edge(M):
+    """Every product -128 * -128 = 2^14, so each 1024-k fp32 partial sum of the
+    tensor-core route is exactly 2^24; a mixed-sign half keeps the partials
+    near the edge with both signs. Bit-exact against the oracle."""
+    K, N = 4096, 256
+    w = W.a8w8_acc(M, K, N, seed=M, b_trans=True, acc_bound=2**31)
+    w.A[...] = -128
+    w.B[...] = -128
+    w.B[N // 2:, ::2] = 127   # columns of B stored [N,K]: alternate signs along k in the upper half
+    A, B = logical(w)
+    C, acc = run(w, "f32")
+    assert q.last_kernel() == "gemv_acc_prep+gemv_acc_a8w8_kmajor_tc"
+    assert_equal(acc, want_acc(w.acc_in, A, B), f"tensor-core decode accumulator M={M}")
+    assert_equal(C, O.a8w8_dequant_acc(w.acc_in, A, B, w.act_scale, w.weight_scale, "f32"), f"M={M}")

@@ -45,6 +45,23 @@ def test_a8w8_4096(workspace, kernel):
     assert_equal(got[rows], want, "a8w8 4096^3 sampled rows")
 
 
+def test_a8w8_acc_decode_M16_8192x28672_b_trans():
+    """16 rows on the tensor-core route at the decode size: 1024 sampled
+    columns x all rows, bit-exact."""
+    w = W.a8w8_acc(16, 8192, 28672, seed=0, b_trans=True)
+    acc = torch.empty((16, 28672), dtype=torch.int32, device="cuda")
+    C = q.qmm_a8w8_acc(dev(w.A), dev(w.B), dev(w.act_scale), dev(w.weight_scale), acc_in=dev(w.acc_in),
+                       acc_out=acc, b_trans=True, out_dtype=torch.bfloat16)
+    q.check_device_error()
+    assert q.last_kernel() == "gemv_acc_prep+gemv_acc_a8w8_kmajor_tc"
+    cols = np.sort(np.random.default_rng(16).choice(28672, 1024, replace=False))
+    B = np.ascontiguousarray(w.B[cols].T)   # the sampled columns of the logical [K, N] weight
+    want = O.a8w8_dequant_acc(w.acc_in[:, cols], w.A, B, w.act_scale, w.weight_scale[cols], "bf16")
+    assert_equal(host(C)[:, cols], want, "decode accumulating A8W8, M = 16, sampled columns")
+    want_acc = O.wrap_int32(w.acc_in[:, cols].astype(np.int64) + O.a8w8_acc(w.A, B).astype(np.int64))
+    assert_equal(host(acc)[:, cols], want_acc, "decode accumulator, M = 16, sampled columns")
+
+
 @pytest.mark.parametrize("b_trans", [False, True])
 def test_a8w8_acc_decode_M1_8192x28672(b_trans):
     w = W.a8w8_acc(1, 8192, 28672, seed=0, b_trans=b_trans)
