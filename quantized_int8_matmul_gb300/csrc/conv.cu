@@ -341,45 +341,101 @@ __device__ __forceinline__ void conv_w16_elements(const ConvW16& a, long long fi
   }
 }
 
-// One CTA per 64 pixels x 64 channels of one image, transposed through shared
-// memory: reads 64 channel rows of 64 bytes, writes 64 pixel rows of 64 fp16.
-// The CTAs of the last z slice (blockIdx.z == Nb) instead convert the weight,
-// w_per elements each, so both operands take one launch.
+// Rows (channels) 4i..4i+3 of four consecutive pixels, one word per row ->
+// one word per pixel holding its four channels (byte i = row i).
+__device__ __forceinline__ void transpose4x4(const uint32_t (&r)[4], uint32_t (&c)[4]) {
+  const uint32_t t0 = prmt(r[0], r[1], 0x5140u), t1 = prmt(r[0], r[1], 0x7362u);
+  const uint32_t t2 = prmt(r[2], r[3], 0x5140u), t3 = prmt(r[2], r[3], 0x7362u);
+  c[0] = prmt(t0, t2, 0x5410u);
+  c[1] = prmt(t0, t2, 0x7632u);
+  c[2] = prmt(t1, t3, 0x5410u);
+  c[3] = prmt(t1, t3, 0x7632u);
+}
+
+// Four bytes (channels) minus the zero point as two exact fp16 pairs: each
+// byte, biased to unsigned, goes into the low mantissa bits of 1024 (ulp 1)
+// and 1024 + bias + zp is subtracted (every value involved is an integer
+// below 2048, so the subtraction is exact).
+template <bool U>
+__device__ __forceinline__ void shifted_half4(uint32_t w, __half2 off, uint32_t& lo, uint32_t& hi) {
+  const uint32_t u = U ? w : (w ^ 0x80808080u);
+  const uint32_t l = prmt(u, 0x64646464u, 0x4140u), h = prmt(u, 0x64646464u, 0x4342u);
+  const __half2 a = __hsub2(*reinterpret_cast<const __half2*>(&l), off);
+  const __half2 b = __hsub2(*reinterpret_cast<const __half2*>(&h), off);
+  lo = *reinterpret_cast<const uint32_t*>(&a);
+  hi = *reinterpret_cast<const uint32_t*>(&b);
+}
+
+constexpr int kXPix = 256;              // pixels per CTA of conv_x16_kernel
+constexpr int kXPitch = kXPix + 4;      // shared row pitch (65 words): consecutive rows one bank apart
+
+// One CTA per 256 pixels x 64 channels of one image: the channel rows come in
+// with 16-byte loads into shared memory; each thread then takes a 4-pixel x
+// 8-channel block (eight 32-bit reads, conflict-free), transposes it in
+// registers and writes each pixel's 8 shifted channels as one 16-byte store,
+// four lanes covering 32 channels of a pixel (64 contiguous bytes). The CTAs
+// of the z slices from Nb on instead convert the weight, w_per elements each,
+// so both operands take one launch.
 template <bool U, bool WU>
 __global__ void __launch_bounds__(kThreads) conv_x16_kernel(const uint8_t* __restrict__ x, int C, int HW, int Nb,
                                                             const void* xzp, __half* __restrict__ x16, bool vec,
                                                             const ConvW16 wa, long long w_per) {
   asm volatile("griddepcontrol.launch_dependents;");   // a dependent GEMM may start its prologue
-  if ((int)blockIdx.z == Nb) {
-    conv_w16_elements<WU>(wa, ((long long)blockIdx.y * gridDim.x + blockIdx.x) * w_per, w_per);
+  if ((int)blockIdx.z >= Nb) {
+    const long long cta = ((long long)(blockIdx.z - Nb) * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+    conv_w16_elements<WU>(wa, cta * w_per, w_per);
     return;
   }
-  __shared__ uint8_t tile[64][64 + 16];
-  const int p0 = blockIdx.x * 64, c0 = blockIdx.y * 64, n = blockIdx.z;
-  const int zp = xzp ? zp_value<U>(xzp, 0) : 0;
+  __shared__ __align__(16) uint8_t tile[64][kXPitch];
+  const int p0 = blockIdx.x * kXPix, c0 = blockIdx.y * 64, n = blockIdx.z;
+  const int tid = threadIdx.x;
   {
-    const int lc = threadIdx.x >> 2, lp = (threadIdx.x & 3) * 16;
-    const uint8_t* src = x + ((size_t)n * C + c0 + lc) * HW + p0 + lp;
-    if (vec && p0 + lp + 16 <= HW) {
-      const uint4 v = ldg_nc_v4(src);
-      *reinterpret_cast<uint4*>(&tile[lc][lp]) = v;
-    } else {
-      for (int i = 0; i < 16; ++i) tile[lc][lp + i] = (p0 + lp + i < HW) ? src[i] : (uint8_t)0;
+    const int col = (tid & 15) * 16;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int row = (tid >> 4) + 16 * j;
+      const uint8_t* src = x + ((size_t)n * C + c0 + row) * HW + p0 + col;
+      uint32_t* d = reinterpret_cast<uint32_t*>(&tile[row][col]);
+      if (vec && p0 + col + 16 <= HW) {
+        const uint4 v = ldg_nc_v4(src);
+        d[0] = v.x;
+        d[1] = v.y;
+        d[2] = v.z;
+        d[3] = v.w;
+      } else {
+        for (int i = 0; i < 16; ++i) tile[row][col + i] = (p0 + col + i < HW) ? src[i] : (uint8_t)0;
+      }
     }
   }
   __syncthreads();
-  const int pp = threadIdx.x >> 2, cc = (threadIdx.x & 3) * 16;
-  if (p0 + pp < HW) {
-    uint32_t h[8];
+  const int zp = xzp ? zp_value<U>(xzp, 0) : 0;
+  const __half off = __int2half_rn((U ? 1024 : 1152) + zp);
+  const __half2 off2 = __halves2half2(off, off);
+  const int lane = tid & 31, warp = tid >> 5;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const __half2 v = __halves2half2(__int2half_rn(byte_value<U>(tile[cc + 2 * i][pp]) - zp),
-                                       __int2half_rn(byte_value<U>(tile[cc + 2 * i + 1][pp]) - zp));
-      h[i] = *reinterpret_cast<const uint32_t*>(&v);
+  for (int job = 0; job < 2; ++job) {
+    // a warp step: 4 channel octets x 8 pixel quads; with the 65-word row pitch
+    // lane (co, pq) reads bank 8 (co mod 4) + pq (+ const): all 32 distinct
+    const int co = 4 * job + (lane & 3);   // channels 8 co .. 8 co + 7 of the block
+    const int pq = 8 * warp + (lane >> 2);   // pixels 4 pq .. 4 pq + 3 of the tile
+    uint32_t r0[4], r1[4], c0w[4], c1w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      r0[i] = *reinterpret_cast<const uint32_t*>(&tile[8 * co + i][4 * pq]);
+      r1[i] = *reinterpret_cast<const uint32_t*>(&tile[8 * co + 4 + i][4 * pq]);
     }
-    __half* d = x16 + ((size_t)n * HW + p0 + pp) * C + c0 + cc;
-    st_v4(d, h[0], h[1], h[2], h[3]);
-    st_v4(d + 8, h[4], h[5], h[6], h[7]);
+    transpose4x4(r0, c0w);
+    transpose4x4(r1, c1w);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int p = p0 + 4 * pq + j;
+      if (p < HW) {
+        uint32_t h[4];
+        shifted_half4<U>(c0w[j], off2, h[0], h[1]);
+        shifted_half4<U>(c1w[j], off2, h[2], h[3]);
+        st_v4(x16 + ((size_t)n * HW + p) * C + c0 + 8 * co, h[0], h[1], h[2], h[3]);
+      }
+    }
   }
 }
 
@@ -392,10 +448,13 @@ cudaError_t launch_conv_operands(const void* x, bool xu, int Nb, int C, int HW, 
   if (Nb <= 0 || C <= 0 || HW <= 0 || M <= 0) return cudaSuccess;
   if (C % 64 != 0 || Nb >= 65535 || C / 64 > 65535) return cudaErrorInvalidValue;
   const bool vec = HW % 16 == 0 && (reinterpret_cast<uintptr_t>(x) % 16) == 0;
-  const dim3 grid((HW + 63) / 64, C / 64, Nb + 1);   // z == Nb: the weight, split over that slice's CTAs
+  // z >= Nb: the weight, over enough slices for at least 256 CTAs
+  const long long slice = (long long)((HW + kXPix - 1) / kXPix) * (C / 64);
+  const long long wz = std::max(1LL, std::min((256 + slice - 1) / slice, 65535LL - Nb));
+  const dim3 grid((HW + kXPix - 1) / kXPix, C / 64, (unsigned)(Nb + wz));
   const long long wtotal = (long long)M * kH * kW * Cg;
-  const long long slice = (long long)grid.x * grid.y;
-  const long long w_per = ((wtotal + slice - 1) / slice + kThreads - 1) / kThreads * kThreads;
+  const long long wctas = slice * wz;
+  const long long w_per = ((wtotal + wctas - 1) / wctas + kThreads - 1) / kThreads * kThreads;
   ConvW16 wa{static_cast<const uint8_t*>(w), M, Cg, kH, kW, wzp, wzp_count, w16};
   const uint8_t* p = static_cast<const uint8_t*>(x);
   if (xu && wu) conv_x16_kernel<true, true><<<grid, kThreads, 0, s>>>(p, C, HW, Nb, xzp, x16, vec, wa, w_per);
