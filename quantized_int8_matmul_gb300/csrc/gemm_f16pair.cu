@@ -38,9 +38,11 @@
 namespace qmm {
 namespace gemmf {
 
-// Pair tile: 256 rows x BN columns, BN = 256 or 224 (a template parameter,
-// chosen per problem by the launcher to fill the last wave of tiles). Each
-// CTA stages two 64-column B boxes (128 columns) and the MMA reads BN/2.
+// Pair tile: 256 rows x BN columns, BN = 256 or 224 (192 too for the
+// convolution; a template parameter, chosen per problem by the launcher to
+// fill the last wave of tiles). Each CTA stages two 64-column B boxes (128
+// columns) and the MMA reads BN/2; the convolution's im2col copy delivers
+// exactly BN/2 pixel rows.
 constexpr int BM = 128;
 constexpr int BMP = 2 * BM;
 constexpr int BN_MAX = 256;
@@ -635,7 +637,9 @@ __global__ void __launch_bounds__(NT, 1)
           continue;
         }
         const uint32_t bar = full_leader0 + (uint32_t)slot * 8u;
-        if (rank == 0) mbar_arrive_expect_tx(&sm.full[slot], 2u * STAGE_BYTES);
+        // the convolution's B box is BNH pixel rows of 128 bytes (the other
+        // instantiations always fill both 64-column boxes)
+        if (rank == 0) mbar_arrive_expect_tx(&sm.full[slot], 2u * (CV ? (uint32_t)(A_BYTES + 128 * BNH) : STAGE_BYTES));
         const uint32_t dst = sbase + (uint32_t)slot * STAGE_BYTES;
         const int ab = p.a_bstride ? (p.a_bmod ? tc.b % p.a_bmod : tc.b) : 0, bb = p.b_bstride ? tc.b : 0;
         const int nc = tc.n0 + (int)rank * BNH;
@@ -894,6 +898,26 @@ cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool
   return dispatch<256>(a, a_u8, b_u8, mmi, cs, c_vec, ta, tb, tc, s);
 }
 
+// The convolution's pair-tile width, by the cost model of choose_tile_width
+// over 256, 224 and 192 columns (output pixels): its problems are often a few
+// tiles short of whole waves (3x3 8x256x56x56: 104, 112 or 136 tiles on 76
+// SM pairs, all two waves; 192 makes them the shortest).
+int conv_tile_width(const GemmF16Args& a) {
+  const long long clusters = std::max(1, num_sms() / 2);
+  const long long m_tiles = (a.M + gemmf::BMP - 1) / gemmf::BMP;
+  int best = 256;
+  long long best_cost = -1;
+  for (int bn : {256, 224, 192}) {
+    const long long tiles = (long long)a.batch * m_tiles * ((a.N + bn - 1) / bn);
+    const long long cost = (tiles + clusters - 1) / clusters * (bn + 16);
+    if (best_cost < 0 || cost < best_cost) {
+      best = bn;
+      best_cost = cost;
+    }
+  }
+  return best;
+}
+
 cudaError_t launch_gemm_f16pair_conv(const GemmF16Args& a, const CUtensorMap& tx, cudaStream_t s,
                                      const char** kernel_name) {
   using namespace gemmf;
@@ -913,7 +937,12 @@ cudaError_t launch_gemm_f16pair_conv(const GemmF16Args& a, const CUtensorMap& tx
                    4ull * (uint64_t)a.N, 4ull * (uint64_t)a.M * (uint64_t)a.N, 16, 32, CU_TENSOR_MAP_SWIZZLE_64B);
   if (e != cudaSuccess) return e;
   *kernel_name = "gemm_tc05_pair_f16ops_conv_im2col";
-  return launch_one<256, false, false, true, false, false, false, true>(a, cs, c_vec, ta, tx, tc, s);
+  // the im2col map's pixel box is conv_tile_width(a) / 2 (the caller builds it)
+  switch (conv_tile_width(a)) {
+    case 192: return launch_one<192, false, false, true, false, false, false, true>(a, cs, c_vec, ta, tx, tc, s);
+    case 224: return launch_one<224, false, false, true, false, false, false, true>(a, cs, c_vec, ta, tx, tc, s);
+    default: return launch_one<256, false, false, true, false, false, false, true>(a, cs, c_vec, ta, tx, tc, s);
+  }
 }
 
 cudaError_t launch_gemm_w8_bf16pair(const GemmF16Args& a, int w_k, cudaStream_t s, const char** kernel_name) {

@@ -98,6 +98,9 @@ cudaError_t launch_gemm_f16pair(const GemmF16Args& a, bool a_u8, bool b_u8, bool
 // described by tx (rank 4, {C, W, H, N}, 64 channels x 128 pixels, 128-byte
 // swizzle), C int32 [N * G][Mg][P]; the operands already hold x - x_zp and
 // w - w_zp, so the epilogue stores the exact sums unchanged.
+// Pair-tile width (output pixels) the convolution launch uses for these
+// arguments: 256, 224 or 192. The im2col map's pixel box must be half of it.
+int conv_tile_width(const GemmF16Args& a);
 cudaError_t launch_gemm_f16pair_conv(const GemmF16Args& a, const CUtensorMap& tx, cudaStream_t s,
                                      const char** kernel_name);
 

@@ -1251,14 +1251,6 @@ qmm_status conv_integer(const void* x, int x_dtype, const void* w, int w_dtype, 
     const int Cg = (int)(C / group);
     cudaError_t e = launch_conv_operands(x, xu, (int)N, (int)C, (int)(H * W), x_zero_point, x16, w, wu, (int)M, Cg,
                                          (int)kH, (int)kW, w_zero_point, (int)w_zp_count, w16, s);
-    CUtensorMap tx{};
-    if (e == cudaSuccess) {
-      const uint64_t dims[4] = {(uint64_t)C, (uint64_t)W, (uint64_t)H, (uint64_t)N};
-      const uint64_t strides[3] = {(uint64_t)C * 2, (uint64_t)W * C * 2, (uint64_t)H * W * C * 2};
-      const uint32_t es[4] = {1u, (uint32_t)pl.sw, (uint32_t)pl.sh, 1u};
-      e = make_tmap_im2col(&tx, x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, dims, strides, pl.lower, pl.upper, 64, 128,
-                           es, CU_TENSOR_MAP_SWIZZLE_128B);
-    }
     GemmF16Args f{};
     f.A16 = w16;
     f.a_bstride = group > 1 ? Mg * pl.Kg : 0;
@@ -1281,6 +1273,15 @@ qmm_status conv_integer(const void* x, int x_dtype, const void* w, int w_dtype, 
     f.cv_cb = Cg / 64;
     f.cv_G = (int)group;
     f.cv_Cg = Cg;
+    // each copy gathers the pixel rows of one CTA's half of the pair tile
+    CUtensorMap tx{};
+    if (e == cudaSuccess) {
+      const uint64_t dims[4] = {(uint64_t)C, (uint64_t)W, (uint64_t)H, (uint64_t)N};
+      const uint64_t strides[3] = {(uint64_t)C * 2, (uint64_t)W * C * 2, (uint64_t)H * W * C * 2};
+      const uint32_t es[4] = {1u, (uint32_t)pl.sw, (uint32_t)pl.sh, 1u};
+      e = make_tmap_im2col(&tx, x16, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, dims, strides, pl.lower, pl.upper, 64,
+                           (uint32_t)(conv_tile_width(f) / 2), es, CU_TENSOR_MAP_SWIZZLE_128B);
+    }
     const char* gname = "none";
     if (e == cudaSuccess) e = launch_gemm_f16pair_conv(f, tx, s, &gname);
     return finish_launch(e, "conv_f16_nhwc+gemm_tc05_pair_f16ops_conv_im2col");

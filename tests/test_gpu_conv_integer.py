@@ -99,6 +99,25 @@ def test_conv_integer_implicit_gemm_rank3(L, k, pads, stride, dil):
     assert_equal(got, want(c), f"implicit-GEMM rank-3 L={L} k={k}")
 
 
+# Batches sized so that, on a 152-SM GB300 (76 SM pairs), the pair-tile width
+# chosen for the convolution is 256 (25 images of 768 output pixels: 75 tiles
+# of 256, one wave) and 224 (38 images of 448 pixels: 76 tiles of 224); the
+# small geometries above all take 192.
+WIDTH_GEOMETRIES = [
+    ((25, 64, 24, 32), (16, 64, 3, 3), [1, 1, 1, 1], [1, 1], [1, 1], 1),
+    ((38, 64, 16, 28), (16, 64, 3, 3), [1, 1, 1, 1], [1, 1], [1, 1], 1),
+]
+
+
+@pytest.mark.parametrize("geom", range(len(WIDTH_GEOMETRIES)))
+def test_conv_integer_implicit_gemm_tile_widths(geom):
+    xs, ws, pads, strides, dils, group = WIDTH_GEOMETRIES[geom]
+    c = W.conv_integer_case(xs, ws, pads, strides, dils, group, seed=geom + 77)
+    got = run(c)
+    assert q.last_kernel() == IM2COL
+    assert_equal(got, want(c), f"implicit-GEMM conv, tile-width geometry {geom}")
+
+
 def test_conv_integer_implicit_gemm_extremes_and_wrap():
     """Shifted operands at the extremes (255 - 0 and -128 - 127): each exact
     fp32 chunk of 256 taps sums to 256 * 65025 < 2^24; and a reduction long
