@@ -374,8 +374,8 @@ constexpr int kXPitch = kXPix + 4;      // shared row pitch (65 words): consecut
 // 8-channel block (eight 32-bit reads, conflict-free), transposes it in
 // registers and writes each pixel's 8 shifted channels as one 16-byte store,
 // four lanes covering 32 channels of a pixel (64 contiguous bytes). The CTAs
-// of the z slices from Nb on instead convert the weight, w_per elements each,
-// so both operands take one launch.
+// of the z slices from Nb on instead convert the weight, w_per elements each
+// (at most two per thread), so both operands take one launch.
 template <bool U, bool WU>
 __global__ void __launch_bounds__(kThreads) conv_x16_kernel(const uint8_t* __restrict__ x, int C, int HW, int Nb,
                                                             const void* xzp, __half* __restrict__ x16, bool vec,
@@ -448,11 +448,14 @@ cudaError_t launch_conv_operands(const void* x, bool xu, int Nb, int C, int HW, 
   if (Nb <= 0 || C <= 0 || HW <= 0 || M <= 0) return cudaSuccess;
   if (C % 64 != 0 || Nb >= 65535 || C / 64 > 65535) return cudaErrorInvalidValue;
   const bool vec = HW % 16 == 0 && (reinterpret_cast<uintptr_t>(x) % 16) == 0;
-  // z >= Nb: the weight, over enough slices for at least 256 CTAs
+  // z >= Nb: the weight, over enough slices for at most two elements per
+  // thread (each is a gathered byte: a thread's loads would otherwise queue
+  // one DRAM round trip after another)
   const long long slice = (long long)((HW + kXPix - 1) / kXPix) * (C / 64);
-  const long long wz = std::max(1LL, std::min((256 + slice - 1) / slice, 65535LL - Nb));
-  const dim3 grid((HW + kXPix - 1) / kXPix, C / 64, (unsigned)(Nb + wz));
   const long long wtotal = (long long)M * kH * kW * Cg;
+  const long long wneed = (wtotal + 2LL * kThreads - 1) / (2LL * kThreads);   // CTAs at two elements per thread
+  const long long wz = std::max(1LL, std::min((wneed + slice - 1) / slice, 65535LL - Nb));
+  const dim3 grid((HW + kXPix - 1) / kXPix, C / 64, (unsigned)(Nb + wz));
   const long long wctas = slice * wz;
   const long long w_per = ((wtotal + wctas - 1) / wctas + kThreads - 1) / kThreads * kThreads;
   ConvW16 wa{static_cast<const uint8_t*>(w), M, Cg, kH, kW, wzp, wzp_count, w16};
