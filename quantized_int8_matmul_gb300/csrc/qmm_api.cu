@@ -1066,6 +1066,94 @@ qmm_status qmm_a8w8_host(const int8_t* hA, const int8_t* hB, int64_t M, int64_t 
   uint8_t* pbase = base + hp.off_pack;
   __half* a16 = reinterpret_cast<__half*>(pbase);
   __half* b16 = reinterpret_cast<__half*>(pbase + hp.pl.off_b);
+  if (M >= 512 && N >= 1024) {
+    // 2 x 2 blocks: A in two row panels and B in two column panels, so the
+    // first block's GEMM needs only a quarter of each operand and its rows of C
+    // go back while the remaining operands are still coming in (row panels
+    // alone wait for the whole of B first). Every block has a dense device
+    // buffer; B's column panels come in and C's blocks go out as pitched copies.
+    const int64_t M1 = std::min(M, ((M + 1) / 2 + 255) / 256 * 256);
+    const int64_t N1 = std::min(N, ((N + 1) / 2 + 255) / 256 * 256);
+    const int64_t r0s[2] = {0, M1}, rws[2] = {M1, M - M1}, c0s[2] = {0, N1}, cls[2] = {N1, N - N1};
+    auto c_block = [&](int i, int j) { return dC + (size_t)(r0s[i] * N + rws[i] * c0s[j]) * celem; };
+    const char* gname = "none";
+    const uint8_t* cB = static_cast<const uint8_t*>(static_cast<const void*>(hB));
+    e = cudaEventRecord(hpipe->start, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hpipe->h2d, hpipe->start, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hpipe->d2h, hpipe->start, 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(dW, h_weight_scale, (size_t)w_count * 4, cudaMemcpyHostToDevice, hpipe->h2d);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(dAct, h_act_scale, (size_t)act_count * 4, cudaMemcpyHostToDevice, hpipe->h2d);
+    // in: A0, B0, B1, A1 (events in[0], in[2], in[3], in[1])
+    auto copy_a = [&](int i) {
+      cudaError_t x = cudaMemcpyAsync(dA + r0s[i] * K, cA + r0s[i] * K, (size_t)rws[i] * K, cudaMemcpyHostToDevice,
+                                      hpipe->h2d);
+      return x == cudaSuccess ? cudaEventRecord(hpipe->in[i], hpipe->h2d) : x;
+    };
+    auto copy_b = [&](int j) {
+      cudaError_t x = cudaMemcpy2DAsync(dB + K * c0s[j], (size_t)cls[j], cB + c0s[j], (size_t)N, (size_t)cls[j],
+                                        (size_t)K, cudaMemcpyHostToDevice, hpipe->h2d);
+      return x == cudaSuccess ? cudaEventRecord(hpipe->in[2 + j], hpipe->h2d) : x;
+    };
+    if (e == cudaSuccess) e = copy_a(0);
+    if (e == cudaSuccess) e = copy_b(0);
+    if (e == cudaSuccess) e = copy_b(1);
+    if (e == cudaSuccess) e = copy_a(1);
+    // on the caller's stream, in the order the operands arrive: each panel's
+    // conversion, each block's GEMM, and each block of C back on the second
+    // copy stream as soon as it is written
+    auto convert_a = [&](int i) {
+      cudaError_t x = cudaStreamWaitEvent(s, hpipe->in[i], 0);
+      return x == cudaSuccess ? launch_convert_bulk(dA + r0s[i] * K, false, a16 + r0s[i] * K, rws[i] * K, nullptr,
+                                                    false, nullptr, 0, err, s)
+                              : x;
+    };
+    auto convert_b = [&](int j) {
+      cudaError_t x = cudaStreamWaitEvent(s, hpipe->in[2 + j], 0);
+      return x == cudaSuccess ? launch_convert_bulk(nullptr, false, nullptr, 0, dB + K * c0s[j], false,
+                                                    b16 + K * c0s[j], K * cls[j], err, s)
+                              : x;
+    };
+    int nb = 0;
+    auto block = [&](int i, int j) {
+      GemmF16Args f{};
+      f.A16 = a16 + r0s[i] * K;
+      f.B16 = b16 + K * c0s[j];
+      f.batch = 1;
+      f.M = (int)rws[i];
+      f.K = (int)K;
+      f.N = (int)cls[j];
+      f.C = c_block(i, j);
+      f.c_f32 = c_dtype == QMM_F32;
+      f.act_scale = dAct + (act_count == 1 ? 0 : r0s[i]);
+      f.act_count = (int)act_count;
+      f.w_scale = dW + (w_count == 1 ? 0 : c0s[j]);
+      f.w_count = (int)w_count;
+      f.zp_row_mod = (int)rws[i];
+      f.err = err;
+      cudaError_t x = launch_gemm_f16pair(f, false, false, false, chunk_k_for(false, false), s, &gname);
+      if (x == cudaSuccess) x = cudaEventRecord(hpipe->out[nb], s);
+      if (x == cudaSuccess) x = cudaStreamWaitEvent(hpipe->d2h, hpipe->out[nb], 0);
+      ++nb;
+      if (x == cudaSuccess)
+        x = cudaMemcpy2DAsync(cC + (size_t)(r0s[i] * N + c0s[j]) * celem, (size_t)N * celem, c_block(i, j),
+                              (size_t)cls[j] * celem, (size_t)cls[j] * celem, (size_t)rws[i], cudaMemcpyDeviceToHost,
+                              hpipe->d2h);
+      return x;
+    };
+    if (e == cudaSuccess) e = convert_a(0);
+    if (e == cudaSuccess) e = convert_b(0);
+    if (e == cudaSuccess) e = block(0, 0);
+    if (e == cudaSuccess) e = convert_b(1);
+    if (e == cudaSuccess) e = block(0, 1);
+    if (e == cudaSuccess) e = convert_a(1);
+    if (e == cudaSuccess) e = block(1, 0);
+    if (e == cudaSuccess) e = block(1, 1);
+    if (e == cudaSuccess) e = cudaEventRecord(hpipe->done, hpipe->d2h);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hpipe->done, 0);
+    return finish_launch(e, "h2d_pipelined+f16_prepass+gemm_tc05_pair_f16ops_a8w8");
+  }
   // copies in, on the copy stream after the caller's earlier work: B and the
   // scales, then A panel by panel
   e = cudaEventRecord(hpipe->start, s);

@@ -1,8 +1,9 @@
-"""A8W8 from host buffers (qmm_a8w8_host): the row panels' copies in and out
-overlap the GEMMs of the other panels; the result must be bit-identical to the
-oracle and to the device-pointer call, on several panels with a ragged last
-one, both output types, scalar scales, pageable host memory, back-to-back calls
-on one workspace, and the shapes outside the two-pass path."""
+"""A8W8 from host buffers (qmm_a8w8_host): the copies in and out overlap the
+GEMMs (2 x 2 blocks from 512 rows and 1024 columns on, with pitched copies of
+B's column panels and C's blocks; row panels below that); the result must be
+bit-identical to the oracle and to the device-pointer call, with ragged last
+panels, both output types, scalar scales, pageable host memory, back-to-back
+calls on one workspace, and the shapes outside the two-pass path."""
 import numpy as np
 import pytest
 import torch
@@ -30,7 +31,8 @@ def host_call(w, out, pinned=True, workspace="auto", act=None, wsc=None):
     return host(C)
 
 
-@pytest.mark.parametrize("M,K,N", [(2600, 128, 4096), (1000, 1040, 1008), (256, 64, 256)])
+@pytest.mark.parametrize("M,K,N", [(2600, 128, 4096), (1000, 1040, 1008), (256, 64, 256), (1000, 1040, 1040),
+                                   (600, 2064, 1024)])
 @pytest.mark.parametrize("out", ["bf16", "f32"])
 def test_host_pipeline_matches_oracle(M, K, N, out):
     w = W.a8w8(M, K, N, seed=M + K + N)
