@@ -74,14 +74,20 @@ def test_a8w8_acc_decode_M1_8192x28672(b_trans):
     assert_equal(host(C), want, "decode accumulating A8W8, M = 1")
 
 
-def test_dynamic_quantize_matmul_8192x4096x11008():
+@pytest.mark.parametrize("packed", [False, True])
+def test_dynamic_quantize_matmul_8192x4096x11008(packed):
     w = W.dql_matmul_integer_8192x4096x11008()
     rng = np.random.default_rng(9)
     w_scale = rng.uniform(0.001, 0.01, 11008).astype(np.float32)
     bias = rng.standard_normal(11008).astype(np.float32)
-    C, ys, yz = q.dynamic_quantize_matmul(dev(w.x), dev(w.B), dev(w_scale), dev(w.b_zp), dev(bias))
+    if packed:   # the weight converted once, then the chain on it
+        pw = q.dynamic_quantize_matmul_pack_weight(dev(w.B))
+        C, ys, yz = q.dynamic_quantize_matmul_packed(dev(w.x), pw, dev(w_scale), dev(w.b_zp), dev(bias))
+    else:
+        C, ys, yz = q.dynamic_quantize_matmul(dev(w.x), dev(w.B), dev(w_scale), dev(w.b_zp), dev(bias))
     q.check_device_error()
-    assert q.last_kernel() == "dql_f16+gemm_tc05_pair_f16ops_matmul_integer_dequant"
+    assert q.last_kernel() == ("dql_f16+gemm_tc05_pair_f16ops_matmul_integer_dequant"
+                               + ("_packed" if packed else ""))
     rows = sample(8192, 24, 5)
     rows[:2] = [0, 8191]
     want, wys, wyz = O.dynamic_quantize_matmul(w.x, w.B, w_scale, w.b_zp, bias, rows=rows)
