@@ -192,15 +192,17 @@ qmm_status qmm_a8w8_packed(int64_t M, int64_t K, int64_t N, const float* act_sca
  * Host buffers should be page-locked (cudaHostAlloc / cudaHostRegister) for
  * the copies to run asynchronously; they must stay valid and unchanged until
  * the work on `stream` completes (hC is written by then).
- * Where the two-pass path applies (qmm_a8w8_workspace_bytes(M, K, N) > 0), A
- * is processed in row panels sized so each panel's pair tiles fill whole
- * waves of the GPU: B, the scales and A's panels are copied in on one internal
- * copy stream, each panel's pre-pass and GEMM run on `stream` as soon as its
- * rows have arrived, and each panel's rows of C are copied back on a second
- * internal stream as soon as they are written, so the copies in both
- * directions overlap the GEMMs of the other panels. Elsewhere the call copies
- * in, runs qmm_a8w8 and copies out on `stream`. Calls on one device enqueue one
- * at a time (the internal streams and events are shared).
+ * Where the two-pass path applies (qmm_a8w8_workspace_bytes(M, K, N) > 0), the
+ * copies in run on one internal copy stream, the pre-passes and GEMMs on
+ * `stream` as soon as their operands have arrived, and the copies of C back on
+ * a second internal stream as soon as each part is written, so the copies in
+ * both directions overlap the GEMMs. From 512 rows and 1024 columns on the
+ * work is 2 x 2 blocks (A in two row panels, B in two column panels copied as
+ * pitched panels; each block's C goes back as a pitched copy), so the first
+ * GEMM needs a quarter of each operand; below that, all of B and then A's row
+ * panels, sized so each panel's pair tiles fill whole waves. Elsewhere the
+ * call copies in, runs qmm_a8w8 and copies out on `stream`. Calls on one
+ * device enqueue one at a time (the internal streams and events are shared).
  * Errors: as qmm_a8w8_ws, plus QMM_ERR_CUDA when a copy cannot be enqueued.
  */
 size_t qmm_a8w8_host_workspace_bytes(int64_t M, int64_t K, int64_t N, int64_t act_count, int64_t w_count,
