@@ -97,11 +97,14 @@ def test_packed_decode_scalar_scale_and_row_range():
 
 
 @pytest.mark.parametrize("M", [1, 4, 16])
-def test_packed_decode_8192x28672(M):
-    """The decode workload at full size, 1024 sampled columns x all rows."""
+@pytest.mark.parametrize("zp", [False, True])
+def test_packed_decode_8192x28672(M, zp):
+    """The decode workload at full size, 1024 sampled columns x all rows; with
+    a per-column zero point too (the row sums come from one more MMA per step)."""
     w = W.decode_gemv(M)
     cols = np.random.default_rng(M).choice(28672, 1024, replace=False)
-    run(w.A_bits, w.A, w.W, w.scale, None, torch.bfloat16, cols=cols)
+    z = ((np.arange(28672, dtype=np.int32) * 7) % 15 - 7) if zp else None
+    run(w.A_bits, w.A, w.W, w.scale, z, torch.bfloat16, cols=cols)
 
 
 def test_packed_decode_is_deterministic_and_reuses_the_pack():
